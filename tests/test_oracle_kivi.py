@@ -1,0 +1,148 @@
+"""Pins of the oracle's KIVI quantiser and packing to what the pages and the
+arithmetic fix (no GPU)."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import kivi
+
+BITS = (2, 4, 8)
+
+
+def _fp16_values(rng, shape, scale=1.0):
+    return (rng.standard_normal(shape) * scale).astype(np.float16).astype(np.float32)
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_error_bound_half_scale(bits):
+    """|x - deq(q(x))| <= scale/2 per element (up to float32 rounding)."""
+    rng = np.random.default_rng(bits)
+    x = _fp16_values(rng, (64, 8, 32))
+    x[:, 3, :] *= 40.0                                        # outlier slices
+    q, s, z = kivi.quantize_slices(x, bits)
+    deq = kivi.dequantize_slices(q, s, z)
+    s32 = s.astype(np.float32)[..., None]
+    err = np.abs(x - deq)
+    slack = 4 * np.spacing(np.abs(x) + np.abs(z.astype(np.float32)[..., None]))
+    assert np.all(err <= 0.5 * s32 * (1 + 2.0 ** -9) + slack)
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_code_is_nearest_level_brute_force(bits):
+    """Each code minimises |x - (z + q s)| over all 2^b codes in exact
+    arithmetic (half-way cases go to the even code); fp32 may only differ on
+    quotients within 1e-5 of a half-integer."""
+    rng = np.random.default_rng(100 + bits)
+    x = _fp16_values(rng, (200, 32))
+    q, s, z = kivi.quantize_slices(x, bits)
+    lb = (1 << bits) - 1
+    checked = 0
+    for i in range(x.shape[0]):
+        S = Fraction(float(s[i]))
+        Z = Fraction(float(z[i]))
+        for j in range(32):
+            t = (Fraction(float(x[i, j])) - Z) / S
+            best = min(range(lb + 1), key=lambda c: (abs(t - c), c % 2))
+            frac = t - int(t)
+            if abs(frac - Fraction(1, 2)) < Fraction(1, 100000):
+                continue
+            assert q[i, j] == best, (i, j, float(t))
+            checked += 1
+    assert checked > 0.99 * x.size
+
+
+def test_exact_half_way_goes_to_even():
+    """x - z = (k + 1/2) s exactly: the code is the even neighbour."""
+    s = 0.25
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0] = 0.0                 # min -> zero = 0
+    x[0, 1] = 0.75                # max -> range 0.75 over 3 levels: s = 0.25
+    x[0, 2] = 0.125               # t = 0.5 -> 0
+    x[0, 3] = 0.375               # t = 1.5 -> 2
+    x[0, 4] = 0.625               # t = 2.5 -> 2
+    q, sh, zh = kivi.quantize_slices(x, 2)
+    assert float(sh[0]) == s and float(zh[0]) == 0.0
+    assert list(q[0, :5]) == [0, 3, 0, 2, 2]
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_constant_slice_eps(bits):
+    """A constant slice (P1 bug class 1) keeps a nonzero scale and round-trips."""
+    x = np.full((3, 32), 0.7109375, np.float32)     # fp16-exact
+    q, s, z = kivi.quantize_slices(x, bits)
+    assert np.all(q == 0)
+    assert np.all(s.astype(np.float32) > 0)
+    assert float(s[0]) == float(np.float16(np.float32(1e-5)))
+    assert np.array_equal(kivi.dequantize_slices(q, s, z), x)
+
+
+def test_tiny_range_no_nan():
+    """A slice whose range is below eps (P1 bug class 2): finite, within s/2."""
+    x = (np.float32(1.0) + np.arange(32, dtype=np.float32) * np.float32(2.0 ** -10)).astype(np.float32)
+    x = x.astype(np.float16).astype(np.float32)[None]
+    q, s, z = kivi.quantize_slices(x, 2)
+    d = kivi.dequantize_slices(q, s, z)
+    assert np.all(np.isfinite(d))
+    assert np.all(np.abs(d - x) <= 0.5 * s.astype(np.float32)[..., None] + 1e-6)
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_grid_values_round_trip_and_end_codes(bits):
+    """Values on the grid z + k s (both ends present) give codes k exactly and
+    dequantise exactly; the clamp reaches 0 and 2^b - 1 (P1 bug class 3)."""
+    lb = (1 << bits) - 1
+    rng = np.random.default_rng(7)
+    k = rng.integers(0, lb + 1, size=(16, 32))
+    k[:, 0] = 0
+    k[:, 1] = lb
+    s, z = 2.0 ** -3, -1.0
+    x = (z + k * s).astype(np.float32)
+    q, sh, zh = kivi.quantize_slices(x, bits)
+    assert np.array_equal(q, k.astype(np.uint8))
+    assert np.array_equal(kivi.dequantize_slices(q, sh, zh), x)
+    assert q.min() == 0 and q.max() == lb
+
+
+def test_nan_rejected():
+    x = np.zeros((1, 32), np.float32)
+    x[0, 5] = np.nan
+    with pytest.raises(ValueError):
+        kivi.quantize_slices(x, 4)
+
+
+def test_k_groups_per_channel_v_per_token_axes():
+    """K: one scale per channel over the 32 tokens; V: one per token per 32
+    channels (the KIVI placement)."""
+    rng = np.random.default_rng(3)
+    k = _fp16_values(rng, (32, 64))
+    k[:, 5] *= 100.0                          # channel outlier -> only channel 5's scale
+    q, s, z = kivi.quantize_k_group(k, 2)
+    assert s.shape == (64,) and q.shape == (32, 64)
+    big = float(s[5])
+    assert all(float(s[c]) < big / 10 for c in range(64) if c != 5)
+    v = _fp16_values(rng, (32, 64))
+    v[7, :32] *= 100.0                        # token outlier in channel group 0
+    qv, sv, zv = kivi.quantize_v_rows(v, 4)
+    assert sv.shape == (32, 2)
+    assert float(sv[7, 0]) > 10 * max(float(sv[t, 0]) for t in range(32) if t != 7)
+    assert float(sv[7, 1]) < 10 * float(np.median(sv[:, 1].astype(np.float32)))
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_pack_unpack_every_level(bits):
+    per = 8 // bits
+    lb = (1 << bits) - 1
+    codes = np.array([(i * 7 + 3) % (lb + 1) for i in range(4 * 256)], np.uint8).reshape(4, 256)
+    codes[0, : lb + 1] = np.arange(lb + 1)
+    packed = kivi.pack_codes(codes, bits)
+    assert packed.shape == (4, codes.shape[1] * bits // 8)
+    assert np.array_equal(kivi.unpack_codes(packed, bits), codes)
+
+
+def test_pack_layout_v0_in_low_bits():
+    """Foundry spec, "Step 3: Packing": [v0:2][v1:2][v2:2][v3:2] and
+    [v0:4][v1:4], read with v0 in the least-significant bits."""
+    assert kivi.pack_codes(np.array([[1, 2, 3, 0]], np.uint8), 2)[0, 0] == 0b00111001
+    assert kivi.pack_codes(np.array([[0xA, 0x5]], np.uint8), 4)[0, 0] == 0x5A
+    assert list(kivi.pack_codes(np.array([[7, 200]], np.uint8), 8)[0]) == [7, 200]
