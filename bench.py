@@ -1,0 +1,380 @@
+"""Benchmark of the quantised KV-cache decode step on GB300.
+
+Workload: Llama-3-8B-shaped decode attention, one layer (reported x32 for the
+model step): batch 16, 32 query heads, 8 KV heads, head_dim 128, context
+32768, bf16 activations, K 2-bit per channel / V 4-bit per token in 32-token
+/ 32-channel groups, fp16 residual 32, sinks 4 + window 128. K channel (h, c)
+is scaled by a seeded exp(U(0, ln 75)); V, q ~ N(0, 1). Inputs are synthetic
+and generated on the device; the cache (543 MB per layer step) is larger
+than L2, so no flush is needed between steps.
+
+One step = kv_append of one new token (K, V) + kv_decode_attn, the whole
+hot path of a decode step for one layer. Reported:
+  value      effective bandwidth over the step's algorithmic bytes (GB/s)
+  roofline   the split-KV decode kernel alone: algorithmic bytes / its
+             average duration (CUDA events the library records on the
+             launching stream), against the measured HBM peak
+  e2e        the same step through the public API with host buffers
+             (pinned host -> device inputs, device -> host output)
+  cpu_baseline  the CPU oracle timed on a bounded sample of the workload
+
+--impl reference times the CPU oracle (the reference arm) on the same
+workload, a bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Quantised-KV decode attn: HBM GB/s (% of peak), µs/step; append tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = dict(batch=16, n_q_heads=32, n_kv_heads=8, head_dim=128, context=32768, act_dtype="bf16",
+                k_bits=2, v_bits=4, n_sink=4, window=128, layers_reported=32)
+WORKLOAD_NAME = ("llama8b decode attention: B16 Hq32 Hkv8 D128 context 32768 bf16, "
+                 "KIVI K2/V4 groups 32, residual 32, sinks 4 + window 128; one layer timed, x32 reported")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_inputs(torch, w, seed, n_tokens, device):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    B, H, D = w["batch"], w["n_kv_heads"], w["head_dim"]
+    fac = torch.exp(torch.rand((H, D), generator=g, device=device) * math.log(75.0))
+    k = (torch.randn((B, H, n_tokens, D), generator=g, device=device) * fac[None, :, None, :]).to(torch.bfloat16)
+    v = torch.randn((B, H, n_tokens, D), generator=g, device=device).to(torch.bfloat16)
+    return k, v, fac
+
+
+def algorithmic_bytes(stats, w):
+    """Bytes the decode must read: every code, scale, zero and exact row it
+    attends to, plus q in and the fp32 output."""
+    B, Hq, D = w["batch"], w["n_q_heads"], w["head_dim"]
+    cache = (stats["code_bytes"] + stats["kmeta_bytes"] + stats["vmeta_bytes"] + stats["sink_bytes"]
+             + stats["tail_bytes"])
+    return cache + B * Hq * D * 2 + B * Hq * D * 4
+
+
+def append_bytes(w):
+    """kv_append of one token: K and V read, written to the exact tail."""
+    B, H, D = w["batch"], w["n_kv_heads"], w["head_dim"]
+    return 2 * (B * H * D * 2) * 2
+
+
+def cpu_baseline(n_pairs=2, seed=7):
+    """The oracle as it stands, on a bounded sample: n_pairs (b, kv head)
+    units of the workload (one KV head with its 4 query heads, 32767-token
+    prefill + 1 append), timing the decode attention. Returns GB/s over the
+    sample's algorithmic bytes."""
+    import numpy as np
+    from oracle import CacheConfig, OracleCache
+    w = WORKLOAD
+    L = w["context"]
+    total_bytes, total_t = 0, 0.0
+    for i in range(n_pairs):
+        rng = np.random.default_rng(seed + i)
+        fac = np.exp(rng.uniform(0, math.log(75.0), size=w["head_dim"])).astype(np.float32)
+        k = (rng.standard_normal((1, 1, L, w["head_dim"]), dtype=np.float32) * fac)
+        v = rng.standard_normal((1, 1, L, w["head_dim"]), dtype=np.float32)
+        q = rng.standard_normal((1, 4, w["head_dim"]), dtype=np.float32)
+        import torch
+        rb = lambda x: torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+        k, v, q = rb(k), rb(v), rb(q)
+        oc = OracleCache(CacheConfig(n_layers=1, batch=1, n_kv_heads=1, n_q_heads=4, head_dim=w["head_dim"],
+                                     max_tokens=L + 64, k_bits=w["k_bits"], v_bits=w["v_bits"],
+                                     n_sink=w["n_sink"], window=w["window"], act_dtype="bf16"))
+        oc.prefill_quantize(0, k, v)
+        t0 = time.perf_counter()
+        oc.decode_attn(0, q)
+        total_t += time.perf_counter() - t0
+        s = oc.stats(0)
+        total_bytes += (s["code_bytes"] + s["kmeta_bytes"] + s["vmeta_bytes"] + s["sink_bytes"]
+                        + s["tail_bytes"] + 4 * w["head_dim"] * 2 + 4 * w["head_dim"] * 4)
+    return total_bytes / total_t / 1e9, total_t, n_pairs
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    steps_t = []
+    for s in range(args.warmup + args.steps):
+        gbs, t, n = cpu_baseline(n_pairs=1, seed=100 + s)
+        if s >= args.warmup:
+            steps_t.append((gbs, t))
+    value = statistics.mean(g for g, _ in steps_t)
+    ms = statistics.mean(t for _, t in steps_t) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME,
+                       "sample": "per step: one (sequence, KV head) unit with its 4 query heads, decode only"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "one (b, kv-head) unit per step, 32768-token context"},
+            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from bit_kv_cache_append_gb300 import binding
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+    w = WORKLOAD
+    L = w["context"]
+    n_steps_total = args.warmup + args.steps + 2
+    cache = binding.KVCache(device=dev, n_layers=1, batch=w["batch"], n_kv_heads=w["n_kv_heads"],
+                            n_q_heads=w["n_q_heads"], head_dim=w["head_dim"], max_tokens=L + 2 * n_steps_total + 64,
+                            k_bits=w["k_bits"], v_bits=w["v_bits"], n_sink=w["n_sink"], window=w["window"],
+                            act_dtype="bf16")
+    stream = torch.cuda.current_stream()
+    k, v, fac = make_inputs(torch, w, 1234 + rank, L - 1, dev)
+    # prefill (append tokens/s of the bulk quantiser), timed once
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    cache.prefill_quantize(0, k, v)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prefill_ms = e0.elapsed_time(e1)
+    prefill_tok_s = w["batch"] * (L - 1) / (prefill_ms / 1e3)
+    del k, v
+    g = torch.Generator(device=dev)
+    g.manual_seed(99 + rank)
+    B, H, Hq, D = w["batch"], w["n_kv_heads"], w["n_q_heads"], w["head_dim"]
+    nk = (torch.randn((n_steps_total, B, H, 1, D), generator=g, device=dev) * fac[None, None, :, None, :]).to(torch.bfloat16)
+    nv = torch.randn((n_steps_total, B, H, 1, D), generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn((B, Hq, D), generator=g, device=dev).to(torch.bfloat16)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+
+    def step(i):
+        cache.append(0, nk[i], nv[i])
+        cache.decode_attn(0, q, out=out)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    stats0 = cache.stats(0)
+    # per-step events around the split kernel (recorded by the library)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in kev:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    bytes_steps = []
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = binding.launch_count()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        cache.set_timing_events(*kev[i])
+        step(args.warmup + i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = binding.launch_count() - launches0
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    cache.set_timing_events(None, None)
+    ms_total = t0.elapsed_time(t1)
+    stats1 = cache.stats(0)
+    dec_bytes = (algorithmic_bytes(stats0, w) + algorithmic_bytes(stats1, w)) / 2
+    step_bytes = dec_bytes + append_bytes(w)
+    kernel_ms = [a.elapsed_time(b) for a, b in kev]
+    kernel_avg_ms = statistics.mean(kernel_ms)
+    cache.check_device_error()
+
+    # e2e: host buffers through the public API, copies inside the timed region
+    hk = nk[: args.steps].cpu().pin_memory()
+    hv = nv[: args.steps].cpu().pin_memory()
+    hq = q.cpu().pin_memory()
+    hout = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
+    dk = torch.empty_like(nk[0])
+    dv = torch.empty_like(nv[0])
+    dq = torch.empty_like(q)
+    cache2 = cache  # continue the same sequence
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for i in range(args.steps):
+        dk.copy_(hk[i], non_blocking=True)
+        dv.copy_(hv[i], non_blocking=True)
+        dq.copy_(hq, non_blocking=True)
+        cache2.append(0, dk, dv)
+        cache2.decode_attn(0, dq, out=out)
+        hout.copy_(out, non_blocking=True)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = c0.elapsed_time(c1) / args.steps
+    h2d = (dk.numel() + dv.numel() + dq.numel()) * 2
+    d2h = hout.numel() * 4
+
+    # in-process copy-kernel bandwidth (same kernel style, 1 GiB)
+    src = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        binding.copy_bandwidth(src, dst)
+    torch.cuda.synchronize()
+    cts = []
+    for _ in range(10):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        binding.copy_bandwidth(src, dst)
+        b.record(stream)
+        torch.cuda.synchronize()
+        cts.append(a.elapsed_time(b))
+    copy_gbs = 2 * (1 << 30) / (statistics.median(cts) / 1e3) / 1e9
+    del src, dst
+
+    ms_step = ms_total / args.steps
+    if pg:
+        t = torch.tensor([ms_step, e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_step, e2e_ms = float(t[0]), float(t[1])
+    value = world * step_bytes / (ms_step / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+    achieved = dec_bytes / (kernel_avg_ms / 1e3) / 1e9
+    if rank == 0:
+        cpu_gbs, cpu_t, cpu_n = cpu_baseline(n_pairs=2)
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME, "global_batch": w["batch"] * world, "seq_len": L,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (about 543 MB of cache read per step)",
+                       "arith": "codes exact in f16 MMA operands, scales folded as f16 hi+lo, f32 accumulate"},
+            "us_per_step": round(ms_step * 1e3, 2),
+            "us_per_model_step_x32": round(ms_step * 1e3 * w["layers_reported"], 1),
+            "pct_of_peak": round(100 * achieved / peak, 2),
+            "append_tokens_per_s": round(w["batch"] / (ms_step / 1e3), 1),
+            "prefill_tokens_per_s": round(prefill_tok_s, 1),
+            "copy_kernel_gbs": round(copy_gbs, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": "decode_kivi_kernel<128,2,4> (split-KV partitions + exact pools)",
+                         "algorithmic_bytes_per_launch": int(dec_bytes), "peak_kind": f"{peak_kind} hbm_gbs",
+                         "kernel_us": round(kernel_avg_ms * 1e3, 2)},
+            "cpu_baseline": {"value": round(cpu_gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{cpu_n} (b, kv-head) units with 4 query heads each, 32768-token "
+                                       f"context, decode only ({cpu_t:.1f} s)"},
+            "e2e": {"value": round(world * step_bytes / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

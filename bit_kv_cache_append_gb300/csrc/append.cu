@@ -1,0 +1,418 @@
+// Append-side kernels: exact tail ring and sink buffer writes, KIVI group
+// quantisation (with KVSink calibration exclusion), TurboQuant per-token
+// quantisation, and the KVSink sink-row gather.
+#include "kvq_device.cuh"
+
+namespace kvq {
+namespace {
+
+// Rotate 8 RoPE pairs (channels c0..c0+7 with c0+D/2..) held as act-dtype
+// bits, at table row `tab_row` ([D/2][2] cos, sin); results rounded back to
+// the activation dtype (posttrainllm "StreamingLLM + KIVI", "RoPE caveat":
+// keys keep the rotation of their absolute position).
+__device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float* tab_row, int c0, int bf16) {
+  uint16_t* pl = reinterpret_cast<uint16_t*>(&lo);
+  uint16_t* ph = reinterpret_cast<uint16_t*>(&hi);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float x = act_to_float(pl[i], bf16), y = act_to_float(ph[i], bf16);
+    const float c = tab_row[2 * (c0 + i)], s = tab_row[2 * (c0 + i) + 1];
+    float rx, ry;
+    rope_pair(x, y, c, s, &rx, &ry);
+    pl[i] = float_to_act(rx, bf16);
+    ph[i] = float_to_act(ry, bf16);
+  }
+}
+
+// ---------------------------------------------------------------- tail ring
+// Rows at positions >= tail_from go to the tail ring (slot pos mod tail_cap);
+// positions < n_sink also go to the overlay sink buffer (slot = pos).
+__global__ void tail_write_kernel(AppendArgs a, int row_begin, int n_rows) {
+  const Geometry& G = a.geo;
+  const int D = G.D, half = D / 2, cpr = half / 8;
+  const int bh = blockIdx.y;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  const int row = row_begin + idx / cpr;
+  if (row >= row_begin + n_rows) return;
+  const int c0 = (idx % cpr) * 8;
+  const int64_t pos = a.L0 + row;
+  const bool to_tail = pos >= a.tail_from;
+  const bool to_sink = pos < G.n_sink;
+  if (!to_tail && !to_sink) return;
+  const size_t in_row = (static_cast<size_t>(bh) * a.n + row) * D;
+  uint4 klo = *reinterpret_cast<const uint4*>(a.k + in_row + c0);
+  uint4 khi = *reinterpret_cast<const uint4*>(a.k + in_row + half + c0);
+  const uint4 vlo = *reinterpret_cast<const uint4*>(a.v + in_row + c0);
+  const uint4 vhi = *reinterpret_cast<const uint4*>(a.v + in_row + half + c0);
+  if (a.tab.rope) rotate8(klo, khi, a.tab.rope + static_cast<size_t>(pos) * D, c0, G.act_bf16);
+  if (to_tail) {
+    const size_t t = (static_cast<size_t>(bh) * G.tail_cap + (pos & (G.tail_cap - 1))) * D;
+    *reinterpret_cast<uint4*>(a.lay.tail_k + t + c0) = klo;
+    *reinterpret_cast<uint4*>(a.lay.tail_k + t + half + c0) = khi;
+    *reinterpret_cast<uint4*>(a.lay.tail_v + t + c0) = vlo;
+    *reinterpret_cast<uint4*>(a.lay.tail_v + t + half + c0) = vhi;
+  }
+  if (to_sink) {
+    const size_t t = (static_cast<size_t>(bh) * G.n_sink_slots + pos) * D;
+    *reinterpret_cast<uint4*>(a.lay.sink_k + t + c0) = klo;
+    *reinterpret_cast<uint4*>(a.lay.sink_k + t + half + c0) = khi;
+    *reinterpret_cast<uint4*>(a.lay.sink_v + t + c0) = vlo;
+    *reinterpret_cast<uint4*>(a.lay.sink_v + t + half + c0) = vhi;
+  }
+}
+
+// ---------------------------------------------------------------- KIVI flush
+// One CTA per (completed group, b, h); D threads. Quantisation follows
+// posttrainllm "StreamingLLM + KIVI", "Affine quantisation formula", in the
+// unsigned-code form: scale = max((max - min) / (2^b - 1), 1e-5) in fp32,
+// scale and zero (= min) stored as fp16, code = rint((x - zero) / scale)
+// clamped to [0, 2^b - 1], computed from the stored fp16 values promoted to
+// fp32. K: one (scale, zero) per channel over the group's 32 tokens; V: one
+// per token per 32-channel group (the KIVI group idea, same page, "Caveats").
+// KVSink (VeloxQuant-MLX "KVSink-Adapted Sink Protection", "How it works" 3):
+// before calibration every sink row of the group is replaced by its nearest
+// non-sink row (ties to the earlier row); sink rows keep the substitute's
+// codes and the group's mask bit tells attention to skip them.
+__device__ __forceinline__ void quantize_slice_params(float mn, float mx, int bits, __half* sh,
+                                                      __half* zh, float* s, float* z) {
+  const float lb = static_cast<float>((1 << bits) - 1);
+  const float s32 = fmaxf(__fdiv_rn(__fsub_rn(mx, mn), lb), 1e-5f);
+  *sh = __float2half_rn(s32);
+  *zh = __float2half_rn(mn);
+  *s = __half2float(*sh);
+  *z = __half2float(*zh);
+}
+
+__device__ __forceinline__ uint8_t quantize_code(float x, float s, float z, int bits) {
+  const float lb = static_cast<float>((1 << bits) - 1);
+  float q = rintf(__fdiv_rn(__fsub_rn(x, z), s));
+  q = fminf(fmaxf(q, 0.0f), lb);
+  return static_cast<uint8_t>(q);
+}
+
+__device__ __forceinline__ uint32_t pack_half2_bits(__half lo, __half hi) {
+  return static_cast<uint32_t>(__half_as_ushort(lo)) |
+         (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+}
+
+template <int D>
+__global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
+  constexpr int HALF = D / 2, NV = D / 32, CPR = HALF / 8;
+  __shared__ float xk[32][D + 1];
+  __shared__ float xv[32][D + 1];
+  __shared__ uint8_t ck[32][D];
+  __shared__ uint8_t cv[32][D];
+  __shared__ int sub[32];
+  __shared__ uint32_t smask;
+  const Geometry& G = a.geo;
+  const int tid = threadIdx.x;
+  const int bh = blockIdx.y, b = bh / G.H, h = bh % G.H;
+  const int64_t g = a.g_first + blockIdx.x;
+  const int64_t p0 = g * kGroup;
+  const int slot = static_cast<int>(g % G.n_slots);
+  const int bf16 = G.act_bf16;
+
+  if (tid == 0) {
+    uint32_t m = 0;
+    if (a.dyn_active) {
+      for (int j = 0; j < a.n_dyn_sel; ++j) {
+        const int64_t p = a.lay.sink_pos[b * kMaxSinks + j];
+        if (p >= p0 && p < p0 + kGroup) m |= 1u << (p - p0);
+      }
+    }
+    smask = m;
+    for (int r = 0; r < 32; ++r) {
+      int s = r;
+      if (((m >> r) & 1u) && m != 0xFFFFFFFFu) {
+        for (int d = 1; d < 32; ++d) {
+          if (r - d >= 0 && !((m >> (r - d)) & 1u)) { s = r - d; break; }
+          if (r + d < 32 && !((m >> (r + d)) & 1u)) { s = r + d; break; }
+        }
+      }
+      sub[r] = s;
+    }
+  }
+  __syncthreads();
+
+  for (int idx = tid; idx < 32 * CPR; idx += D) {
+    const int r = idx / CPR, c0 = (idx % CPR) * 8;
+    const int64_t pos = p0 + sub[r];
+    uint4 klo, khi, vlo, vhi;
+    if (pos < a.L0) {
+      const size_t t = (static_cast<size_t>(bh) * G.tail_cap + (pos & (G.tail_cap - 1))) * D;
+      klo = *reinterpret_cast<const uint4*>(a.lay.tail_k + t + c0);
+      khi = *reinterpret_cast<const uint4*>(a.lay.tail_k + t + HALF + c0);
+      vlo = *reinterpret_cast<const uint4*>(a.lay.tail_v + t + c0);
+      vhi = *reinterpret_cast<const uint4*>(a.lay.tail_v + t + HALF + c0);
+    } else {
+      const size_t t = (static_cast<size_t>(bh) * a.n + (pos - a.L0)) * D;
+      klo = *reinterpret_cast<const uint4*>(a.k + t + c0);
+      khi = *reinterpret_cast<const uint4*>(a.k + t + HALF + c0);
+      vlo = *reinterpret_cast<const uint4*>(a.v + t + c0);
+      vhi = *reinterpret_cast<const uint4*>(a.v + t + HALF + c0);
+      if (a.tab.rope) rotate8(klo, khi, a.tab.rope + static_cast<size_t>(pos) * D, c0, bf16);
+    }
+    const uint16_t* pkl = reinterpret_cast<const uint16_t*>(&klo);
+    const uint16_t* pkh = reinterpret_cast<const uint16_t*>(&khi);
+    const uint16_t* pvl = reinterpret_cast<const uint16_t*>(&vlo);
+    const uint16_t* pvh = reinterpret_cast<const uint16_t*>(&vhi);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      xk[r][c0 + i] = act_to_float(pkl[i], bf16);
+      xk[r][HALF + c0 + i] = act_to_float(pkh[i], bf16);
+      xv[r][c0 + i] = act_to_float(pvl[i], bf16);
+      xv[r][HALF + c0 + i] = act_to_float(pvh[i], bf16);
+    }
+  }
+  __syncthreads();
+
+  uint8_t* chunk = a.lay.chunks + (static_cast<size_t>(bh) * G.n_slots + slot) * G.chunk.bytes;
+  {  // K: channel tid over the 32 tokens
+    const int c = tid;
+    float mn = xk[0][c], mx = mn;
+    for (int r = 1; r < 32; ++r) {
+      mn = fminf(mn, xk[r][c]);
+      mx = fmaxf(mx, xk[r][c]);
+    }
+    __half sh, zh;
+    float s, z;
+    quantize_slice_params(mn, mx, G.kb, &sh, &zh, &s, &z);
+    for (int r = 0; r < 32; ++r) ck[r][c] = quantize_code(xk[r][c], s, z, G.kb);
+    reinterpret_cast<uint32_t*>(chunk + G.chunk.kmeta_off)[c] = pack_half2_bits(sh, zh);
+  }
+  {  // V: token r, channel group vg (index rotated by 8 vg to spread banks)
+    const int r = tid / NV, vg = tid % NV, base = 32 * vg;
+    float mn = xv[r][base], mx = mn;
+    for (int i = 0; i < 32; ++i) {
+      const float x = xv[r][base + ((i + 8 * vg) & 31)];
+      mn = fminf(mn, x);
+      mx = fmaxf(mx, x);
+    }
+    __half sh, zh;
+    float s, z;
+    quantize_slice_params(mn, mx, G.vb, &sh, &zh, &s, &z);
+    for (int i = 0; i < 32; ++i) {
+      const int c = base + ((i + 8 * vg) & 31);
+      cv[r][c] = quantize_code(xv[r][c], s, z, G.vb);
+    }
+    reinterpret_cast<uint32_t*>(chunk + G.chunk.vmeta_off)[r * NV + vg] = pack_half2_bits(sh, zh);
+  }
+  __syncthreads();
+
+  const int kwpl = D * G.kb / 32, vwpl = D * G.vb / 32;  // words per lane block
+  for (int wi = tid; wi < 32 * kwpl; wi += D) {
+    const int lane = wi / kwpl, w = wi % kwpl, per = 32 / G.kb;
+    uint32_t word = 0;
+    for (int i = 0; i < per; ++i) {
+      int tok, ch, wd, bit;
+      const int f = w * per + i;
+      k_frag_pos(D, lane, f, &tok, &ch);
+      frag_bits(G.kb, f, &wd, &bit);
+      word |= static_cast<uint32_t>(ck[tok][ch]) << bit;
+    }
+    reinterpret_cast<uint32_t*>(chunk + G.chunk.kc_off)[lane * kwpl + w] = word;
+  }
+  for (int wi = tid; wi < 32 * vwpl; wi += D) {
+    const int lane = wi / vwpl, w = wi % vwpl, per = 32 / G.vb;
+    uint32_t word = 0;
+    for (int i = 0; i < per; ++i) {
+      int tok, ch, wd, bit;
+      const int f = w * per + i;
+      v_frag_pos(D, lane, f, &tok, &ch);
+      frag_bits(G.vb, f, &wd, &bit);
+      word |= static_cast<uint32_t>(cv[tok][ch]) << bit;
+    }
+    reinterpret_cast<uint32_t*>(chunk + G.chunk.vc_off)[lane * vwpl + w] = word;
+  }
+  if (G.n_dyn && h == 0 && tid == 0) a.lay.sink_mask[b * G.n_slots + slot] = smask;
+}
+
+// ---------------------------------------------------------------- TurboQuant
+// One warp per (token, b, h): Foundry "TurboQuant KV Cache Compression - Spec",
+// "Algorithm Detail" with the as-built order (signs, then the Walsh-Hadamard
+// butterflies with stage length 1, 2, 4, ..., then 1/sqrt(d)); the norm is the
+// fixed pairwise tree over x^2 (stride D/2, D/4, ..., 1) and its sqrt; each
+// coordinate becomes w = (y/n + 1) * 0.5 and its code counts the boundaries
+// <= w. Lane l holds channels i*32 + l.
+template <int D>
+__device__ __forceinline__ float tq_code_row(float (&x)[D / 32], const float* signs, const float* bnd,
+                                             int bits, float rsq, uint8_t* codes_smem) {
+  constexpr int NS = D / 32;
+  const int lane = threadIdx.x & 31;
+  float y[NS], sq[NS];
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    y[i] = __fmul_rn(x[i], signs[i * 32 + lane]);
+    sq[i] = __fmul_rn(x[i], x[i]);
+  }
+#pragma unroll
+  for (int len = 1; len < 32; len <<= 1) {
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, y[i], len);
+      y[i] = (lane & len) ? __fsub_rn(o, y[i]) : __fadd_rn(y[i], o);
+    }
+  }
+#pragma unroll
+  for (int sl = 1; sl < NS; sl <<= 1) {
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      if ((i & sl) == 0) {
+        const float u = y[i], v = y[i + sl];
+        y[i] = __fadd_rn(u, v);
+        y[i + sl] = __fsub_rn(u, v);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NS; ++i) y[i] = __fmul_rn(y[i], rsq);
+#pragma unroll
+  for (int sl = NS / 2; sl >= 1; sl >>= 1) {
+#pragma unroll
+    for (int i = 0; i < sl; ++i) sq[i] = __fadd_rn(sq[i], sq[i + sl]);
+  }
+  float acc = sq[0];
+#pragma unroll
+  for (int st = 16; st >= 1; st >>= 1) {
+    const float o = __shfl_down_sync(0xffffffffu, acc, st);
+    if (lane < st) acc = __fadd_rn(acc, o);
+  }
+  const float n = __shfl_sync(0xffffffffu, __fsqrt_rn(acc), 0);
+  const int nb = (1 << bits) - 1;
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    const float u = (n > 0.0f) ? __fdiv_rn(y[i], n) : 0.0f;
+    const float w = __fmul_rn(__fadd_rn(u, 1.0f), 0.5f);
+    int code = 0;
+    for (int k = 0; k < nb; ++k) code += (w >= bnd[k]) ? 1 : 0;
+    codes_smem[i * 32 + lane] = static_cast<uint8_t>(code);
+  }
+  return n;
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) tq_quantize_kernel(AppendArgs a, int row_begin, int n_rows) {
+  constexpr int NS = D / 32;
+  __shared__ uint8_t codes[4][D];
+  __shared__ float s_signs[D];
+  __shared__ float s_bk[16], s_bv[16];
+  const Geometry& G = a.geo;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) s_signs[i] = a.tab.signs[i];
+  if (threadIdx.x < 16) {
+    s_bk[threadIdx.x] = (threadIdx.x < (1 << G.kb) - 1) ? a.tab.cb_k[threadIdx.x] : 2.0f;
+    s_bv[threadIdx.x] = (threadIdx.x < (1 << G.vb) - 1) ? a.tab.cb_v[threadIdx.x] : 2.0f;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = row_begin + blockIdx.x * 4 + warp;
+  if (row >= row_begin + n_rows) return;
+  const int bh = blockIdx.y;
+  const int64_t pos = a.L0 + row;
+  const size_t in_row = (static_cast<size_t>(bh) * a.n + row) * D;
+  const int bf16 = G.act_bf16;
+  const float rsq = static_cast<float>(1.0 / sqrt(static_cast<double>(D)));
+  float xk[NS], xv[NS];
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    xk[i] = act_to_float(a.k[in_row + i * 32 + lane], bf16);
+    xv[i] = act_to_float(a.v[in_row + i * 32 + lane], bf16);
+  }
+  if (a.tab.rope) {
+    const float* tr = a.tab.rope + static_cast<size_t>(pos) * D;
+#pragma unroll
+    for (int i = 0; i < NS / 2; ++i) {
+      const int c = i * 32 + lane;
+      float rx, ry;
+      rope_pair(xk[i], xk[i + NS / 2], tr[2 * c], tr[2 * c + 1], &rx, &ry);
+      xk[i] = act_to_float(float_to_act(rx, bf16), bf16);
+      xk[i + NS / 2] = act_to_float(float_to_act(ry, bf16), bf16);
+    }
+  }
+  const int slot = static_cast<int>((pos / kGroup) % G.n_slots);
+  const int r = static_cast<int>(pos % kGroup);
+  uint8_t* chunk = a.lay.chunks + (static_cast<size_t>(bh) * G.n_slots + slot) * G.chunk.bytes;
+  for (int which = 0; which < 2; ++which) {
+    const int bits = which ? G.vb : G.kb;
+    const float n = which ? tq_code_row<D>(xv, s_signs, s_bv, bits, rsq, codes[warp])
+                          : tq_code_row<D>(xk, s_signs, s_bk, bits, rsq, codes[warp]);
+    __syncwarp();
+    const int row_words = D * bits / 32, per = 32 / bits;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(chunk + (which ? G.chunk.vc_off : G.chunk.kc_off) +
+                                                r * (D * bits / 8));
+    if (lane < row_words) {
+      uint32_t word = 0;
+      for (int i = 0; i < per; ++i) word |= static_cast<uint32_t>(codes[warp][lane * per + i]) << (bits * i);
+      dst[lane] = word;
+    }
+    if (lane == 0)
+      reinterpret_cast<float*>(chunk + (which ? G.chunk.vmeta_off : G.chunk.kmeta_off))[r] = n;
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------- KVSink rows
+// Copy the selected sink rows of the prefill input (keys rotated like every
+// other key) into the sink buffer.
+__global__ void sink_gather_kernel(AppendArgs a) {
+  const Geometry& G = a.geo;
+  const int D = G.D, half = D / 2, cpr = half / 8;
+  const int j = blockIdx.x, bh = blockIdx.y, b = bh / G.H;
+  const int64_t pos = a.lay.sink_pos[b * kMaxSinks + j];
+  const int64_t row = pos - a.L0;
+  if (row < 0 || row >= a.n) return;
+  for (int idx = threadIdx.x; idx < cpr; idx += blockDim.x) {
+    const int c0 = idx * 8;
+    const size_t in_row = (static_cast<size_t>(bh) * a.n + row) * D;
+    uint4 klo = *reinterpret_cast<const uint4*>(a.k + in_row + c0);
+    uint4 khi = *reinterpret_cast<const uint4*>(a.k + in_row + half + c0);
+    const uint4 vlo = *reinterpret_cast<const uint4*>(a.v + in_row + c0);
+    const uint4 vhi = *reinterpret_cast<const uint4*>(a.v + in_row + half + c0);
+    if (a.tab.rope) rotate8(klo, khi, a.tab.rope + static_cast<size_t>(pos) * D, c0, G.act_bf16);
+    const size_t t = (static_cast<size_t>(bh) * G.n_sink_slots + j) * D;
+    *reinterpret_cast<uint4*>(a.lay.sink_k + t + c0) = klo;
+    *reinterpret_cast<uint4*>(a.lay.sink_k + t + half + c0) = khi;
+    *reinterpret_cast<uint4*>(a.lay.sink_v + t + c0) = vlo;
+    *reinterpret_cast<uint4*>(a.lay.sink_v + t + half + c0) = vhi;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int64_t* launches) {
+  const Geometry& G = a.geo;
+  const int BH = G.B * G.H;
+  if (!G.mode_tq && a.n_groups > 0) {
+    dim3 grid(a.n_groups, BH);
+    if (G.D == 128) kivi_flush_kernel<128><<<grid, 128, 0, s>>>(a);
+    else kivi_flush_kernel<64><<<grid, 64, 0, s>>>(a);
+    ++*launches;
+  }
+  if (G.mode_tq && a.n > 0) {
+    dim3 grid((a.n + 3) / 4, BH);
+    if (G.D == 128) tq_quantize_kernel<128><<<grid, 128, 0, s>>>(a, 0, a.n);
+    else tq_quantize_kernel<64><<<grid, 128, 0, s>>>(a, 0, a.n);
+    ++*launches;
+  }
+  int64_t first = a.n;
+  if (a.L0 < G.n_sink) first = 0;
+  else if (a.tail_from < a.L0 + a.n) first = a.tail_from > a.L0 ? a.tail_from - a.L0 : 0;
+  if (first < a.n) {
+    const int rows = static_cast<int>(a.n - first);
+    const int cpr = G.D / 16;
+    const int threads = 128;
+    dim3 grid(static_cast<unsigned>((static_cast<int64_t>(rows) * cpr + threads - 1) / threads), BH);
+    tail_write_kernel<<<grid, threads, 0, s>>>(a, static_cast<int>(first), rows);
+    ++*launches;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sink_gather(const AppendArgs& a, cudaStream_t s, int64_t* launches) {
+  if (a.n_dyn_sel <= 0) return cudaSuccess;
+  dim3 grid(a.n_dyn_sel, a.geo.B * a.geo.H);
+  sink_gather_kernel<<<grid, 32, 0, s>>>(a);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

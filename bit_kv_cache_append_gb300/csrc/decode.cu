@@ -1,0 +1,231 @@
+// TurboQuant split kernel, the log-sum-exp merge of the partials and the
+// decode dispatch.
+#include "decode_common.cuh"
+
+namespace kvq {
+
+cudaError_t launch_kivi_d64(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_kivi_d128(const DecodeArgs& a, cudaStream_t s);
+
+namespace {
+
+// Walsh-Hadamard butterflies (stage length 1, 2, ..., D/2) over a vector held
+// as lane l -> elements i*32 + l.
+template <int D>
+__device__ __forceinline__ void warp_fwht(float (&y)[D / 32]) {
+  constexpr int NS = D / 32;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int len = 1; len < 32; len <<= 1) {
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, y[i], len);
+      y[i] = (lane & len) ? o - y[i] : y[i] + o;
+    }
+  }
+#pragma unroll
+  for (int sl = 1; sl < NS; sl <<= 1) {
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      if ((i & sl) == 0) {
+        const float u = y[i], v = y[i + sl];
+        y[i] = u + v;
+        y[i + sl] = u - v;
+      }
+    }
+  }
+}
+
+// TurboQuant decode in the rotated domain (Foundry "TurboQuant KV Cache
+// Compression - Spec", "Optimization: Fused dequant-dot"): the query is
+// rotated once (R q, R = H D / sqrt(d)), dotted with n_k (2 c[code] - 1) per
+// coordinate, and the values are accumulated as n_v (2 c[code] - 1) in the
+// rotated domain; the merge kernel rotates the output back once.
+// One warp per token in turn over the partition's tokens.
+template <int D>
+__global__ void __launch_bounds__(128) decode_tq_kernel(DecodeArgs a) {
+  constexpr int NS = D / 32, NW = 4;
+  __shared__ float red[NW * kMaxGqa * (D + 2)];
+  __shared__ float ck[16], cv[16];
+  const Geometry& G = a.geo;
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (split == a.n_splits) {
+    exact_partition<D>(a, b, h, red);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = G.gqa;
+  if (threadIdx.x < 16) {
+    const int nk = 1 << G.kb, nv = 1 << G.vb;
+    ck[threadIdx.x] = threadIdx.x < nk ? 2.0f * a.tab.cb_k[nk - 1 + threadIdx.x] - 1.0f : 0.0f;
+    cv[threadIdx.x] = threadIdx.x < nv ? 2.0f * a.tab.cb_v[nv - 1 + threadIdx.x] - 1.0f : 0.0f;
+  }
+  __syncthreads();
+  const float rsq = static_cast<float>(1.0 / sqrt(static_cast<double>(D)));
+  float qr[kMaxGqa][NS];
+#pragma unroll
+  for (int j = 0; j < kMaxGqa; ++j) {
+#pragma unroll
+    for (int i = 0; i < NS; ++i)
+      qr[j][i] = (j < gq) ? query_value(a, b, h * gq + j, i * 32 + lane) * a.tab.signs[i * 32 + lane] : 0.0f;
+    warp_fwht<D>(qr[j]);
+#pragma unroll
+    for (int i = 0; i < NS; ++i) qr[j][i] *= rsq;
+  }
+  float m[kMaxGqa], l[kMaxGqa], o[kMaxGqa][NS];
+#pragma unroll
+  for (int j = 0; j < kMaxGqa; ++j) {
+    m[j] = -INFINITY;
+    l[j] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NS; ++i) o[j][i] = 0.0f;
+  }
+  const int64_t gs0 = a.g_begin + static_cast<int64_t>(split) * a.groups_per_split;
+  const int64_t gend = a.g_begin + a.n_groups;
+  const int64_t gs1 = gs0 + a.groups_per_split < gend ? gs0 + a.groups_per_split : gend;
+  const int64_t t0 = gs0 * kGroup > a.qlo ? gs0 * kGroup : a.qlo;
+  const int64_t t1 = gs1 * kGroup < a.F ? gs1 * kGroup : a.F;
+  const int bh = b * G.H + h;
+  const int kmask = (1 << G.kb) - 1, vmask = (1 << G.vb) - 1;
+  for (int64_t p = t0 + warp; p < t1; p += NW) {
+    const int slot = static_cast<int>((p / kGroup) % G.n_slots), r = static_cast<int>(p % kGroup);
+    const uint8_t* chunk = a.lay.chunks + (static_cast<size_t>(bh) * G.n_slots + slot) * G.chunk.bytes;
+    const uint8_t* krow = chunk + G.chunk.kc_off + r * (D * G.kb / 8);
+    const uint8_t* vrow = chunk + G.chunk.vc_off + r * (D * G.vb / 8);
+    const float kn = reinterpret_cast<const float*>(chunk + G.chunk.kmeta_off)[r];
+    const float vn = reinterpret_cast<const float*>(chunk + G.chunk.vmeta_off)[r];
+    float ky[NS], vy[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const int c = i * 32 + lane;
+      const int kc = (krow[c * G.kb / 8] >> ((c % (8 / G.kb)) * G.kb)) & kmask;
+      const int vc = (vrow[c * G.vb / 8] >> ((c % (8 / G.vb)) * G.vb)) & vmask;
+      ky[i] = kn * ck[kc];
+      vy[i] = vn * cv[vc];
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxGqa; ++j) {
+      if (j >= gq) break;
+      float s = 0.0f;
+#pragma unroll
+      for (int i = 0; i < NS; ++i) s = fmaf(qr[j][i], ky[i], s);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      const float mn = fmaxf(m[j], s);
+      const float al = exp2f(m[j] - mn);
+      const float pp = exp2f(s - mn);
+      l[j] = l[j] * al + pp;
+#pragma unroll
+      for (int i = 0; i < NS; ++i) o[j][i] = fmaf(o[j][i], al, pp * vy[i]);
+      m[j] = mn;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxGqa; ++j) {
+    if (j >= gq) break;
+    float* rj = red + (warp * kMaxGqa + j) * (D + 2);
+#pragma unroll
+    for (int i = 0; i < NS; ++i) rj[i * 32 + lane] = o[j][i];
+    if (lane == 0) {
+      rj[D] = m[j];
+      rj[D + 1] = l[j];
+    }
+  }
+  __syncthreads();
+  write_partial<D, NW>(a, red, b, h, split);
+}
+
+// One warp per (b, query head): combine the partials by log-sum-exp
+// (M = max m_s, o = sum 2^(m_s - M) o_s / sum 2^(m_s - M) l_s) and, in
+// TurboQuant mode, rotate the output back (x = D FWHT(y) / sqrt(d)).
+template <int D>
+__global__ void __launch_bounds__(128) merge_kernel(DecodeArgs a) {
+  constexpr int NS = D / 32;
+  const Geometry& G = a.geo;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;
+  if (row >= G.B * G.Hq) return;
+  const int ns = a.n_splits + 1;
+  const float* ml = a.part_ml + static_cast<size_t>(row) * ns * 2;
+  float M = -INFINITY;
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, ml[2 * s]);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float L = 0.0f, o[NS];
+#pragma unroll
+  for (int i = 0; i < NS; ++i) o[i] = 0.0f;
+  for (int s = 0; s < ns; ++s) {
+    const float ms = ml[2 * s];
+    if (ms == -INFINITY) continue;
+    const float w = exp2f(ms - M);
+    L += ml[2 * s + 1] * w;
+    const float* po = a.part_o + (static_cast<size_t>(row) * ns + s) * D;
+#pragma unroll
+    for (int i = 0; i < NS; ++i) o[i] = fmaf(po[i * 32 + lane], w, o[i]);
+  }
+  const float inv = 1.0f / L;
+#pragma unroll
+  for (int i = 0; i < NS; ++i) o[i] *= inv;
+  if (G.mode_tq) {
+    warp_fwht<D>(o);
+    const float rsq = static_cast<float>(1.0 / sqrt(static_cast<double>(D)));
+#pragma unroll
+    for (int i = 0; i < NS; ++i) o[i] = o[i] * rsq * a.tab.signs[i * 32 + lane];
+  }
+#pragma unroll
+  for (int i = 0; i < NS; ++i) a.out[static_cast<size_t>(row) * D + i * 32 + lane] = o[i];
+  if (a.lse && lane == 0) a.lse[row] = (M + log2f(L)) * 0.69314718055994530942f;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1,
+                          int64_t* launches) {
+  const Geometry& G = a.geo;
+  cudaError_t e;
+  if (ev0) cudaEventRecord(ev0, s);
+  if (!G.mode_tq) {
+    e = (G.D == 128) ? launch_kivi_d128(a, s) : launch_kivi_d64(a, s);
+  } else {
+    dim3 grid(a.n_splits + 1, G.H, G.B);
+    if (G.D == 128) decode_tq_kernel<128><<<grid, 128, 0, s>>>(a);
+    else decode_tq_kernel<64><<<grid, 128, 0, s>>>(a);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) return e;
+  if (ev1) cudaEventRecord(ev1, s);
+  const int rows = G.B * G.Hq;
+  if (G.D == 128) merge_kernel<128><<<(rows + 3) / 4, 128, 0, s>>>(a);
+  else merge_kernel<64><<<(rows + 3) / 4, 128, 0, s>>>(a);
+  *launches += 2;
+  return cudaGetLastError();
+}
+
+// 16-byte vectorised grid-stride copy: the in-process bandwidth reference.
+namespace {
+__global__ void __launch_bounds__(256) copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                   size_t n) {
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t step = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (; i + 3 * step < n; i += 4 * step) {
+    const uint4 a0 = src[i], a1 = src[i + step], a2 = src[i + 2 * step], a3 = src[i + 3 * step];
+    dst[i] = a0;
+    dst[i + step] = a1;
+    dst[i + 2 * step] = a2;
+    dst[i + 3 * step] = a3;
+  }
+  for (; i < n; i += step) dst[i] = src[i];
+}
+}  // namespace
+
+cudaError_t launch_copy(const void* src, void* dst, size_t bytes, cudaStream_t s, int64_t* launches) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t n = bytes / 16;
+  copy_kernel<<<sms * 8, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

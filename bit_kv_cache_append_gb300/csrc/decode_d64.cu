@@ -1,0 +1,6 @@
+// Decode kernels instantiated for head_dim 64.
+#include "decode_kivi.cuh"
+
+namespace kvq {
+cudaError_t launch_kivi_d64(const DecodeArgs& a, cudaStream_t s) { return launch_kivi_d<64>(a, s); }
+}  // namespace kvq

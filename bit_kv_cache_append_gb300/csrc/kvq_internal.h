@@ -1,0 +1,97 @@
+// Kernel argument blocks and launchers of the library (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kvq_layout.h"
+
+namespace kvq {
+
+// Device pointers of one layer inside the arena.
+struct LayerDev {
+  uint8_t* chunks;      // [B][H][n_slots][chunk.bytes]
+  uint16_t* tail_k;     // [B][H][tail_cap][D]  act dtype bits
+  uint16_t* tail_v;
+  uint16_t* sink_k;     // [B][H][n_sink_slots][D]
+  uint16_t* sink_v;
+  int64_t* sink_pos;    // [B][kMaxSinks]
+  uint32_t* sink_mask;  // [B][n_slots]
+};
+
+// Tables shared by every layer.
+struct TablesDev {
+  const float* rope;    // [rope_max_pos][D/2][2] or nullptr
+  const float* signs;   // [D] TurboQuant +-1
+  const float* cb_k;    // boundaries[2^kb - 1] then centroids[2^kb]
+  const float* cb_v;
+  int* err_flag;
+};
+
+// One append: tokens [L0, L0 + n) arrive in `k`, `v` ([B][H][n][D]).
+struct AppendArgs {
+  Geometry geo;
+  LayerDev lay;
+  TablesDev tab;
+  const uint16_t* k;
+  const uint16_t* v;
+  int n;
+  int64_t L0;           // L before the append
+  int64_t tail_from;    // rows at positions >= tail_from go to the tail ring
+  int64_t g_first;      // first group that completes in this append
+  int n_groups;         // groups completing in this append (KIVI)
+  int dyn_active;       // KVSink: sink positions valid for exclusion
+  int n_dyn_sel;        // KVSink: number of selected sinks
+};
+
+// Decode attention of one layer.
+struct DecodeArgs {
+  Geometry geo;
+  LayerDev lay;
+  TablesDev tab;
+  const uint16_t* q;    // [B][Hq][D] act dtype bits
+  float* part_o;        // [B][Hq][ns][D]
+  float* part_ml;       // [B][Hq][ns][2]  (max in log2 units, sum)
+  float* out;           // [B][Hq][D]
+  float* lse;           // [B][Hq] or nullptr
+  int64_t L, F, qlo;    // quantised segment [qlo, F), tail [F, L)
+  int64_t g_begin;      // first group of the quantised segment
+  int n_groups;         // groups touching [qlo, F)
+  int groups_per_split;
+  int n_splits;         // quantised partitions; partition n_splits = exact pools
+  int n_sink_read;      // overlay: sink slots [0, n) read from the sink buffer
+  int n_dyn_sel;        // KVSink: selected sinks (read when pos < F)
+  float qscale;         // log2(e) / sqrt(D)
+};
+
+// KVSink selection scratch.
+struct SinkSelectArgs {
+  Geometry geo;
+  LayerDev lay;
+  TablesDev tab;
+  const uint16_t* k;    // [B][H][n][D]
+  int n;
+  float* norms;         // [B][n]
+  float* cand_m;        // [B][n_chunks][kMaxSinks]
+  int64_t* cand_p;
+  int n_chunks;
+  int k_sel;            // sinks to select
+};
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int64_t* launches);
+cudaError_t launch_sink_select(const SinkSelectArgs& a, cudaStream_t s, int64_t* launches);
+cudaError_t launch_sink_gather(const AppendArgs& a, cudaStream_t s, int64_t* launches);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1,
+                          int64_t* launches);
+cudaError_t launch_copy(const void* src, void* dst, size_t bytes, cudaStream_t s,
+                        int64_t* launches);
+
+// Host-built tables (independent of any other implementation).
+void build_rope_table(float* out, int64_t max_pos, int D, double base);
+void build_signs(float* out, int D, uint64_t seed);
+// Lloyd-Max quantiser of Beta(a, a) on [0, 1] with 2^bits levels, by
+// composite Gauss-Legendre quadrature of the density; double precision.
+void build_beta_codebook(double a, int bits, double* boundaries, double* centroids);
+
+}  // namespace kvq

@@ -1,0 +1,112 @@
+// Internal layout of the cache arena: group chunks, the tail ring and the
+// fragment-native order of the packed codes. Included by the host code and
+// by the kernels of the library (and by nothing else).
+//
+// A "chunk" holds one 32-token group of one (layer, b, kv-head):
+//   KIVI:       [K codes 32*D*kb/8][K meta D x (s,z) f16][V codes 32*D*vb/8]
+//               [V meta 32 x D/32 x (s,z) f16]
+//   TurboQuant: [K codes 32 x D*kb/8 row-major][K norms 32 f32]
+//               [V codes 32 x D*vb/8 row-major][V norms 32 f32]
+// Chunk sizes are multiples of 16 bytes so one 1-D bulk copy moves a chunk.
+//
+// KIVI codes are stored in the order the decode kernel's tensor-core
+// fragments consume them (the canonical, page-defined order is produced by
+// kv_cache_export). The 32 lanes of the consuming warp (lane = 4 g + t) own
+// D codes each, as a contiguous block of D*bits/8 bytes. Fragment element
+// f = 0 .. D-1 of a lane maps to a (token, channel) of the group:
+//   K (A operand of S^T = K Q^T, m16n8k16, rows = tokens, k = channels):
+//     f = ((mt * S + s) * 4 + r) * 2 + e,  S = D/16, mt in {0,1}, r in 0..3
+//     token = 16 mt + g + 8 (r & 1);  channel = t D/4 + 4 s + 2 (r >> 1) + e
+//   V (A operand of O^T = V^T P^T, rows = channels, k = tokens):
+//     f = ((m * 2 + kb) * 4 + r) * 2 + e,  m in [0, D/16), kb in {0,1}
+//     channel = 16 m + g + 8 (r & 1);  token = 16 kb + 2 t + e + 8 (r >> 1)
+// Within a lane block, element f sits in 32-bit word f / (32/bits) at bit
+// bits * j + 16 e, j = (f % (32/bits)) / 2: the two elements of one f16x2
+// register are 16 bits apart, so a mask and an f16 magic-number OR turn a
+// pair of codes into an exact f16x2 value.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define KVQ_HD __host__ __device__ __forceinline__
+#else
+#define KVQ_HD inline
+#endif
+
+namespace kvq {
+
+constexpr int kGroup = 32;
+constexpr int kMaxSinks = 32;
+constexpr int kMaxGqa = 4;
+
+struct Chunk {
+  int kc_off, kmeta_off, vc_off, vmeta_off, bytes;
+};
+
+KVQ_HD Chunk chunk_layout(int mode_tq, int D, int kb, int vb) {
+  Chunk c;
+  c.kc_off = 0;
+  c.kmeta_off = kGroup * D * kb / 8;
+  if (!mode_tq) {
+    c.vc_off = c.kmeta_off + 4 * D;
+    c.vmeta_off = c.vc_off + kGroup * D * vb / 8;
+    c.bytes = c.vmeta_off + 4 * D;
+  } else {
+    c.vc_off = c.kmeta_off + 4 * kGroup;
+    c.vmeta_off = c.vc_off + kGroup * D * vb / 8;
+    c.bytes = c.vmeta_off + 4 * kGroup;
+  }
+  return c;
+}
+
+// (token, channel) of fragment element f of lane (g, t) for K.
+KVQ_HD void k_frag_pos(int D, int lane, int f, int* token, int* channel) {
+  const int g = lane >> 2, t = lane & 3, S = D / 16;
+  const int e = f & 1, r = (f >> 1) & 3, ms = f >> 3;  // ms = mt * S + s
+  const int mt = ms / S, s = ms % S;
+  *token = 16 * mt + g + 8 * (r & 1);
+  *channel = t * (D / 4) + 4 * s + 2 * (r >> 1) + e;
+}
+
+// (token, channel) of fragment element f of lane (g, t) for V.
+KVQ_HD void v_frag_pos(int D, int lane, int f, int* token, int* channel) {
+  (void)D;
+  const int g = lane >> 2, t = lane & 3;
+  const int e = f & 1, r = (f >> 1) & 3, mk = f >> 3;  // mk = m * 2 + kb
+  const int m = mk >> 1, kb = mk & 1;
+  *channel = 16 * m + g + 8 * (r & 1);
+  *token = 16 * kb + 2 * t + e + 8 * (r >> 1);
+}
+
+// Word index and bit position of element f inside a lane block.
+KVQ_HD void frag_bits(int bits, int f, int* word, int* bit) {
+  const int per_word = 32 / bits;
+  const int w = f / per_word, i = f % per_word;
+  *word = w;
+  *bit = bits * (i >> 1) + 16 * (i & 1);
+}
+
+// Arena geometry shared by every layer.
+struct Geometry {
+  int B, H, Hq, D, gqa;
+  int mode_tq, kb, vb;
+  int n_sink, window, evict_window, n_dyn;
+  int act_bf16;
+  int64_t max_tokens;
+  int n_slots;        // group chunks per (layer, b, h)
+  int tail_cap;       // rows per (layer, b, h) in the tail ring (power of 2)
+  int n_sink_slots;   // rows per (layer, b, h) in the sink buffer
+  int max_splits;
+  Chunk chunk;
+  int64_t rope_max_pos;
+  // byte offsets inside the arena
+  size_t off_err, off_rope, off_signs, off_cbk, off_cbv, off_part_o, off_part_ml;
+  size_t off_norms, off_cand_m, off_cand_p, n_cand_chunks;
+  size_t off_layers, layer_bytes;
+  size_t l_chunks, l_tail_k, l_tail_v, l_sink_k, l_sink_v, l_sink_pos, l_sink_mask;
+  size_t total;
+};
+
+}  // namespace kvq

@@ -1,0 +1,190 @@
+// KVSink-style sink selection (VeloxQuant-MLX "KVSink-Adapted Sink
+// Protection", "How it works" 1): the per-token key L2 norm averaged over the
+// KV heads, and the top-k positions per sequence (norm descending, ties to the
+// lower position).
+#include "kvq_device.cuh"
+
+namespace kvq {
+namespace {
+
+// One warp per (token, b): head norms by the fixed pairwise tree over k^2
+// (stride D/2, D/4, ..., 1), summed over heads in head order, divided by Hkv.
+template <int D>
+__global__ void __launch_bounds__(128) keynorm_kernel(SinkSelectArgs a) {
+  constexpr int NS = D / 32;
+  const Geometry& G = a.geo;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 4 + warp, b = blockIdx.y;
+  if (t >= a.n) return;
+  const int bf16 = G.act_bf16;
+  float acc = 0.0f;
+  for (int h = 0; h < G.H; ++h) {
+    const size_t row = ((static_cast<size_t>(b) * G.H + h) * a.n + t) * D;
+    float x[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) x[i] = act_to_float(a.k[row + i * 32 + lane], bf16);
+    if (a.tab.rope) {
+      const float* tr = a.tab.rope + static_cast<size_t>(t) * D;
+#pragma unroll
+      for (int i = 0; i < NS / 2; ++i) {
+        const int c = i * 32 + lane;
+        float rx, ry;
+        rope_pair(x[i], x[i + NS / 2], tr[2 * c], tr[2 * c + 1], &rx, &ry);
+        x[i] = act_to_float(float_to_act(rx, bf16), bf16);
+        x[i + NS / 2] = act_to_float(float_to_act(ry, bf16), bf16);
+      }
+    }
+    float sq[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) sq[i] = __fmul_rn(x[i], x[i]);
+#pragma unroll
+    for (int sl = NS / 2; sl >= 1; sl >>= 1) {
+#pragma unroll
+      for (int i = 0; i < sl; ++i) sq[i] = __fadd_rn(sq[i], sq[i + sl]);
+    }
+    float s = sq[0];
+#pragma unroll
+    for (int st = 16; st >= 1; st >>= 1) {
+      const float o = __shfl_down_sync(0xffffffffu, s, st);
+      if (lane < st) s = __fadd_rn(s, o);
+    }
+    const float nrm = __fsqrt_rn(s);
+    acc = (h == 0) ? nrm : __fadd_rn(acc, nrm);
+  }
+  if (lane == 0) a.norms[static_cast<size_t>(b) * a.n + t] = __fdiv_rn(acc, static_cast<float>(G.H));
+}
+
+__device__ __forceinline__ bool better(float m1, int64_t p1, float m2, int64_t p2) {
+  return m1 > m2 || (m1 == m2 && p1 < p2);
+}
+
+constexpr int kTopkThreads = 256;
+constexpr int kTopkPer = 4;
+constexpr int kChunk = kTopkThreads * kTopkPer;
+
+// k rounds of a block-wide arg-best over candidates held 4 per thread;
+// the winner of each round is taken out and written in rank order.
+__device__ void block_topk(float (&m)[kTopkPer], int64_t (&p)[kTopkPer], int k, float* out_m,
+                           int64_t* out_p) {
+  __shared__ float wm[kTopkThreads / 32];
+  __shared__ int64_t wp[kTopkThreads / 32];
+  __shared__ float bm;
+  __shared__ int64_t bp;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int round = 0; round < k; ++round) {
+    float cm = -INFINITY;
+    int64_t cp = INT64_MAX;
+#pragma unroll
+    for (int i = 0; i < kTopkPer; ++i)
+      if (better(m[i], p[i], cm, cp)) { cm = m[i]; cp = p[i]; }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, cm, off);
+      const int64_t op = __shfl_xor_sync(0xffffffffu, cp, off);
+      if (better(om, op, cm, cp)) { cm = om; cp = op; }
+    }
+    if (lane == 0) { wm[warp] = cm; wp[warp] = cp; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float xm = wm[0];
+      int64_t xp = wp[0];
+      for (int w = 1; w < kTopkThreads / 32; ++w)
+        if (better(wm[w], wp[w], xm, xp)) { xm = wm[w]; xp = wp[w]; }
+      bm = xm;
+      bp = xp;
+      out_m[round] = xm;
+      out_p[round] = xp;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kTopkPer; ++i)
+      if (p[i] == bp && m[i] == bm) { m[i] = -INFINITY; p[i] = INT64_MAX; }
+    __syncthreads();
+  }
+}
+
+// Pass 1: the top k of each chunk of kChunk positions of one sequence.
+__global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(SinkSelectArgs a) {
+  const int chunk = blockIdx.x, b = blockIdx.y;
+  float m[kTopkPer];
+  int64_t p[kTopkPer];
+#pragma unroll
+  for (int i = 0; i < kTopkPer; ++i) {
+    const int64_t t = static_cast<int64_t>(chunk) * kChunk + i * kTopkThreads + threadIdx.x;
+    if (t < a.n) { m[i] = a.norms[static_cast<size_t>(b) * a.n + t]; p[i] = t; }
+    else { m[i] = -INFINITY; p[i] = INT64_MAX; }
+  }
+  const size_t o = (static_cast<size_t>(b) * a.n_chunks + chunk) * kMaxSinks;
+  block_topk(m, p, a.k_sel, a.cand_m + o, a.cand_p + o);
+}
+
+// Pass 2: the top k over the chunk winners of one sequence, by k rounds of a
+// block-wide arg-best over the candidate array (each winner is struck out in
+// place), stored in ascending position order as the sink set.
+__global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(SinkSelectArgs a) {
+  const int b = blockIdx.x;
+  __shared__ float fm[kMaxSinks];
+  __shared__ int64_t fp[kMaxSinks];
+  __shared__ float wm[kTopkThreads / 32];
+  __shared__ int64_t wp[kTopkThreads / 32];
+  __shared__ int wc[kTopkThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n_cand = a.n_chunks * kMaxSinks;
+  float* cm_base = a.cand_m + static_cast<size_t>(b) * n_cand;
+  int64_t* cp_base = a.cand_p + static_cast<size_t>(b) * n_cand;
+  for (int round = 0; round < a.k_sel; ++round) {
+    float bm = -INFINITY;
+    int64_t bp = INT64_MAX;
+    int bc = -1;
+    for (int c = threadIdx.x; c < n_cand; c += kTopkThreads) {
+      if (c % kMaxSinks >= a.k_sel) continue;
+      const float m = cm_base[c];
+      const int64_t p = cp_base[c];
+      if (better(m, p, bm, bp)) { bm = m; bp = p; bc = c; }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, bm, off);
+      const int64_t op = __shfl_xor_sync(0xffffffffu, bp, off);
+      const int oc = __shfl_xor_sync(0xffffffffu, bc, off);
+      if (better(om, op, bm, bp)) { bm = om; bp = op; bc = oc; }
+    }
+    if (lane == 0) { wm[warp] = bm; wp[warp] = bp; wc[warp] = bc; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float xm = wm[0];
+      int64_t xp = wp[0];
+      int xc = wc[0];
+      for (int w = 1; w < kTopkThreads / 32; ++w)
+        if (better(wm[w], wp[w], xm, xp)) { xm = wm[w]; xp = wp[w]; xc = wc[w]; }
+      fm[round] = xm;
+      fp[round] = xp;
+      if (xc >= 0) { cm_base[xc] = -INFINITY; cp_base[xc] = INT64_MAX; }
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < a.k_sel; ++i) {  // ascending by position
+      const int64_t x = fp[i];
+      int j = i - 1;
+      while (j >= 0 && fp[j] > x) { fp[j + 1] = fp[j]; --j; }
+      fp[j + 1] = x;
+    }
+    for (int i = 0; i < a.k_sel; ++i) a.lay.sink_pos[b * kMaxSinks + i] = fp[i];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_sink_select(const SinkSelectArgs& a, cudaStream_t s, int64_t* launches) {
+  dim3 g1((a.n + 3) / 4, a.geo.B);
+  if (a.geo.D == 128) keynorm_kernel<128><<<g1, 128, 0, s>>>(a);
+  else keynorm_kernel<64><<<g1, 128, 0, s>>>(a);
+  dim3 g2(a.n_chunks, a.geo.B);
+  topk_chunk_kernel<<<g2, kTopkThreads, 0, s>>>(a);
+  topk_final_kernel<<<a.geo.B, kTopkThreads, 0, s>>>(a);
+  *launches += 3;
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -202,51 +202,70 @@ class OracleCache:
     def _append_rotated(self, layer: int, k, v) -> None:
         st, cfg = self.layers[layer], self.cfg
         n = k.shape[2]
-        for i in range(n):
-            pos = st.L + i
-            st.rows[pos] = (k[:, :, i].copy(), v[:, :, i].copy())
-            if pos < cfg.n_sink:
-                st.sink_k[:, :, pos] = k[:, :, i]
-                st.sink_v[:, :, pos] = v[:, :, i]
-        old_qend = self.q_end(layer)
-        st.L += n
-        new_qend = self.q_end(layer)
+        L0, L1 = st.L, st.L + n
+        for pos in range(L0, min(L1, cfg.n_sink)):
+            st.sink_k[:, :, pos] = k[:, :, pos - L0]
+            st.sink_v[:, :, pos] = v[:, :, pos - L0]
+        q0 = self.q_end(layer)
+        st.L = L1
+        q1 = self.q_end(layer)
+
+        def rows(p0, p1):
+            """K, V rows [B, H, p1-p0, D] of positions p0..p1-1 (stored or new)."""
+            if p0 >= L0:
+                return k[:, :, p0 - L0:p1 - L0], v[:, :, p0 - L0:p1 - L0]
+            ks = [st.rows[p][0] if p < L0 else k[:, :, p - L0] for p in range(p0, p1)]
+            vs = [st.rows[p][1] if p < L0 else v[:, :, p - L0] for p in range(p0, p1)]
+            return np.stack(ks, axis=2), np.stack(vs, axis=2)
+
         if cfg.mode == "kivi":
-            for g in range(old_qend // GROUP, new_qend // GROUP):
-                self._quantize_group(layer, g)
-        else:
-            for pos in range(old_qend, new_qend):
-                self._quantize_token(layer, pos)
+            g0, g1 = q0 // GROUP, q1 // GROUP
+            if g1 > g0:
+                kr, vr = rows(GROUP * g0, GROUP * g1)
+                self._quantize_groups(layer, g0, kr, vr)
+        elif q1 > q0:
+            kr, vr = rows(q0, q1)
+            kc, kn = tq.quantize(kr, self.sgn, self.cb_k[0])
+            vc, vn = tq.quantize(vr, self.sgn, self.cb_v[0])
+            for i, pos in enumerate(range(q0, q1)):
+                st.tokens[pos] = (kc[:, :, i], kn[:, :, i], vc[:, :, i], vn[:, :, i])
+        # keep the exact rows still read from the tail or waiting for a group
         F = self.fp16_begin(layer)
         for pos in [p for p in st.rows if p < F]:
             del st.rows[pos]
+        for pos in range(max(F, L0), L1):
+            st.rows[pos] = (k[:, :, pos - L0].copy(), v[:, :, pos - L0].copy())
 
-    def _quantize_group(self, layer: int, g: int) -> None:
+    def _quantize_groups(self, layer: int, g0: int, kr: np.ndarray, vr: np.ndarray) -> None:
+        """Quantise consecutive groups g0.. from rows [B, H, 32 * ng, D]."""
         st, cfg = self.layers[layer], self.cfg
-        kr = np.stack([st.rows[GROUP * g + r][0] for r in range(GROUP)], axis=2)
-        vr = np.stack([st.rows[GROUP * g + r][1] for r in range(GROUP)], axis=2)
-        mask = np.zeros(cfg.batch, np.uint32)
+        B, H, T, D = kr.shape
+        ng = T // GROUP
+        kr = kr.reshape(B, H, ng, GROUP, D)
+        vr = vr.reshape(B, H, ng, GROUP, D)
+        masks = np.zeros((ng, B), np.uint32)
         if cfg.n_dyn_sinks and st.sink_pos is not None:
-            kr = kr.copy()
-            vr = vr.copy()
-            for b in range(cfg.batch):
-                rows = {int(p) - GROUP * g for p in st.sink_pos[b]
-                        if GROUP * g <= p < GROUP * (g + 1)}
-                for r in rows:
-                    mask[b] |= np.uint32(1 << r)
-                if rows:
-                    kr[b] = kvsink.exclude(kr[b], rows)
-                    vr[b] = kvsink.exclude(vr[b], rows)
-        kq, ks, kz = kivi.quantize_k_group(kr, cfg.k_bits)
-        vq, vs, vz = kivi.quantize_v_rows(vr, cfg.v_bits)
-        st.groups[g] = dict(kq=kq, ks=ks, kz=kz, vq=vq, vs=vs, vz=vz, mask=mask)
-
-    def _quantize_token(self, layer: int, pos: int) -> None:
-        st = self.layers[layer]
-        kx, vx = st.rows[pos]
-        kc, kn = tq.quantize(kx, self.sgn, self.cb_k[0])
-        vc, vn = tq.quantize(vx, self.sgn, self.cb_v[0])
-        st.tokens[pos] = (kc, kn, vc, vn)
+            hit = sorted({int(p) // GROUP - g0 for p in st.sink_pos.ravel()
+                          if 0 <= int(p) // GROUP - g0 < ng})
+            if hit:
+                kr = kr.copy()
+                vr = vr.copy()
+            for i in hit:
+                g = g0 + i
+                for b in range(B):
+                    sink_rows = {int(p) - GROUP * g for p in st.sink_pos[b]
+                                 if GROUP * g <= p < GROUP * (g + 1)}
+                    for r in sink_rows:
+                        masks[i, b] |= np.uint32(1 << r)
+                    if sink_rows:
+                        kr[b, :, i] = kvsink.exclude(kr[b, :, i], sink_rows)
+                        vr[b, :, i] = kvsink.exclude(vr[b, :, i], sink_rows)
+        kq, ks, kz = kivi.quantize_k_group(kr, cfg.k_bits)      # [B,H,ng,32,D], [B,H,ng,D]
+        vq, vs, vz = kivi.quantize_v_rows(vr, cfg.v_bits)       # [B,H,ng,32,D], [B,H,ng,32,D/32]
+        for i in range(ng):
+            st.groups[g0 + i] = dict(kq=kq[:, :, i], ks=ks[:, :, i], kz=kz[:, :, i],
+                                     vq=vq[:, :, i], vs=vs[:, :, i], vz=vz[:, :, i],
+                                     mask=masks[i])
 
     # ------------------------------------------------------------ eviction
     def evict(self, layer: int):

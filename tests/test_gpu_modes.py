@@ -1,0 +1,150 @@
+"""GPU parity of the StreamingLLM ring (eviction + RoPE), TurboQuant and
+KVSink modes against the oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+from bit_kv_cache_append_gb300 import workloads as W
+from tests.parity import cache_kwargs, compare_attention, compare_exports, oracle_config, torch_act
+
+pytestmark = pytest.mark.gpu
+
+
+def _pair(kw):
+    from bit_kv_cache_append_gb300.binding import KVCache
+    from oracle import OracleCache
+    return KVCache(**kw), OracleCache(oracle_config(kw))
+
+
+def _decode_both(gc, oc, layer, q, act, heads=None):
+    import torch
+    out = gc.decode_attn(layer, torch_act(q, act))
+    torch.cuda.synchronize()
+    gc.check_device_error()
+    o_ref, _ = oc.decode_attn(layer, q, heads=heads)
+    return compare_attention(out.cpu().numpy(), o_ref, heads)
+
+
+# ------------------------------------------------------------------ ring
+
+@pytest.mark.parametrize("name", ["ring_int8", "ring_int4"])
+def test_ring_stream_with_rope_and_eviction(name):
+    """Shortened StreamingLLM stream: 2 layers, per step append 1 -> evict ->
+    decode; identical eviction ranges, codes and attention."""
+    w = W.scaled(W.WORKLOADS[name], batch=4, n_kv_heads=4, n_q_heads=4, evict_window=96, n_layers=2)
+    steps = 400
+    kw = cache_kwargs(w, 96 + 64, rope_max_pos=steps)
+    gc, oc = _pair(kw)
+    ranges_g, ranges_o = [], []
+    for t in range(steps):
+        for layer in range(2):
+            k, v = W.kv_tokens(w, 3, 1, layer=layer, first_pos=t)
+            gc.append(layer, torch_act(k, "f16"), torch_act(v, "f16"))
+            oc.append(layer, k, v)
+            ranges_g.append(gc.evict(layer))
+            ranges_o.append(oc.evict(layer))
+            if t % 37 == 5 or t == steps - 1:
+                _decode_both(gc, oc, layer, W.queries(w, 3, t), "f16")
+    assert ranges_g == ranges_o
+    for layer in range(2):
+        compare_exports(gc, oc, layer)
+
+
+def test_rope_table_matches_oracle():
+    from oracle import rope
+    w = W.scaled(W.WORKLOADS["ring_int8"], batch=1, n_layers=1)
+    gc, _ = _pair(cache_kwargs(w, 4096, rope_max_pos=70000))
+    tab = gc.export(0, "rope")
+    pos = [0, 1, 2, 3, 100, 4095, 4096, 65535, 69999]
+    assert np.array_equal(tab[pos], rope.cos_sin(pos, 64, 10000.0))
+
+
+def test_ring_capacity_requires_eviction():
+    from bit_kv_cache_append_gb300.binding import KVError, KV_ERR_CAPACITY
+    w = W.scaled(W.WORKLOADS["ring_int4"], batch=1, n_kv_heads=1, n_q_heads=1, evict_window=64, n_layers=1)
+    gc, _ = _pair(cache_kwargs(w, 128, rope_max_pos=1000))
+    for t in range(128):
+        k, v = W.kv_tokens(w, 4, 1, first_pos=t)
+        gc.append(0, torch_act(k, "f16"), torch_act(v, "f16"))
+    with pytest.raises(KVError) as e:
+        gc.append(0, torch_act(k, "f16"), torch_act(v, "f16"))
+    assert e.value.status == KV_ERR_CAPACITY
+    gc.evict(0)
+    gc.append(0, torch_act(k, "f16"), torch_act(v, "f16"))
+
+
+# ------------------------------------------------------------------ TurboQuant
+
+@pytest.mark.parametrize("D", [128, 64])
+@pytest.mark.parametrize("kb,vb", [(4, 2), (4, 4), (2, 2)])
+def test_turboquant_codes_and_attention(kb, vb, D):
+    w = W.scaled(W.WORKLOADS["turboquant_k4v2"], batch=2, n_kv_heads=2, n_q_heads=8, head_dim=D,
+                 k_bits=kb, v_bits=vb)
+    kw = cache_kwargs(w, 1024, seed=1234)
+    gc, oc = _pair(kw)
+    assert np.array_equal(gc.export(0, "tq_signs"), oc.sgn)
+    for which, bits in (("codebook_k", kb), ("codebook_v", vb)):
+        cb = gc.export(0, which)
+        bnd, cen = oc.cb_k if which == "codebook_k" else oc.cb_v
+        assert np.array_equal(cb[: (1 << bits) - 1], bnd), which
+        assert np.array_equal(cb[(1 << bits) - 1:], cen), which
+    k, v = W.kv_tokens(w, 6, 700)
+    gc.prefill_quantize(0, torch_act(k, "f16"), torch_act(v, "f16"))
+    oc.prefill_quantize(0, k, v)
+    for i in range(5):
+        k, v = W.kv_tokens(w, 6, 1 + 10 * i, first_pos=700 + i)
+        gc.append(0, torch_act(k, "f16"), torch_act(v, "f16"))
+        oc.append(0, k, v)
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 6), "f16")
+
+
+def test_turboquant_zero_rows():
+    w = W.scaled(W.WORKLOADS["turboquant_k4v4"], batch=1, n_kv_heads=2, n_q_heads=2)
+    gc, oc = _pair(cache_kwargs(w, 256))
+    k, v = W.kv_tokens(w, 2, 64)
+    k[:, :, 10] = 0.0
+    v[:, :, 11] = 0.0
+    gc.prefill_quantize(0, torch_act(k, "f16"), torch_act(v, "f16"))
+    oc.prefill_quantize(0, k, v)
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 2), "f16")
+
+
+# ------------------------------------------------------------------ KVSink
+
+@pytest.mark.parametrize("T", [4096, 1000, 37])
+def test_kvsink_selection_exclusion_and_attention(T):
+    w = W.scaled(W.WORKLOADS["kvsink"], batch=2, context=T)
+    kw = cache_kwargs(w, 8192)
+    gc, oc = _pair(kw)
+    k, v = W.kv_tokens(w, 12, T)
+    gc.prefill_quantize(0, torch_act(k, "f16"), torch_act(v, "f16"))
+    oc.prefill_quantize(0, k, v)
+    if T >= 5:
+        assert np.array_equal(gc.export(0, "sink_pos"), W.sink_positions(12, 2, T))
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 12), "f16")
+    for i in range(40):   # decode-time appends flush groups that may hold sinks
+        k, v = W.kv_tokens(w, 12, 1, first_pos=T + i)
+        gc.append(0, torch_act(k, "f16"), torch_act(v, "f16"))
+        oc.append(0, k, v)
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 13), "f16")
+
+
+def test_kvsink_ties_and_residual_sinks():
+    """Equal key norms go to the lower position; a sink still in the residual
+    is read from the tail until its group is quantised."""
+    w = W.scaled(W.WORKLOADS["kvsink"], batch=1, n_kv_heads=2, n_q_heads=8, context=100)
+    kw = cache_kwargs(w, 512, n_dyn_sinks=3)
+    gc, oc = _pair(kw)
+    rng = np.random.default_rng(0)
+    k = rng.standard_normal((1, 2, 100, 128)).astype(np.float16).astype(np.float32)
+    v = rng.standard_normal((1, 2, 100, 128)).astype(np.float16).astype(np.float32)
+    for p in (7, 40, 70, 97):            # equal rows -> equal norms
+        k[:, :, p] = 30.0
+    gc.prefill_quantize(0, torch_act(k, "f16"), torch_act(v, "f16"))
+    oc.prefill_quantize(0, k, v)
+    assert list(gc.export(0, "sink_pos")[0]) == [7, 40, 70]
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 1), "f16")
