@@ -64,7 +64,7 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms during the timed region."""
+    """nvidia-smi sampled every 20 ms during the timed region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -78,7 +78,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -140,55 +140,71 @@ def append_bytes(w):
     return 2 * (B * H * D * 2) * 2
 
 
-def cpu_baseline(n_pairs=2, seed=7):
-    """The oracle as it stands, on a bounded sample: n_pairs (b, kv head)
-    units of the workload (one KV head with its 4 query heads, 32767-token
-    prefill + 1 append), timing the decode attention. Returns GB/s over the
-    sample's algorithmic bytes."""
+def oracle_sequence(seed=7):
+    """One sequence of the workload (all 8 KV heads, 32767-token prefill and
+    one append) in the CPU oracle."""
     import numpy as np
+    import torch
     from oracle import CacheConfig, OracleCache
     w = WORKLOAD
-    L = w["context"]
-    total_bytes, total_t = 0, 0.0
-    for i in range(n_pairs):
-        rng = np.random.default_rng(seed + i)
-        fac = np.exp(rng.uniform(0, math.log(75.0), size=w["head_dim"])).astype(np.float32)
-        k = (rng.standard_normal((1, 1, L, w["head_dim"]), dtype=np.float32) * fac)
-        v = rng.standard_normal((1, 1, L, w["head_dim"]), dtype=np.float32)
-        q = rng.standard_normal((1, 4, w["head_dim"]), dtype=np.float32)
-        import torch
-        rb = lambda x: torch.from_numpy(x).to(torch.bfloat16).float().numpy()
-        k, v, q = rb(k), rb(v), rb(q)
-        oc = OracleCache(CacheConfig(n_layers=1, batch=1, n_kv_heads=1, n_q_heads=4, head_dim=w["head_dim"],
-                                     max_tokens=L + 64, k_bits=w["k_bits"], v_bits=w["v_bits"],
-                                     n_sink=w["n_sink"], window=w["window"], act_dtype="bf16"))
-        oc.prefill_quantize(0, k, v)
-        t0 = time.perf_counter()
+    L, H, D = w["context"], w["n_kv_heads"], w["head_dim"]
+    rng = np.random.default_rng(seed)
+    fac = np.exp(rng.uniform(0, math.log(75.0), size=(H, D))).astype(np.float32)
+    rb = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).float().numpy()
+    k = rb(rng.standard_normal((1, H, L, D), dtype=np.float32) * fac[None, :, None, :])
+    v = rb(rng.standard_normal((1, H, L, D), dtype=np.float32))
+    q = rb(rng.standard_normal((1, w["n_q_heads"], D), dtype=np.float32))
+    oc = OracleCache(CacheConfig(n_layers=1, batch=1, n_kv_heads=H, n_q_heads=w["n_q_heads"], head_dim=D,
+                                 max_tokens=L + 64, k_bits=w["k_bits"], v_bits=w["v_bits"],
+                                 n_sink=w["n_sink"], window=w["window"], act_dtype="bf16"))
+    oc.prefill_quantize(0, k[:, :, : L - 1], v[:, :, : L - 1])
+    oc.append(0, k[:, :, L - 1:], v[:, :, L - 1:])
+    return oc, q
+
+
+def unit_bytes(oc):
+    """Algorithmic bytes of one (sequence, KV head) unit of the oracle cache."""
+    s = oc.stats(0)
+    H, D, g = oc.cfg.n_kv_heads, oc.cfg.head_dim, oc.g
+    cache = s["code_bytes"] + s["kmeta_bytes"] + s["vmeta_bytes"] + s["sink_bytes"] + s["tail_bytes"]
+    return cache / H + g * D * (2 + 4)
+
+
+def cpu_baseline(repeats=6, seed=7):
+    """The oracle as it stands, on a bounded sample: one sequence of the
+    workload (8 KV-head units, 32 query heads) decoded `repeats` times.
+    Returns (GB/s over the sample's algorithmic bytes, seconds, units)."""
+    oc, q = oracle_sequence(seed)
+    t0 = time.perf_counter()
+    for _ in range(repeats):
         oc.decode_attn(0, q)
-        total_t += time.perf_counter() - t0
-        s = oc.stats(0)
-        total_bytes += (s["code_bytes"] + s["kmeta_bytes"] + s["vmeta_bytes"] + s["sink_bytes"]
-                        + s["tail_bytes"] + 4 * w["head_dim"] * 2 + 4 * w["head_dim"] * 4)
-    return total_bytes / total_t / 1e9, total_t, n_pairs
+    t = time.perf_counter() - t0
+    units = repeats * oc.cfg.n_kv_heads
+    return units * unit_bytes(oc) / t / 1e9, t, units
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle on the bench's workload; each step is
+    the decode of one (sequence, KV head) unit with its 4 query heads."""
     if rank != 0:
         return
-    steps_t = []
+    oc, q = oracle_sequence(11)
+    heads = [(0, j) for j in range(oc.g)]
+    ts = []
     for s in range(args.warmup + args.steps):
-        gbs, t, n = cpu_baseline(n_pairs=1, seed=100 + s)
+        t0 = time.perf_counter()
+        oc.decode_attn(0, q, heads=heads)
         if s >= args.warmup:
-            steps_t.append((gbs, t))
-    value = statistics.mean(g for g, _ in steps_t)
-    ms = statistics.mean(t for _, t in steps_t) * 1e3
+            ts.append(time.perf_counter() - t0)
+    ms = statistics.mean(ts) * 1e3
+    value = unit_bytes(oc) / (ms / 1e3) / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD_NAME,
-                       "sample": "per step: one (sequence, KV head) unit with its 4 query heads, decode only"},
+                       "sample": "per step: decode of one (sequence, KV head) unit with its 4 query heads"},
             "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": "one (b, kv-head) unit per step, 32768-token context"},
+                             "sample": "one (sequence, KV head) unit per step, 32768-token context, decode only"},
             "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -205,7 +221,7 @@ def run_ours(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
         pg = dist
-    w = WORKLOAD
+    w = dict(WORKLOAD, batch=args.batch)
     L = w["context"]
     n_steps_total = args.warmup + args.steps + 2
     cache = binding.KVCache(device=dev, n_layers=1, batch=w["batch"], n_kv_heads=w["n_kv_heads"],
@@ -274,6 +290,11 @@ def run_ours(args, rank, world, local):
     kernel_avg_ms = statistics.mean(kernel_ms)
     cache.check_device_error()
 
+    if args.skip_extras:
+        if rank == 0:
+            print(json.dumps({"ms_per_step": ms_total / args.steps, "kernel_us": kernel_avg_ms * 1e3,
+                              "decode_bytes": int(dec_bytes), "launches": int(launches)}), flush=True)
+        return
     # e2e: host buffers through the public API, copies inside the timed region
     hk = nk[: args.steps].cpu().pin_memory()
     hv = nv[: args.steps].cpu().pin_memory()
@@ -327,7 +348,7 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = measured_peaks()
     achieved = dec_bytes / (kernel_avg_ms / 1e3) / 1e9
     if rank == 0:
-        cpu_gbs, cpu_t, cpu_n = cpu_baseline(n_pairs=2)
+        cpu_gbs, cpu_t, cpu_n = cpu_baseline(repeats=args.cpu_repeats)
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
@@ -348,8 +369,8 @@ def run_ours(args, rank, world, local):
                          "algorithmic_bytes_per_launch": int(dec_bytes), "peak_kind": f"{peak_kind} hbm_gbs",
                          "kernel_us": round(kernel_avg_ms * 1e3, 2)},
             "cpu_baseline": {"value": round(cpu_gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{cpu_n} (b, kv-head) units with 4 query heads each, 32768-token "
-                                       f"context, decode only ({cpu_t:.1f} s)"},
+                             "sample": f"{cpu_n} (sequence, KV head) units with 4 query heads each, "
+                                       f"32768-token context, decode only ({cpu_t:.1f} s)"},
             "e2e": {"value": round(world * step_bytes / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
             "gpu_launches": int(launches),
@@ -363,9 +384,15 @@ def run_ours(args, rank, world, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=WORKLOAD["batch"],
+                    help="sequences (the workload has 16; smaller values give profiling cases)")
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="time the steps only (no e2e, copy or CPU legs); prints a short line")
+    ap.add_argument("--cpu-repeats", type=int, default=6,
+                    help="decodes of one oracle sequence (8 KV-head units each) in the CPU sample")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.warmup < 3:

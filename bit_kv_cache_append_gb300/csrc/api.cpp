@@ -58,6 +58,7 @@ struct kv_cache {
   int device = 0;
   int sm_count = 0;
   int split_ctas_per_sm = 4;
+  int stream_ctas = 0;  // 0: SM count x occupancy
   std::vector<LayerState> layers;
   cudaEvent_t ev0 = nullptr, ev1 = nullptr;
 };
@@ -311,6 +312,7 @@ kv_status kv_cache_create(const kv_cache_config* cfg, void* device_arena, size_t
   cudaError_t e = cudaGetDevice(&c->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
   if (const char* env = std::getenv("KVQ_SPLIT_CTAS_PER_SM")) c->split_ctas_per_sm = std::max(1, std::atoi(env));
+  if (const char* env = std::getenv("KVQ_STREAM_CTAS")) c->stream_ctas = std::max(0, std::atoi(env));
   // host-built tables
   std::vector<float> tmp;
   if (e == cudaSuccess && g.rope_max_pos) {
@@ -412,11 +414,13 @@ kv_status kv_decode_attn(kv_cache* cache, int layer, const void* q, float* out, 
   a.n_sink_read = static_cast<int>(std::min<int64_t>(std::min<int64_t>(g.n_sink, ls.L), a.F));
   a.n_dyn_sel = ls.n_dyn_sel;
   a.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(g.D)));
+  const int64_t units = static_cast<int64_t>(g.B) * g.H;
   if (a.F > a.qlo) {
     a.g_begin = a.qlo / kGroup;
     const int64_t g_end = (a.F + kGroup - 1) / kGroup;
     a.n_groups = static_cast<int>(g_end - a.g_begin);
-    const int64_t units = static_cast<int64_t>(g.B) * g.H;
+    a.work = units * a.n_groups;
+    // TurboQuant partitions: about split_ctas_per_sm CTAs per SM in total
     const int64_t target = static_cast<int64_t>(cache->sm_count) * cache->split_ctas_per_sm;
     int64_t splits = (target + units - 1) / units;
     splits = std::max<int64_t>(1, std::min<int64_t>({splits, g.max_splits, a.n_groups}));
@@ -425,11 +429,15 @@ kv_status kv_decode_attn(kv_cache* cache, int layer, const void* q, float* out, 
   } else {
     a.g_begin = 0;
     a.n_groups = 0;
+    a.work = 0;
     a.groups_per_split = 0;
     a.n_splits = 0;
   }
+  a.n_ctas_hint = cache->stream_ctas;
+  a.ns = g.max_splits + 1;
   int64_t launches = 0;
-  cudaError_t e = kvq::launch_decode(a, static_cast<cudaStream_t>(cuda_stream), cache->ev0, cache->ev1, &launches);
+  cudaError_t e = kvq::launch_decode(a, static_cast<cudaStream_t>(cuda_stream), cache->ev0, cache->ev1,
+                                     cache->sm_count, &launches);
   g_launches += launches;
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return KV_OK;
@@ -659,7 +667,6 @@ kv_status kv_cache_export(kv_cache* cache, int layer, int what, void* host_dst, 
             if (g.mode_tq) {
               std::memcpy(o, reg, static_cast<size_t>(ntok) * rowb);
             } else {
-              const int wpl = static_cast<int>(D) * bits / 32;
               const uint32_t mask = (1u << bits) - 1;
               for (int lane = 0; lane < 32; ++lane)
                 for (int f = 0; f < D; ++f) {
@@ -668,22 +675,23 @@ kv_status kv_cache_export(kv_cache* cache, int layer, int what, void* host_dst, 
                   else kvq::v_frag_pos(static_cast<int>(D), lane, f, &tok, &ch);
                   kvq::frag_bits(bits, f, &w, &bit);
                   uint32_t word;
-                  std::memcpy(&word, reg + (lane * wpl + w) * 4, 4);
+                  std::memcpy(&word, reg + kvq::code_word_offset(lane, w), 4);
                   const uint32_t code = (word >> bit) & mask;
                   o[tok * rowb + ch * bits / 8] |= static_cast<uint8_t>(code << ((ch % (8 / bits)) * bits));
                 }
             }
           } else if (what == KV_EXPORT_K_SCALE || what == KV_EXPORT_K_ZERO) {
             uint16_t* o = reinterpret_cast<uint16_t*>(dst) + (bh * p.G + gi) * D;
-            const int half = what == KV_EXPORT_K_ZERO;
-            for (int ch = 0; ch < D; ++ch) std::memcpy(o + ch, chunk.data() + g.chunk.kmeta_off + ch * 4 + half * 2, 2);
+            const int plane = what == KV_EXPORT_K_ZERO ? static_cast<int>(D) : 0;
+            for (int ch = 0; ch < D; ++ch)
+              std::memcpy(o + ch, chunk.data() + g.chunk.kmeta_off + (plane + kvq::kmeta_pos(static_cast<int>(D), ch)) * 2, 2);
           } else if (what == KV_EXPORT_V_SCALE || what == KV_EXPORT_V_ZERO) {
             const int nv = static_cast<int>(D) / kGroup;
             uint16_t* o = reinterpret_cast<uint16_t*>(dst) + (bh * p.n + gi * kGroup) * nv;
-            const int half = what == KV_EXPORT_V_ZERO;
+            const int plane = what == KV_EXPORT_V_ZERO ? nv : 0;
             for (int r = 0; r < kGroup; ++r)
               for (int vg = 0; vg < nv; ++vg)
-                std::memcpy(o + r * nv + vg, chunk.data() + g.chunk.vmeta_off + (r * nv + vg) * 4 + half * 2, 2);
+                std::memcpy(o + r * nv + vg, chunk.data() + g.chunk.vmeta_off + (r * 2 * nv + plane + vg) * 2, 2);
           } else if (what == KV_EXPORT_K_NORM || what == KV_EXPORT_V_NORM) {
             float* o = reinterpret_cast<float*>(dst) + bh * p.n + gi * kGroup;
             const int off = what == KV_EXPORT_K_NORM ? g.chunk.kmeta_off : g.chunk.vmeta_off;

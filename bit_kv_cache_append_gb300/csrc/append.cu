@@ -90,11 +90,6 @@ __device__ __forceinline__ uint8_t quantize_code(float x, float s, float z, int 
   return static_cast<uint8_t>(q);
 }
 
-__device__ __forceinline__ uint32_t pack_half2_bits(__half lo, __half hi) {
-  return static_cast<uint32_t>(__half_as_ushort(lo)) |
-         (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
-}
-
 template <int D>
 __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
   constexpr int HALF = D / 2, NV = D / 32, CPR = HALF / 8;
@@ -178,7 +173,9 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
     float s, z;
     quantize_slice_params(mn, mx, G.kb, &sh, &zh, &s, &z);
     for (int r = 0; r < 32; ++r) ck[r][c] = quantize_code(xk[r][c], s, z, G.kb);
-    reinterpret_cast<uint32_t*>(chunk + G.chunk.kmeta_off)[c] = pack_half2_bits(sh, zh);
+    __half* km = reinterpret_cast<__half*>(chunk + G.chunk.kmeta_off);
+    km[kmeta_pos(D, c)] = sh;
+    km[D + kmeta_pos(D, c)] = zh;
   }
   {  // V: token r, channel group vg (index rotated by 8 vg to spread banks)
     const int r = tid / NV, vg = tid % NV, base = 32 * vg;
@@ -195,7 +192,9 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
       const int c = base + ((i + 8 * vg) & 31);
       cv[r][c] = quantize_code(xv[r][c], s, z, G.vb);
     }
-    reinterpret_cast<uint32_t*>(chunk + G.chunk.vmeta_off)[r * NV + vg] = pack_half2_bits(sh, zh);
+    __half* vm = reinterpret_cast<__half*>(chunk + G.chunk.vmeta_off) + r * 2 * NV;
+    vm[vg] = sh;
+    vm[NV + vg] = zh;
   }
   __syncthreads();
 
@@ -210,7 +209,7 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
       frag_bits(G.kb, f, &wd, &bit);
       word |= static_cast<uint32_t>(ck[tok][ch]) << bit;
     }
-    reinterpret_cast<uint32_t*>(chunk + G.chunk.kc_off)[lane * kwpl + w] = word;
+    *reinterpret_cast<uint32_t*>(chunk + G.chunk.kc_off + code_word_offset(lane, w)) = word;
   }
   for (int wi = tid; wi < 32 * vwpl; wi += D) {
     const int lane = wi / vwpl, w = wi % vwpl, per = 32 / G.vb;
@@ -222,7 +221,7 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
       frag_bits(G.vb, f, &wd, &bit);
       word |= static_cast<uint32_t>(cv[tok][ch]) << bit;
     }
-    reinterpret_cast<uint32_t*>(chunk + G.chunk.vc_off)[lane * vwpl + w] = word;
+    *reinterpret_cast<uint32_t*>(chunk + G.chunk.vc_off + code_word_offset(lane, w)) = word;
   }
   if (G.n_dyn && h == 0 && tid == 0) a.lay.sink_mask[b * G.n_slots + slot] = smask;
 }

@@ -4,8 +4,8 @@
 
 namespace kvq {
 
-cudaError_t launch_kivi_d64(const DecodeArgs& a, cudaStream_t s);
-cudaError_t launch_kivi_d128(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_kivi_d64(DecodeArgs& a, cudaStream_t s, int sm_count);
+cudaError_t launch_kivi_d128(DecodeArgs& a, cudaStream_t s, int sm_count);
 
 namespace {
 
@@ -48,8 +48,8 @@ __global__ void __launch_bounds__(128) decode_tq_kernel(DecodeArgs a) {
   __shared__ float red[NW * kMaxGqa * (D + 2)];
   __shared__ float ck[16], cv[16];
   const Geometry& G = a.geo;
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  if (split == a.n_splits) {
+  const int split = static_cast<int>(blockIdx.x) - 1, h = blockIdx.y, b = blockIdx.z;
+  if (split < 0) {
     exact_partition<D>(a, b, h, red);
     return;
   }
@@ -132,7 +132,18 @@ __global__ void __launch_bounds__(128) decode_tq_kernel(DecodeArgs a) {
     }
   }
   __syncthreads();
-  write_partial<D, NW>(a, red, b, h, split);
+  write_partial<D, NW>(a, red, b, h, 1 + split);
+}
+
+// Number of partial slots of unit u (slot 0 = exact pools): stream-K parts
+// are the CTAs whose item ranges meet the unit's items.
+__device__ __forceinline__ int slots_of_unit(const DecodeArgs& a, int64_t u) {
+  if (a.geo.mode_tq) return a.n_splits + 1;
+  if (a.work <= 0 || a.n_groups <= 0) return 1;
+  const int64_t first = u * a.n_groups, last = first + a.n_groups - 1;
+  const int c0 = static_cast<int>(((first + 1) * a.n_ctas - 1) / a.work);
+  const int c1 = static_cast<int>(((last + 1) * a.n_ctas - 1) / a.work);
+  return 1 + (c1 - c0 + 1);
 }
 
 // One warp per (b, query head): combine the partials by log-sum-exp
@@ -145,8 +156,8 @@ __global__ void __launch_bounds__(128) merge_kernel(DecodeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + warp;
   if (row >= G.B * G.Hq) return;
-  const int ns = a.n_splits + 1;
-  const float* ml = a.part_ml + static_cast<size_t>(row) * ns * 2;
+  const int ns = slots_of_unit(a, row / G.Hq * G.H + (row % G.Hq) / G.gqa);
+  const float* ml = a.part_ml + static_cast<size_t>(row) * a.ns * 2;
   float M = -INFINITY;
   for (int s = lane; s < ns; s += 32) M = fmaxf(M, ml[2 * s]);
 #pragma unroll
@@ -159,7 +170,7 @@ __global__ void __launch_bounds__(128) merge_kernel(DecodeArgs a) {
     if (ms == -INFINITY) continue;
     const float w = exp2f(ms - M);
     L += ml[2 * s + 1] * w;
-    const float* po = a.part_o + (static_cast<size_t>(row) * ns + s) * D;
+    const float* po = a.part_o + (static_cast<size_t>(row) * a.ns + s) * D;
 #pragma unroll
     for (int i = 0; i < NS; ++i) o[i] = fmaf(po[i * 32 + lane], w, o[i]);
   }
@@ -179,13 +190,13 @@ __global__ void __launch_bounds__(128) merge_kernel(DecodeArgs a) {
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1,
+cudaError_t launch_decode(DecodeArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, int sm_count,
                           int64_t* launches) {
   const Geometry& G = a.geo;
   cudaError_t e;
   if (ev0) cudaEventRecord(ev0, s);
   if (!G.mode_tq) {
-    e = (G.D == 128) ? launch_kivi_d128(a, s) : launch_kivi_d64(a, s);
+    e = (G.D == 128) ? launch_kivi_d128(a, s, sm_count) : launch_kivi_d64(a, s, sm_count);
   } else {
     dim3 grid(a.n_splits + 1, G.H, G.B);
     if (G.D == 128) decode_tq_kernel<128><<<grid, 128, 0, s>>>(a);

@@ -110,14 +110,14 @@ __device__ __forceinline__ float query_value(const DecodeArgs& a, int b, int hq,
 }
 
 // Per-warp online-softmax states of one CTA merged through shared memory and
-// written as the CTA's partial: m (log2 units), l, and the unnormalised
-// output o[D] for each of the G query heads. `red` holds NW * G * (D + 2)
+// written as partial `slot` of each of the G query heads: m (log2 units), l,
+// and the unnormalised output o[D]. `red` holds NW * G * (D + 2)
 // floats: [w][j][0..D-1] = o, [w][j][D] = m, [w][j][D+1] = l.
 template <int D, int NW>
 __device__ __forceinline__ void write_partial(const DecodeArgs& a, const float* red, int b, int h,
-                                              int split) {
+                                              int slot) {
   const Geometry& G = a.geo;
-  const int ns = a.n_splits + 1;
+  const int ns = a.ns;
   for (int idx = threadIdx.x; idx < G.gqa * D; idx += NW * 32) {
     const int j = idx / D, c = idx % D;
     float M = -INFINITY;
@@ -133,7 +133,7 @@ __device__ __forceinline__ void write_partial(const DecodeArgs& a, const float* 
         l += r[D + 1] * sc;
       }
     }
-    const size_t row = (static_cast<size_t>(b) * G.Hq + h * G.gqa + j) * ns + split;
+    const size_t row = (static_cast<size_t>(b) * G.Hq + h * G.gqa + j) * ns + slot;
     a.part_o[row * D + c] = o;
     if (c == 0) {
       a.part_ml[row * 2 + 0] = M;
@@ -218,7 +218,7 @@ __device__ void exact_partition(const DecodeArgs& a, int b, int h, float* red) {
     }
   }
   __syncthreads();
-  write_partial<D, NW>(a, red, b, h, a.n_splits);
+  write_partial<D, NW>(a, red, b, h, 0);
 }
 
 }  // namespace kvq

@@ -2,5 +2,5 @@
 #include "decode_kivi.cuh"
 
 namespace kvq {
-cudaError_t launch_kivi_d64(const DecodeArgs& a, cudaStream_t s) { return launch_kivi_d<64>(a, s); }
+cudaError_t launch_kivi_d64(DecodeArgs& a, cudaStream_t s, int sm_count) { return launch_kivi_d<64>(a, s, sm_count); }
 }  // namespace kvq

@@ -57,9 +57,13 @@ struct DecodeArgs {
   float* lse;           // [B][Hq] or nullptr
   int64_t L, F, qlo;    // quantised segment [qlo, F), tail [F, L)
   int64_t g_begin;      // first group of the quantised segment
-  int n_groups;         // groups touching [qlo, F)
-  int groups_per_split;
-  int n_splits;         // quantised partitions; partition n_splits = exact pools
+  int n_groups;         // groups touching [qlo, F), per (sequence, KV head) unit
+  int64_t work;         // units * n_groups: the flat list the stream-K CTAs split
+  int n_ctas;           // stream-K CTAs (set at launch)
+  int n_ctas_hint;      // 0 = SM count x occupancy
+  int groups_per_split; // TurboQuant: groups per partition
+  int n_splits;         // TurboQuant: quantised partitions
+  int ns;               // partial slots per (sequence, query head); slot 0 = exact pools
   int n_sink_read;      // overlay: sink slots [0, n) read from the sink buffer
   int n_dyn_sel;        // KVSink: selected sinks (read when pos < F)
   float qscale;         // log2(e) / sqrt(D)
@@ -82,7 +86,7 @@ struct SinkSelectArgs {
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int64_t* launches);
 cudaError_t launch_sink_select(const SinkSelectArgs& a, cudaStream_t s, int64_t* launches);
 cudaError_t launch_sink_gather(const AppendArgs& a, cudaStream_t s, int64_t* launches);
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1,
+cudaError_t launch_decode(DecodeArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, int sm_count,
                           int64_t* launches);
 cudaError_t launch_copy(const void* src, void* dst, size_t bytes, cudaStream_t s,
                         int64_t* launches);

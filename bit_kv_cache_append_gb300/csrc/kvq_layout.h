@@ -3,8 +3,8 @@
 // by the kernels of the library (and by nothing else).
 //
 // A "chunk" holds one 32-token group of one (layer, b, kv-head):
-//   KIVI:       [K codes 32*D*kb/8][K meta D x (s,z) f16][V codes 32*D*vb/8]
-//               [V meta 32 x D/32 x (s,z) f16]
+//   KIVI:       [K codes 32*D*kb/8][K scales D f16][K zeros D f16]
+//               [V codes 32*D*vb/8][V meta 32 x (scales D/32 f16, zeros D/32 f16)]
 //   TurboQuant: [K codes 32 x D*kb/8 row-major][K norms 32 f32]
 //               [V codes 32 x D*vb/8 row-major][V norms 32 f32]
 // Chunk sizes are multiples of 16 bytes so one 1-D bulk copy moves a chunk.
@@ -12,18 +12,23 @@
 // KIVI codes are stored in the order the decode kernel's tensor-core
 // fragments consume them (the canonical, page-defined order is produced by
 // kv_cache_export). The 32 lanes of the consuming warp (lane = 4 g + t) own
-// D codes each, as a contiguous block of D*bits/8 bytes. Fragment element
-// f = 0 .. D-1 of a lane maps to a (token, channel) of the group:
+// D codes each. Fragment element f = 0 .. D-1 of a lane maps to a (token,
+// channel) of the group:
 //   K (A operand of S^T = K Q^T, m16n8k16, rows = tokens, k = channels):
 //     f = ((mt * S + s) * 4 + r) * 2 + e,  S = D/16, mt in {0,1}, r in 0..3
 //     token = 16 mt + g + 8 (r & 1);  channel = t D/4 + 4 s + 2 (r >> 1) + e
 //   V (A operand of O^T = V^T P^T, rows = channels, k = tokens):
 //     f = ((m * 2 + kb) * 4 + r) * 2 + e,  m in [0, D/16), kb in {0,1}
 //     channel = 16 m + g + 8 (r & 1);  token = 16 kb + 2 t + e + 8 (r >> 1)
-// Within a lane block, element f sits in 32-bit word f / (32/bits) at bit
+// Element f sits in 32-bit word w = f / (32/bits) of its lane at bit
 // bits * j + 16 e, j = (f % (32/bits)) / 2: the two elements of one f16x2
 // register are 16 bits apart, so a mask and an f16 magic-number OR turn a
-// pair of codes into an exact f16x2 value.
+// pair of codes into an exact f16x2 value. Words are interleaved across
+// lanes in 16-byte pieces (word w of lane L at byte ((w/4) * 32 + L) * 16 +
+// (w % 4) * 4) so that a warp's 16-byte loads are contiguous.
+// K scales and zeros are kept in the order the B operand is built: f16
+// position (u * 4 + t) * 8 + e holds channel t D/4 + 8 u + e (u = pair of
+// k-steps), so the four lanes t read one contiguous 64-byte run.
 #pragma once
 
 #include <cstddef>
@@ -49,7 +54,7 @@ KVQ_HD Chunk chunk_layout(int mode_tq, int D, int kb, int vb) {
   Chunk c;
   c.kc_off = 0;
   c.kmeta_off = kGroup * D * kb / 8;
-  if (!mode_tq) {
+  if (!mode_tq) {  // K meta: D scales then D zeros (f16); V meta per token: D/32 scales, D/32 zeros
     c.vc_off = c.kmeta_off + 4 * D;
     c.vmeta_off = c.vc_off + kGroup * D * vb / 8;
     c.bytes = c.vmeta_off + 4 * D;
@@ -78,6 +83,15 @@ KVQ_HD void v_frag_pos(int D, int lane, int f, int* token, int* channel) {
   const int m = mk >> 1, kb = mk & 1;
   *channel = 16 * m + g + 8 * (r & 1);
   *token = 16 * kb + 2 * t + e + 8 * (r >> 1);
+}
+
+// Byte offset of 32-bit word w of lane `lane` inside a code region.
+KVQ_HD int code_word_offset(int lane, int w) { return (((w >> 2) * 32 + lane) << 4) + ((w & 3) << 2); }
+
+// f16 position of channel c inside the K scale (or zero) array.
+KVQ_HD int kmeta_pos(int D, int c) {
+  const int q = D / 4, t = c / q, r = c % q;
+  return ((r >> 3) * 4 + t) * 8 + (r & 7);
 }
 
 // Word index and bit position of element f inside a lane block.
