@@ -434,6 +434,12 @@ kv_status kv_decode_attn(kv_cache* cache, int layer, const void* q, float* out, 
     a.n_splits = 0;
   }
   a.n_ctas_hint = cache->stream_ctas;
+  a.h2_magic = 0x64006400u;  // f16 1024.0 in both halves
+  for (int k = 0; k < 9; ++k) {  // 2^-k and -1024 * 2^-k as f16x2 (exact powers of two)
+    const uint32_t sc = static_cast<uint32_t>(15 - k) << 10, of = 0x8000u | (static_cast<uint32_t>(25 - k) << 10);
+    a.h2_scale[k] = sc | (sc << 16);
+    a.h2_offset[k] = of | (of << 16);
+  }
   a.ns = g.max_splits + 1;
   int64_t launches = 0;
   cudaError_t e = kvq::launch_decode(a, static_cast<cudaStream_t>(cuda_stream), cache->ev0, cache->ev1,
@@ -682,9 +688,12 @@ kv_status kv_cache_export(kv_cache* cache, int layer, int what, void* host_dst, 
             }
           } else if (what == KV_EXPORT_K_SCALE || what == KV_EXPORT_K_ZERO) {
             uint16_t* o = reinterpret_cast<uint16_t*>(dst) + (bh * p.G + gi) * D;
-            const int plane = what == KV_EXPORT_K_ZERO ? static_cast<int>(D) : 0;
-            for (int ch = 0; ch < D; ++ch)
-              std::memcpy(o + ch, chunk.data() + g.chunk.kmeta_off + (plane + kvq::kmeta_pos(static_cast<int>(D), ch)) * 2, 2);
+            const bool zero = what == KV_EXPORT_K_ZERO;
+            for (int ch = 0; ch < D; ++ch) {
+              const int pos = zero ? static_cast<int>(D) + kvq::kzero_pos(static_cast<int>(D), ch)
+                                   : kvq::kmeta_pos(static_cast<int>(D), ch);
+              std::memcpy(o + ch, chunk.data() + g.chunk.kmeta_off + pos * 2, 2);
+            }
           } else if (what == KV_EXPORT_V_SCALE || what == KV_EXPORT_V_ZERO) {
             const int nv = static_cast<int>(D) / kGroup;
             uint16_t* o = reinterpret_cast<uint16_t*>(dst) + (bh * p.n + gi * kGroup) * nv;

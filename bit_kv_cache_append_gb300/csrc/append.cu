@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
     for (int r = 0; r < 32; ++r) ck[r][c] = quantize_code(xk[r][c], s, z, G.kb);
     __half* km = reinterpret_cast<__half*>(chunk + G.chunk.kmeta_off);
     km[kmeta_pos(D, c)] = sh;
-    km[D + kmeta_pos(D, c)] = zh;
+    km[D + kzero_pos(D, c)] = zh;
   }
   {  // V: token r, channel group vg (index rotated by 8 vg to spread banks)
     const int r = tid / NV, vg = tid % NV, base = 32 * vg;

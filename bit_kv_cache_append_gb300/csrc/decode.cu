@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(128) decode_tq_kernel(DecodeArgs a) {
   const Geometry& G = a.geo;
   const int split = static_cast<int>(blockIdx.x) - 1, h = blockIdx.y, b = blockIdx.z;
   if (split < 0) {
-    exact_partition<D>(a, b, h, red);
+    exact_partition<D, NW>(a, b, h, red);
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -24,14 +24,17 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+// Test for completion of phase `parity`; a thread whose phase is not complete
+// may be suspended for up to about a microsecond before the call returns
+// false, so waiting loops spin slowly.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)
       : "memory");
   return ok != 0;
 }
@@ -59,17 +62,31 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // D += A B with A 16x16 f16 (row), B 16x8 f16 (col), D 16x8 f32.
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Four 8x8 b16 matrices from shared memory into the MMA A-fragment layout;
+// lane L gives the address of row L % 8 of matrix L / 8.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* row_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(row_addr)));
+}
+
+// A value the compiler must keep in a register (it cannot re-derive it).
+__device__ __forceinline__ uint32_t pin(uint32_t x) {
+  uint32_t y;
+  asm volatile("mov.b32 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // Transpose of an 8x8 b16 matrix held one b32 per lane in the MMA layout.
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
 
@@ -111,22 +128,21 @@ __device__ __forceinline__ float query_value(const DecodeArgs& a, int b, int hq,
 
 // Per-warp online-softmax states of one CTA merged through shared memory and
 // written as partial `slot` of each of the G query heads: m (log2 units), l,
-// and the unnormalised output o[D]. `red` holds NW * G * (D + 2)
-// floats: [w][j][0..D-1] = o, [w][j][D] = m, [w][j][D+1] = l.
+// and the unnormalised output o[D]. NW warps do the writing; `red` holds
+// nrows * kMaxGqa * (D + 2) floats: [w][j][0..D-1] = o, [w][j][D] = m,
+// [w][j][D+1] = l.
 template <int D, int NW>
 __device__ __forceinline__ void write_partial(const DecodeArgs& a, const float* red, int b, int h,
-                                              int slot) {
+                                              int slot, int nrows = NW) {
   const Geometry& G = a.geo;
   const int ns = a.ns;
   for (int idx = threadIdx.x; idx < G.gqa * D; idx += NW * 32) {
     const int j = idx / D, c = idx % D;
     float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, red[(w * kMaxGqa + j) * (D + 2) + D]);
+    for (int w = 0; w < nrows; ++w) M = fmaxf(M, red[(w * kMaxGqa + j) * (D + 2) + D]);
     float o = 0.0f, l = 0.0f;
     if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
+      for (int w = 0; w < nrows; ++w) {
         const float* r = red + (w * kMaxGqa + j) * (D + 2);
         const float sc = (r[D] == -INFINITY) ? 0.0f : exp2f(r[D] - M);
         o += r[c] * sc;
@@ -144,11 +160,11 @@ __device__ __forceinline__ void write_partial(const DecodeArgs& a, const float* 
 
 // The exact pools of one (b, h): the sinks read from the sink buffer and the
 // tail [F, L) read from the ring, at fp32 with the query at full precision.
-// One warp per token in turn; lane l holds channels i*32 + l. `red` must hold
-// 4 * kMaxGqa * (D + 2) floats.
-template <int D>
+// NW warps take the tokens in turn; lane l holds channels i*32 + l. `red`
+// must hold NW * kMaxGqa * (D + 2) floats.
+template <int D, int NW>
 __device__ void exact_partition(const DecodeArgs& a, int b, int h, float* red) {
-  constexpr int NS = D / 32, NW = 4;
+  constexpr int NS = D / 32;
   const Geometry& G = a.geo;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = G.gqa;

@@ -3,14 +3,22 @@
 //
 // Work decomposition (stream-K): the quantised segment of every (sequence,
 // KV head) unit is a run of 32-token groups; all units' groups form one flat
-// list that is cut into n_ctas equal contiguous ranges, one per persistent
-// CTA (n_ctas a multiple of the SM count). A CTA walks its range unit by
-// unit; for each unit it touches, its 4 warps take the unit's groups in turn
-// (w, w+4, ...) with private online-softmax states that the CTA merges into
-// one partial (max, sum, unnormalised output) per query head. The first
-// B*Hkv CTAs instead handle the exact pools of one unit each (sinks and
-// tail, exact_partition). The LSE merge kernel combines every partial of a
-// (sequence, query head).
+// list cut into n_ctas equal contiguous ranges, one per persistent CTA
+// (n_ctas = SM count x resident CTAs). A CTA walks its range unit by unit;
+// for each unit it touches, its 4 warp pairs take the unit's groups in turn
+// (p, p+4, ...) and the CTA merges the pairs into one partial (max, sum,
+// unnormalised output) per query head. The first B*Hkv CTAs instead handle
+// the exact pools of one unit each (sinks and tail, exact_partition). The
+// LSE merge kernel combines every partial of a (sequence, query head).
+//
+// Warp specialisation: a pair is a QK warp and a PV warp working on the same
+// group stream. The QK warp turns the K codes into scores and softmax
+// weights and hands the weights (and the rescale factor of the running max)
+// to the PV warp through a double-buffered shared-memory slot; the PV warp
+// turns the V codes into the weighted sum and, being the last reader of each
+// staged chunk, refills the stage with the next 1-D bulk copy. Each role
+// keeps only its own operands in registers, so more warps fit per SM and the
+// two halves of a group's dependency chain overlap across groups.
 //
 // Per group, on the tensor cores (mma.sync m16n8k16, f16 in, f32 out):
 //   scores^T [32 tokens x 8 cols] = zeros-row . q + codes_K [32 x D] . qt
@@ -24,15 +32,12 @@
 // The codes enter the MMA exactly (small integers in f16). The 8 MMA columns
 // hold, for query head j, column 2j = the f16 value of the folded operand
 // and column 2j+1 its f16 residual, so each product is carried at about 22
-// bits and thread (g, t) of the C fragment owns query head t. The residual
-// of q * sK is formed exactly in f16 (an FMA returns q_hi * s - f16(q_hi * s)
-// without rounding), so building the operand costs four f16x2 instructions
-// per register.
+// bits and thread (g, t) of a C fragment owns query head t. The residuals of
+// q * sK and p * sV are formed exactly in f16 (an FMA returns
+// x_hi * s - f16(x_hi * s) without rounding).
 //
-// The group chunks (codes stored in fragment order, see kvq_layout.h) are
-// staged into shared memory by 1-D bulk copies (cp.async.bulk) on an
-// mbarrier, several stages deep per warp, prefetching across unit
-// boundaries; every wait is bounded.
+// Every wait is bounded; a wait that gives up raises the CTA's abort flag so
+// that every other wait of the CTA gives up at once.
 #pragma once
 
 #include "decode_common.cuh"
@@ -53,30 +58,65 @@ __device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t 
   return d;
 }
 
+// 2^x by the hardware approximation (relative error about 2^-22; -inf -> 0),
+// enough for softmax weights.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ __half2 as_h2(uint32_t x) { return *reinterpret_cast<__half2*>(&x); }
 __device__ __forceinline__ uint32_t as_u32(__half2 x) { return *reinterpret_cast<uint32_t*>(&x); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Conversion constants of one code width, pinned in registers once per
+// kernel: the f16x2 magic 1024.0 and, per shift k used by the width, the
+// scale 2^-k and the offset -1024 * 2^-k.
+template <int BITS>
+struct CodeConsts {
+  static constexpr int N = BITS == 2 ? 5 : (BITS == 4 ? 2 : 1);
+  uint32_t magic, scale[N], offset[N];
+  __device__ __forceinline__ void load(const DecodeArgs& a) {
+    magic = pin(a.h2_magic);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      scale[i] = pin(a.h2_scale[i * (BITS == 2 ? 2 : 4)]);
+      offset[i] = pin(a.h2_offset[i * (BITS == 2 ? 2 : 4)]);
+    }
+  }
+};
 
 // Pair j of a packed word (elements at bits BITS*j and BITS*j + 16) as an
 // exact f16x2 of the two codes. The code bits are OR-ed into the mantissa of
 // 1024.0 (0x6400), giving 1024 + c * 2^k exactly, and one f16x2 FMA by
 // 2^-k and -1024 * 2^-k leaves c exactly.
 template <int BITS>
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, int j) {
+__device__ __forceinline__ uint32_t code_pair(const CodeConsts<BITS>& k, uint32_t w, int j) {
   if (BITS == 2) {
     const int jj = j < 5 ? j : j - 5;
     const uint32_t x = j < 5 ? w : (w >> 10);
-    const uint32_t hv = (x & (0x00030003u << (2 * jj))) | 0x64006400u;
-    return hfma2_bits(hv, h2pow2(-2 * jj), h2negpow2(10 - 2 * jj));
+    const uint32_t hv = (x & (0x00030003u << (2 * jj))) | k.magic;
+    return as_u32(__hfma2(as_h2(hv), as_h2(k.scale[jj]), as_h2(k.offset[jj])));
   } else if (BITS == 4) {
     const int jj = j < 2 ? j : j - 2;
     const uint32_t x = j < 2 ? w : (w >> 8);
-    const uint32_t hv = (x & (0x000F000Fu << (4 * jj))) | 0x64006400u;
-    return hfma2_bits(hv, h2pow2(-4 * jj), h2negpow2(10 - 4 * jj));
+    const uint32_t hv = (x & (0x000F000Fu << (4 * jj))) | k.magic;
+    return as_u32(__hfma2(as_h2(hv), as_h2(k.scale[jj % CodeConsts<BITS>::N]), as_h2(k.offset[jj % CodeConsts<BITS>::N])));
   } else {
-    const uint32_t hv = __byte_perm(w, 0x6464u, static_cast<uint32_t>(j | 0x40 | ((j + 2) << 8) | 0x4000));
-    return hfma2_bits(hv, h2pow2(0), h2negpow2(10));
+    const uint32_t hv = __byte_perm(w, k.magic, static_cast<uint32_t>(j | 0x50 | ((j + 2) << 8) | 0x7000));
+    return as_u32(__hsub2(as_h2(hv), as_h2(k.magic)));
   }
 }
+
+#ifndef KVQ_LAZY_RESCALE
+#define KVQ_LAZY_RESCALE 8.0f
+#endif
+// Headroom (log2 units) the running softmax max may lag behind the scores.
+constexpr float kLazyRescale = KVQ_LAZY_RESCALE;
 
 template <int D, int KB, int VB>
 struct KiviTile {
@@ -85,12 +125,21 @@ struct KiviTile {
   static constexpr int VC = KMETA + 4 * D;
   static constexpr int VMETA = VC + 32 * D * VB / 8;
   static constexpr int CHUNK = VMETA + 4 * D;
-  static constexpr int NST = CHUNK <= 6144 ? 3 : 2;  // bulk-copy stages per warp
-  static constexpr int NW = 4;
-  static constexpr int RED_FLOATS = NW * kMaxGqa * (D + 2);
-  static constexpr size_t smem_bytes() {
-    return static_cast<size_t>(NW) * NST * CHUNK + NW * NST * 8 + RED_FLOATS * 4;
-  }
+  static constexpr int NP = 4;                          // warp pairs per CTA
+#ifndef KVQ_DECODE_STAGES
+  static constexpr int NST = CHUNK <= 6144 ? 4 : 3;      // bulk-copy stages per pair
+#else
+  static constexpr int NST = KVQ_DECODE_STAGES;
+#endif
+  static constexpr int PBUF = 32 * 16 + 16;              // weights (16 B per lane) + 4 rescale factors
+  // shared memory: stages | weight buffers | red | barriers | abort flag
+  static constexpr int OFF_PBUF = NP * NST * CHUNK;
+  static constexpr int OFF_RED = OFF_PBUF + NP * 2 * PBUF;
+  static constexpr int RED_FLOATS = 8 * kMaxGqa * (D + 2);  // also the exact partition's 8 warps
+  static constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
+  static constexpr int NBAR = NP * (NST + 4);             // full[NST], pfull[2], pempty[2]
+  static constexpr int OFF_ABORT = OFF_BAR + NBAR * 8;
+  static constexpr size_t smem_bytes() { return OFF_ABORT + 16; }
 };
 
 // CTA that owns flattened item i under the equal split of `work` items into
@@ -99,95 +148,122 @@ __device__ __forceinline__ int owner_cta(int64_t i, int64_t work, int n) {
   return static_cast<int>(((i + 1) * n - 1) / work);
 }
 
-// Walks the items of warp w inside its CTA's range [i0, i1): per unit (run of
-// ng items), the unit's items s + w, s + w + 4, ... where s is the first item
+// Walks the items of pair p inside its CTA's range [i0, i1): per unit (run of
+// ng items), the unit's items s + p, s + p + 4, ... where s is the first item
 // of the unit inside the range. The group index and its ring slot advance by
 // additions; divisions happen only when the walk enters a new unit.
 struct ItemCursor {
-  int64_t item;      // current item (-1: exhausted)
-  int64_t seg_end;   // end of the current unit inside the range
-  int64_t unit;
-  int64_t grp;       // absolute group index of `item`
-  int slot;          // grp mod n_slots
+  int64_t item;       // current item (-1: exhausted)
+  int64_t seg_end;    // end of the current unit inside the range
+  int64_t grp;        // absolute group index of `item`
+  int slot;           // grp mod n_slots
+  const uint8_t* ptr; // chunk of `item`
 
-  __device__ __forceinline__ void enter(int64_t s, int64_t i1, int64_t ng, int w, int64_t g_begin, int n_slots) {
+  __device__ __forceinline__ void enter(int64_t s, int64_t i1, int64_t ng, int w, int64_t g_begin, int n_slots,
+                                        const uint8_t* chunks, int chunk_bytes) {
     while (s < i1) {
       const int64_t u = s / ng;
       const int64_t e = (u + 1) * ng < i1 ? (u + 1) * ng : i1;
       if (s + w < e) {
         item = s + w;
         seg_end = e;
-        unit = u;
         grp = g_begin + (item - u * ng);
         slot = static_cast<int>(grp % n_slots);
+        ptr = chunks + (static_cast<size_t>(u) * n_slots + slot) * chunk_bytes;
         return;
       }
       s = e;
     }
     item = -1;
   }
-  __device__ __forceinline__ void advance(int64_t i1, int64_t ng, int w, int64_t g_begin, int n_slots) {
+  __device__ __forceinline__ void advance(int64_t i1, int64_t ng, int w, int64_t g_begin, int n_slots,
+                                          const uint8_t* chunks, int chunk_bytes) {
     if (item + 4 < seg_end) {
       item += 4;
       grp += 4;
       slot += 4;
-      while (slot >= n_slots) slot -= n_slots;
+      ptr += 4 * chunk_bytes;
+      while (slot >= n_slots) {
+        slot -= n_slots;
+        ptr -= static_cast<size_t>(n_slots) * chunk_bytes;
+      }
     } else {
-      enter(seg_end, i1, ng, w, g_begin, n_slots);
+      enter(seg_end, i1, ng, w, g_begin, n_slots, chunks, chunk_bytes);
     }
   }
 };
 
+// Bounded wait that also gives up when another warp of the CTA has given up.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+#ifndef KVQ_DECODE_MIN_CTAS
+#define KVQ_DECODE_MIN_CTAS 2
+#endif
+
 template <int D, int KB, int VB>
-__global__ void __launch_bounds__(128, 3) decode_kivi_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(DecodeArgs a) {
   using T = KiviTile<D, KB, VB>;
-  constexpr int NW = T::NW, NST = T::NST, CHUNK = T::CHUNK;
+  constexpr int NP = T::NP, NST = T::NST, CHUNK = T::CHUNK;
   constexpr int S = D / 16, MV = D / 16, NVG = D / 32;
   constexpr int KW = D * KB / 32, VW = D * VB / 32;
   constexpr int KPPW = 16 / KB, VPPW = 16 / VB;  // code pairs per 32-bit word
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * NST * CHUNK);
-  float* red = reinterpret_cast<float*>(smem + NW * NST * CHUNK + NW * NST * 8);
+  float* red = reinterpret_cast<float*>(smem + T::OFF_RED);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_ABORT);
 
   const Geometry& G = a.geo;
   const int n_exact = G.B * G.H;
   if (static_cast<int>(blockIdx.x) < n_exact) {
-    exact_partition<D>(a, blockIdx.x / G.H, blockIdx.x % G.H, red);
+    exact_partition<D, 8>(a, blockIdx.x / G.H, blockIdx.x % G.H, red);
     return;
   }
   const unsigned full = 0xffffffffu;
   const int cta = blockIdx.x - n_exact;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = warp & (NP - 1);
+  const bool is_pv = warp >= NP;
   const int g = lane >> 2, t = lane & 3;
   const int gq = G.gqa;
-  const int jc = g >> 1;          // query head of this lane's B column
-  const bool col_lo = g & 1;      // B column holds the residual part
   const int64_t ng = a.n_groups, work = a.work;
   const int64_t i0 = cta * work / a.n_ctas, i1 = (cta + 1) * work / a.n_ctas;
-
-  uint8_t* stages = smem + warp * NST * CHUNK;
-  uint64_t* wb = bars + warp * NST;
   const int n_slots = G.n_slots;
-  auto chunk_src = [&](const ItemCursor& c) {
-    return a.lay.chunks + (static_cast<size_t>(c.unit) * n_slots + c.slot) * CHUNK;
-  };
-  if (lane == 0) {
-#pragma unroll
-    for (int st = 0; st < NST; ++st) mbar_init(&wb[st], 1);
+
+  uint8_t* stages = smem + pair * NST * CHUNK;
+  uint8_t* pbuf = smem + T::OFF_PBUF + pair * 2 * T::PBUF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR) + pair * (NST + 4);
+  uint64_t* full_bar = bars;            // [NST] chunk landed
+  uint64_t* pfull = bars + NST;         // [2] weights written
+  uint64_t* pempty = bars + NST + 2;    // [2] weights read
+  if (threadIdx.x == 0) *abort_flag = 0;
+  if (is_pv && lane == 0) {
+    for (int i = 0; i < NST + 4; ++i) mbar_init(&bars[i], 1);
     mbar_fence_init();
   }
-  __syncwarp();
-  ItemCursor pc;  // producer: the next item whose chunk is to be fetched
-  pc.enter(i0, i1, ng, warp, a.g_begin, n_slots);
-  int issued = 0, consumed = 0;
-  if (lane == 0) {
+  __syncthreads();
+
+  ItemCursor pc;  // producer (PV lane 0): the next item whose chunk is to be fetched
+  int issued = 0;
+  if (is_pv && lane == 0) {
+    pc.enter(i0, i1, ng, pair, a.g_begin, n_slots, a.lay.chunks, CHUNK);
     for (int i = 0; i < NST && pc.item >= 0; ++i) {
-      mbar_expect_tx(&wb[i], CHUNK);
-      bulk_g2s(stages + i * CHUNK, chunk_src(pc), CHUNK, &wb[i]);
-      pc.advance(i1, ng, warp, a.g_begin, n_slots);
+      mbar_expect_tx(&full_bar[i], CHUNK);
+      bulk_g2s(stages + i * CHUNK, pc.ptr, CHUNK, &full_bar[i]);
+      pc.advance(i1, ng, pair, a.g_begin, n_slots, a.lay.chunks, CHUNK);
       ++issued;
     }
   }
+  int n_t = 0;  // groups this pair has processed (stage and buffer phases)
   bool failed = false;
 
   int64_t seg = i0;
@@ -195,239 +271,285 @@ __global__ void __launch_bounds__(128, 3) decode_kivi_kernel(DecodeArgs a) {
     const int64_t unit = seg / ng;
     const int64_t seg_e = (unit + 1) * ng < i1 ? (unit + 1) * ng : i1;
     const int b = static_cast<int>(unit / G.H), h = static_cast<int>(unit % G.H);
-    int64_t grp = a.g_begin + (seg - unit * ng) + warp;   // group of this warp's first item
-    int slot = static_cast<int>(grp % n_slots);
 
-    // query of this lane's B column at full precision, split as f16 hi + lo,
-    // for the lane's quarter of the channels (pairs of adjacent channels)
-    uint32_t qh[S][2], qa[S][2];
+    if (!is_pv) {
+      // ------------------------------------------------------------ QK warp
+      int64_t grp = a.g_begin + (seg - unit * ng) + pair;  // group of this pair's first item
+      int slot = static_cast<int>(grp % n_slots);
+      const int jc = g >> 1;        // query head of this lane's B column
+      const bool col_lo = g & 1;    // B column holds the residual part
+      uint32_t qh[S][2], qa[S][2];  // q of the lane's column: f16 value, and value-or-residual
 #pragma unroll
-    for (int s = 0; s < S; ++s)
+      for (int s = 0; s < S; ++s)
 #pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const int c0 = t * (D / 4) + 4 * s + 2 * p;
-        float x0 = 0.0f, x1 = 0.0f;
-        if (jc < gq) {
-          x0 = query_value(a, b, h * gq + jc, c0);
-          x1 = query_value(a, b, h * gq + jc, c0 + 1);
-        }
-        const uint32_t hi = f2_to_h2(x0, x1);
-        const float2 hf = h2_to_f2(hi);
-        const uint32_t lo = f2_to_h2(x0 - hf.x, x1 - hf.y);
-        qh[s][p] = hi;
-        qa[s][p] = col_lo ? lo : hi;
-      }
-
-    float m_run = -INFINITY, l_run = 0.0f;
-    float oacc[MV][4];
-    float zacc[NVG];
-#pragma unroll
-    for (int m = 0; m < MV; ++m) oacc[m][0] = oacc[m][1] = oacc[m][2] = oacc[m][3] = 0.0f;
-#pragma unroll
-    for (int v = 0; v < NVG; ++v) zacc[v] = 0.0f;
-
-    for (int64_t item = seg + warp; item < seg_e && !failed; item += 4) {
-      const int st = consumed % NST;
-      const bool ok = mbar_wait_bounded(&wb[st], static_cast<uint32_t>((consumed / NST) & 1));
-      if (__any_sync(full, !ok)) {
-        failed = true;
-        break;
-      }
-      const uint8_t* tile = stages + st * CHUNK;
-
-      uint32_t kr[KW], vr[VW];
-#pragma unroll
-      for (int i = 0; i < KW / 4; ++i)
-        *reinterpret_cast<uint4*>(&kr[4 * i]) = reinterpret_cast<const uint4*>(tile)[i * 32 + lane];
-#pragma unroll
-      for (int i = 0; i < VW / 4; ++i)
-        *reinterpret_cast<uint4*>(&vr[4 * i]) = reinterpret_cast<const uint4*>(tile + T::VC)[i * 32 + lane];
-
-      // scores^T: zero-point row first, then codes_K . qt
-      float sc[2][4];
-      {
-        const uint4* ks = reinterpret_cast<const uint4*>(tile + T::KMETA);
-        const uint4* kz = reinterpret_cast<const uint4*>(tile + T::KMETA + 2 * D);
-        uint32_t bq[S][2];
-        float zb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int u = 0; u < S / 2; ++u) {
-          const uint4 s4 = ks[u * 4 + t];
-          const uint4 z4 = kz[u * 4 + t];
-          const uint32_t sp[4] = {s4.x, s4.y, s4.z, s4.w};
-          const uint32_t zp[4] = {z4.x, z4.y, z4.z, z4.w};
-#pragma unroll
-          for (int hlf = 0; hlf < 2; ++hlf) {
-            const int s = 2 * u + hlf;
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-              const __half2 sv = as_h2(sp[2 * hlf + p]);
-              const __half2 x = __hmul2(as_h2(qh[s][p]), sv);
-              const __half2 y = __hfma2(as_h2(qh[s][p]), sv, __hneg2(x));
-              const __half2 z = __hfma2(as_h2(qa[s][p]), sv, y);
-              bq[s][p] = col_lo ? as_u32(z) : as_u32(x);
-            }
-            mma_f16(zb, zp[2 * hlf], zp[2 * hlf], zp[2 * hlf + 1], zp[2 * hlf + 1], qa[s][0], qa[s][1]);
+        for (int p = 0; p < 2; ++p) {
+          const int c0 = t * (D / 4) + 4 * s + 2 * p;
+          float x0 = 0.0f, x1 = 0.0f;
+          if (jc < gq) {
+            x0 = query_value(a, b, h * gq + jc, c0);
+            x1 = query_value(a, b, h * gq + jc, c0 + 1);
           }
+          const uint32_t hi = f2_to_h2(x0, x1);
+          const float2 hf = h2_to_f2(hi);
+          qh[s][p] = hi;
+          qa[s][p] = col_lo ? f2_to_h2(x0 - hf.x, x1 - hf.y) : hi;
         }
+      float m_run = -INFINITY, l_run = 0.0f;
+      const int64_t first_item = unit * ng, last_item = first_item + ng - 1;  // the unit's edge groups
+      CodeConsts<KB> kc;
+      kc.load(a);
+      for (int64_t item = seg + pair; item < seg_e && !failed; item += NP, ++n_t) {
+        const int st = n_t % NST, pb = n_t & 1;
+        if (__any_sync(full, !wait_or_abort(&full_bar[st], static_cast<uint32_t>((n_t / NST) & 1), abort_flag))) {
+          failed = true;
+          break;
+        }
+        const uint8_t* tile = stages + st * CHUNK;
+        uint32_t kr[KW];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int i = 0; i < KW / 4; ++i)
+          *reinterpret_cast<uint4*>(&kr[4 * i]) = reinterpret_cast<const uint4*>(tile)[i * 32 + lane];
+
+        float sc[2][4];
+        {
+          const uint4* ks = reinterpret_cast<const uint4*>(tile + T::KMETA);
+          // the zero-point operand: every row is the k-step's zero row
+          const uint8_t* zrow = tile + T::KMETA + 2 * D + ((lane >> 4) & 1) * 16;
+          uint32_t bq[S][2];
+          float zb[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) sc[mt][e] = zb[e];
+          for (int u = 0; u < S / 2; ++u) {
+            const uint4 s4 = ks[u * 4 + t];
+            const uint32_t sp[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+              const int s = 2 * u + hlf;
+#pragma unroll
+              for (int p = 0; p < 2; ++p) {
+                const __half2 sv = as_h2(sp[2 * hlf + p]);
+                const __half2 x = __hmul2(as_h2(qh[s][p]), sv);
+                const __half2 y = __hfma2(as_h2(qh[s][p]), sv, __hneg2(x));
+                const __half2 z = __hfma2(as_h2(qa[s][p]), sv, y);
+                bq[s][p] = col_lo ? as_u32(z) : as_u32(x);
+              }
+              uint32_t za[4];
+              ldmatrix_x4(za, zrow + s * 32);
+              mma_f16(zb[hlf], za[0], za[1], za[2], za[3], qa[s][0], qa[s][1]);
+            }
+          }
+          float sa[2][2][4] = {};
 #pragma unroll
           for (int s = 0; s < S; ++s) {
-            const int pb = (mt * S + s) * 4;
-            const uint32_t a0 = code_pair<KB>(kr[(pb + 0) / KPPW], (pb + 0) % KPPW);
-            const uint32_t a1 = code_pair<KB>(kr[(pb + 1) / KPPW], (pb + 1) % KPPW);
-            const uint32_t a2 = code_pair<KB>(kr[(pb + 2) / KPPW], (pb + 2) % KPPW);
-            const uint32_t a3 = code_pair<KB>(kr[(pb + 3) / KPPW], (pb + 3) % KPPW);
-            mma_f16(sc[mt], a0, a1, a2, a3, bq[s][0], bq[s][1]);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              const int pbase = (mt * S + s) * 4;
+              const uint32_t a0 = code_pair<KB>(kc, kr[(pbase + 0) / KPPW], (pbase + 0) % KPPW);
+              const uint32_t a1 = code_pair<KB>(kc, kr[(pbase + 1) / KPPW], (pbase + 1) % KPPW);
+              const uint32_t a2 = code_pair<KB>(kc, kr[(pbase + 2) / KPPW], (pbase + 2) % KPPW);
+              const uint32_t a3 = code_pair<KB>(kc, kr[(pbase + 3) / KPPW], (pbase + 3) % KPPW);
+              mma_f16(sa[mt][s & 1], a0, a1, a2, a3, bq[s][0], bq[s][1]);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float z = zb[0][e] + zb[1][e];
+            sc[0][e] = (sa[0][0][e] + sa[0][1][e]) + z;
+            sc[1][e] = (sa[1][0][e] + sa[1][1][e]) + z;
           }
         }
-      }
 
-      // valid tokens: inside [qlo, F) and not a KVSink sink of this group
-      const int64_t p0 = grp * kGroup;
-      uint32_t vbits = 0xffffffffu;
-      if (p0 < a.qlo) vbits &= 0xffffffffu << static_cast<int>(a.qlo - p0);
-      if (p0 + kGroup > a.F) vbits &= (1u << static_cast<int>(a.F - p0)) - 1u;
-      if (G.n_dyn) vbits &= ~a.lay.sink_mask[b * G.n_slots + slot];
-      const bool qvalid = t < gq;
-
-      float pr[2][2];  // [mt][row half]: scores, then probabilities
-      float mx = -INFINITY;
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int tok = 16 * mt + g + 8 * r;
-          const float v = sc[mt][2 * r] + sc[mt][2 * r + 1];
-          pr[mt][r] = (qvalid && ((vbits >> tok) & 1u)) ? v : -INFINITY;
-          mx = fmaxf(mx, pr[mt][r]);
+        // valid tokens: inside [qlo, F) and not a KVSink sink of this group
+        // (only the first and last group of the segment can be partial)
+        uint32_t vbits = 0xffffffffu;
+        if (item == first_item || item == last_item || G.n_dyn) {
+          const int64_t p0 = grp * kGroup;
+          if (p0 < a.qlo) vbits &= 0xffffffffu << static_cast<int>(a.qlo - p0);
+          if (p0 + kGroup > a.F) vbits &= (1u << static_cast<int>(a.F - p0)) - 1u;
+          if (G.n_dyn) vbits &= ~a.lay.sink_mask[b * n_slots + slot];
         }
-      mx = fmaxf(mx, __shfl_xor_sync(full, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(full, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(full, mx, 16));
-      // lazy rescaling: keep the running max unless the tile exceeds it by
-      // more than 2^8, so probabilities stay below 256 (exact either way)
-      const bool grow = mx > m_run + 8.0f;
-      if (__any_sync(full, grow)) {
-        const float mn = grow ? mx : m_run;
-        const float al = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - mn);
-        l_run *= al;
+        float pr[2][2];
 #pragma unroll
-        for (int m = 0; m < MV; ++m) {
-          oacc[m][0] *= al;
-          oacc[m][1] *= al;
-          oacc[m][2] *= al;
-          oacc[m][3] *= al;
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) pr[mt][r] = sc[mt][2 * r] + sc[mt][2 * r + 1];
+        if (vbits != 0xffffffffu || gq < kMaxGqa) {  // uniform: only edge groups pay for masking
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int tok = 16 * mt + g + 8 * r;
+              if (t >= gq || !((vbits >> tok) & 1u)) pr[mt][r] = -INFINITY;
+            }
         }
-#pragma unroll
-        for (int v = 0; v < NVG; ++v) zacc[v] *= al;
-        m_run = mn;
-      }
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float p = (pr[mt][r] == -INFINITY) ? 0.0f : exp2f(pr[mt][r] - m_run);
-          pr[mt][r] = p;
-          l_run += p;
+        // lazy rescaling: the running max only moves when some score exceeds
+        // it by more than the headroom, so weights stay below 2^8 and the
+        // common path needs one warp vote instead of a max reduction
+        float al = 1.0f;
+        float mx = fmaxf(fmaxf(pr[0][0], pr[0][1]), fmaxf(pr[1][0], pr[1][1]));
+        if (__any_sync(full, mx > m_run + kLazyRescale)) {
+          mx = fmaxf(mx, __shfl_xor_sync(full, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(full, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(full, mx, 16));
+          const float mn = mx > m_run + kLazyRescale ? mx : m_run;
+          al = (m_run == -INFINITY) ? 0.0f : fast_exp2(m_run - mn);
+          l_run *= al;
+          m_run = mn;
         }
-
-      // out^T += codes_V^T . pt, one folded pt per V channel group
-      // V scales and zeros of this thread's four tokens (NVG/2 f16x2 words of
-      // scales, then NVG/2 of zeros, per token)
-      __half2 vsp[2][2][NVG / 2], vzp[2][2][NVG / 2];
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const __half2* row = reinterpret_cast<const __half2*>(tile + T::VMETA) + (16 * mt + g + 8 * r) * NVG;
-#pragma unroll
-          for (int i = 0; i < NVG / 2; ++i) {
-            vsp[mt][r][i] = row[i];
-            vzp[mt][r][i] = row[NVG / 2 + i];
-          }
-        }
-#pragma unroll
-      for (int v = 0; v < NVG; ++v) {
-        uint32_t R[2][2];
+        const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
+        uint32_t ph[4];  // weights as (f16 value, f16 residual) per token
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const __half2 sp = vsp[mt][r][v >> 1], zp = vzp[mt][r][v >> 1];
-            const float sv = (v & 1) ? __high2float(sp) : __low2float(sp);
-            const float zv = (v & 1) ? __high2float(zp) : __low2float(zp);
-            const float x = pr[mt][r] * sv;
-            const __half hx = __float2half_rn(x);
-            R[mt][r] = f2_to_h2(__half2float(hx), x - __half2float(hx));
-            zacc[v] = fmaf(pr[mt][r], zv, zacc[v]);
+            const float p = fast_exp2(pr[mt][r] - mref);
+            l_run += p;
+            const __half hp = __float2half_rn(p);
+            ph[mt * 2 + r] = as_u32(__halves2half2(hp, __float2half_rn(p - __half2float(hp))));
           }
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-          const uint32_t b0 = movmatrix_t(R[kb][0]);
-          const uint32_t b1 = movmatrix_t(R[kb][1]);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int m = 2 * v + hh;
-            const int pb = (m * 2 + kb) * 4;
-            const uint32_t a0 = code_pair<VB>(vr[(pb + 0) / VPPW], (pb + 0) % VPPW);
-            const uint32_t a1 = code_pair<VB>(vr[(pb + 1) / VPPW], (pb + 1) % VPPW);
-            const uint32_t a2 = code_pair<VB>(vr[(pb + 2) / VPPW], (pb + 2) % VPPW);
-            const uint32_t a3 = code_pair<VB>(vr[(pb + 3) / VPPW], (pb + 3) % VPPW);
-            mma_f16(oacc[m], a0, a1, a2, a3, b0, b1);
-          }
+        // hand the weights to the PV warp
+        if (__any_sync(full, !wait_or_abort(&pempty[pb], static_cast<uint32_t>(((n_t >> 1) & 1) ^ 1), abort_flag))) {
+          failed = true;
+          break;
         }
+        uint8_t* pw = pbuf + pb * T::PBUF;
+        *reinterpret_cast<uint4*>(pw + lane * 16) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+        if (g == 0) reinterpret_cast<float*>(pw + 32 * 16)[t] = al;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pfull[pb]);
+        grp += NP;
+        slot += NP;
+        while (slot >= n_slots) slot -= n_slots;
       }
-
-      __syncwarp();
-      ++consumed;
-      if (lane == 0 && pc.item >= 0) {
-        mbar_expect_tx(&wb[st], CHUNK);
-        bulk_g2s(stages + st * CHUNK, chunk_src(pc), CHUNK, &wb[st]);
-        pc.advance(i1, ng, warp, a.g_begin, n_slots);
-        ++issued;
-      }
-      grp += 4;
-      slot += 4;
-      while (slot >= n_slots) slot -= n_slots;
-    }
-    issued = __shfl_sync(full, issued, 0);
-
-    // warp state -> shared memory (thread (g, t) owns query t, rows g, g+8)
-    l_run += __shfl_xor_sync(full, l_run, 4);
-    l_run += __shfl_xor_sync(full, l_run, 8);
-    l_run += __shfl_xor_sync(full, l_run, 16);
-#pragma unroll
-    for (int v = 0; v < NVG; ++v) {
-      zacc[v] += __shfl_xor_sync(full, zacc[v], 4);
-      zacc[v] += __shfl_xor_sync(full, zacc[v], 8);
-      zacc[v] += __shfl_xor_sync(full, zacc[v], 16);
-    }
-    if (t < gq) {
-      float* rj = red + (warp * kMaxGqa + t) * (D + 2);
-#pragma unroll
-      for (int m = 0; m < MV; ++m) {
-        rj[16 * m + g] = oacc[m][0] + oacc[m][1] + zacc[m / 2];
-        rj[16 * m + g + 8] = oacc[m][2] + oacc[m][3] + zacc[m / 2];
-      }
-      if (g == 0) {
+      l_run += __shfl_xor_sync(full, l_run, 4);
+      l_run += __shfl_xor_sync(full, l_run, 8);
+      l_run += __shfl_xor_sync(full, l_run, 16);
+      __syncthreads();  // (1) the previous unit's partial has been written
+      if (t < gq && g == 0) {
+        float* rj = red + (pair * kMaxGqa + t) * (D + 2);
         rj[D] = m_run;
         rj[D + 1] = l_run;
       }
+    } else {
+      // ------------------------------------------------------------ PV warp
+      float oacc[MV][4];
+      float zacc[NVG];
+#pragma unroll
+      for (int m = 0; m < MV; ++m) oacc[m][0] = oacc[m][1] = oacc[m][2] = oacc[m][3] = 0.0f;
+#pragma unroll
+      for (int v = 0; v < NVG; ++v) zacc[v] = 0.0f;
+      const __half2 keep_lo = __halves2half2(__float2half_rn(0.0f), __float2half_rn(1.0f));
+      CodeConsts<VB> vc;
+      vc.load(a);
+      for (int64_t item = seg + pair; item < seg_e && !failed; item += NP, ++n_t) {
+        const int st = n_t % NST, pb = n_t & 1;
+        const bool ok = wait_or_abort(&pfull[pb], static_cast<uint32_t>((n_t >> 1) & 1), abort_flag) &&
+                        wait_or_abort(&full_bar[st], static_cast<uint32_t>((n_t / NST) & 1), abort_flag);
+        if (__any_sync(full, !ok)) {
+          failed = true;
+          break;
+        }
+        const uint8_t* tile = stages + st * CHUNK;
+        const uint8_t* pw = pbuf + pb * T::PBUF;
+        const uint4 pv4 = *reinterpret_cast<const uint4*>(pw + lane * 16);
+        const float al = reinterpret_cast<const float*>(pw + 32 * 16)[t];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pempty[pb]);
+        const uint32_t ph[4] = {pv4.x, pv4.y, pv4.z, pv4.w};
+        if (__any_sync(full, al != 1.0f)) {
+#pragma unroll
+          for (int m = 0; m < MV; ++m) {
+            oacc[m][0] *= al;
+            oacc[m][1] *= al;
+            oacc[m][2] *= al;
+            oacc[m][3] *= al;
+          }
+#pragma unroll
+          for (int v = 0; v < NVG; ++v) zacc[v] *= al;
+        }
+        uint32_t vr[VW];
+#pragma unroll
+        for (int i = 0; i < VW / 4; ++i)
+          *reinterpret_cast<uint4*>(&vr[4 * i]) = reinterpret_cast<const uint4*>(tile + T::VC)[i * 32 + lane];
+        // V scales and zeros of this thread's four tokens (NVG/2 f16x2 words
+        // of scales, then NVG/2 of zeros, per token)
+        __half2 vsp[4][NVG / 2], vzp[4][NVG / 2];
+        float pf[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int tok = 16 * (k >> 1) + g + 8 * (k & 1);
+          const __half2* row = reinterpret_cast<const __half2*>(tile + T::VMETA) + tok * NVG;
+#pragma unroll
+          for (int i = 0; i < NVG / 2; ++i) {
+            vsp[k][i] = row[i];
+            vzp[k][i] = row[NVG / 2 + i];
+          }
+          const __half2 pk = as_h2(ph[k]);
+          pf[k] = __low2float(pk) + __high2float(pk);
+        }
+#pragma unroll
+        for (int v = 0; v < NVG; ++v) {
+          uint32_t R[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __half2 s2 = (v & 1) ? __high2half2(vsp[k][v >> 1]) : __low2half2(vsp[k][v >> 1]);
+            const float zv = (v & 1) ? __high2float(vzp[k][v >> 1]) : __low2float(vzp[k][v >> 1]);
+            // (p_hi s, p_lo s), the exact residual of p_hi s, and their sum
+            const __half2 pk = as_h2(ph[k]);
+            const __half2 x = __hmul2(pk, s2);
+            const __half2 e = __hfma2(__low2half2(pk), s2, __hneg2(__low2half2(x)));
+            R[k] = as_u32(__hfma2(e, keep_lo, x));
+            zacc[v] = fmaf(pf[k], zv, zacc[v]);
+          }
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            const uint32_t b0 = movmatrix_t(R[2 * kb]);
+            const uint32_t b1 = movmatrix_t(R[2 * kb + 1]);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int m = 2 * v + hh;
+              const int pbase = (m * 2 + kb) * 4;
+              const uint32_t a0 = code_pair<VB>(vc, vr[(pbase + 0) / VPPW], (pbase + 0) % VPPW);
+              const uint32_t a1 = code_pair<VB>(vc, vr[(pbase + 1) / VPPW], (pbase + 1) % VPPW);
+              const uint32_t a2 = code_pair<VB>(vc, vr[(pbase + 2) / VPPW], (pbase + 2) % VPPW);
+              const uint32_t a3 = code_pair<VB>(vc, vr[(pbase + 3) / VPPW], (pbase + 3) % VPPW);
+              mma_f16(oacc[m], a0, a1, a2, a3, b0, b1);
+            }
+          }
+        }
+        // this pair is done with the stage: refill it with the next chunk
+        __syncwarp();
+        if (lane == 0 && pc.item >= 0) {
+          mbar_expect_tx(&full_bar[st], CHUNK);
+          bulk_g2s(stages + st * CHUNK, pc.ptr, CHUNK, &full_bar[st]);
+          pc.advance(i1, ng, pair, a.g_begin, n_slots, a.lay.chunks, CHUNK);
+          ++issued;
+        }
+      }
+#pragma unroll
+      for (int v = 0; v < NVG; ++v) {
+        zacc[v] += __shfl_xor_sync(full, zacc[v], 4);
+        zacc[v] += __shfl_xor_sync(full, zacc[v], 8);
+        zacc[v] += __shfl_xor_sync(full, zacc[v], 16);
+      }
+      __syncthreads();  // (1) the previous unit's partial has been written
+      if (t < gq) {
+        float* rj = red + (pair * kMaxGqa + t) * (D + 2);
+#pragma unroll
+        for (int m = 0; m < MV; ++m) {
+          rj[16 * m + g] = oacc[m][0] + oacc[m][1] + zacc[m / 2];
+          rj[16 * m + g + 8] = oacc[m][2] + oacc[m][3] + zacc[m / 2];
+        }
+      }
     }
-    __syncthreads();
-    write_partial<D, NW>(a, red, b, h, 1 + cta - owner_cta(unit * ng, work, a.n_ctas));
-    __syncthreads();
+    __syncthreads();  // (2) red complete
+    write_partial<D, 8>(a, red, b, h, 1 + cta - owner_cta(unit * ng, work, a.n_ctas), NP);
     seg = seg_e;
   }
-  if (failed) {
-    if (lane == 0) set_error(a.tab.err_flag, kErrTimeout);
-    // let the copies still in flight land before the CTA exits
-    for (int i = consumed; i < issued; ++i)
-      (void)mbar_wait_bounded(&wb[i % NST], static_cast<uint32_t>((i / NST) & 1));
+  if ((failed || *abort_flag) && lane == 0) set_error(a.tab.err_flag, kErrTimeout);
+  // the copies this pair issued but never consumed must land before exit
+  if (is_pv && lane == 0) {
+    for (int i = n_t; i < issued; ++i)
+      (void)mbar_wait_bounded(&full_bar[i % NST], static_cast<uint32_t>((i / NST) & 1));
   }
 }
 
@@ -440,7 +562,7 @@ cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
     cudaError_t e = cudaFuncSetAttribute(decode_kivi_kernel<D, KB, VB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, decode_kivi_kernel<D, KB, VB>, 128, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, decode_kivi_kernel<D, KB, VB>, 256, smem);
     if (e != cudaSuccess) return e;
     if (occupancy < 1) occupancy = 1;
   }
@@ -453,7 +575,7 @@ cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
   if (n < 1) n = 1;
   a.n_ctas = static_cast<int>(n);
   const int n_exact = a.geo.B * a.geo.H;
-  decode_kivi_kernel<D, KB, VB><<<n_exact + (a.work > 0 ? a.n_ctas : 0), 128, smem, s>>>(a);
+  decode_kivi_kernel<D, KB, VB><<<n_exact + (a.work > 0 ? a.n_ctas : 0), 256, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -67,6 +67,12 @@ struct DecodeArgs {
   int n_sink_read;      // overlay: sink slots [0, n) read from the sink buffer
   int n_dyn_sel;        // KVSink: selected sinks (read when pos < F)
   float qscale;         // log2(e) / sqrt(D)
+  // f16x2 constants of the code-to-f16 conversion, read from the parameter
+  // bank so that one instruction needs at most one immediate: the magic
+  // 1024.0 pair, and per shift k the scale 2^-k and offset -1024 * 2^-k.
+  uint32_t h2_magic;
+  uint32_t h2_scale[9];
+  uint32_t h2_offset[9];
 };
 
 // KVSink selection scratch.

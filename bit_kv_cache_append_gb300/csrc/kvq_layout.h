@@ -26,9 +26,10 @@
 // pair of codes into an exact f16x2 value. Words are interleaved across
 // lanes in 16-byte pieces (word w of lane L at byte ((w/4) * 32 + L) * 16 +
 // (w % 4) * 4) so that a warp's 16-byte loads are contiguous.
-// K scales and zeros are kept in the order the B operand is built: f16
-// position (u * 4 + t) * 8 + e holds channel t D/4 + 8 u + e (u = pair of
-// k-steps), so the four lanes t read one contiguous 64-byte run.
+// K scales are kept in the order the B operand is built: f16 position
+// (u * 4 + t) * 8 + e holds channel t D/4 + 8 u + e (u = pair of k-steps), so
+// the four lanes t read one contiguous 64-byte run; K zeros are kept as one
+// 16-value row per k-step in MMA k order (kzero_pos).
 #pragma once
 
 #include <cstddef>
@@ -88,10 +89,19 @@ KVQ_HD void v_frag_pos(int D, int lane, int f, int* token, int* channel) {
 // Byte offset of 32-bit word w of lane `lane` inside a code region.
 KVQ_HD int code_word_offset(int lane, int w) { return (((w >> 2) * 32 + lane) << 4) + ((w & 3) << 2); }
 
-// f16 position of channel c inside the K scale (or zero) array.
+// f16 position of channel c inside the K scale array.
 KVQ_HD int kmeta_pos(int D, int c) {
   const int q = D / 4, t = c / q, r = c % q;
   return ((r >> 3) * 4 + t) * 8 + (r & 7);
+}
+
+// f16 position of channel c inside the K zero array: for k-step s the 16
+// zeros of its MMA k-slots in k order (k = 2t + e + 8p holds channel
+// t D/4 + 4s + 2p + e), so one row of 16 values is the zero-point operand.
+KVQ_HD int kzero_pos(int D, int c) {
+  const int q = D / 4, t = c / q, r = c % q;
+  const int s = r >> 2, p = (r >> 1) & 1, e = r & 1;
+  return s * 16 + 2 * t + e + 8 * p;
 }
 
 // Word index and bit position of element f inside a lane block.
