@@ -27,7 +27,7 @@ SYMBOLS = ("kv_cache_required_bytes", "kv_cache_create", "kv_cache_destroy", "kv
            "kv_append", "kv_prefill_quantize", "kv_evict", "kv_decode_attn", "kv_cache_stats",
            "kv_cache_export_bytes", "kv_cache_export", "kv_cache_check_device_error",
            "kv_cache_set_timing_events", "kv_launch_count", "kv_copy_bandwidth_kernel",
-           "kv_last_error")
+           "kv_last_error", "kv_decode_attn_noalloc")
 
 
 class KVError(RuntimeError):
@@ -67,6 +67,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kv_prefill_quantize": [vp, i32, vp, vp, i32, vp],
         "kv_evict": [vp, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)],
         "kv_decode_attn": [vp, i32, vp, vp, vp, vp],
+        "kv_decode_attn_noalloc": [vp, i32, vp, vp, vp, vp],
         "kv_cache_stats": [vp, i32, ctypes.POINTER(CacheStats)],
         "kv_cache_export_bytes": [vp, i32, i32, ctypes.POINTER(sz)],
         "kv_cache_export": [vp, i32, i32, vp, sz, vp],
@@ -192,6 +193,17 @@ class KVCache:
             out = torch.empty((c.batch, c.n_q_heads, c.head_dim), dtype=torch.float32, device=q.device)
         lp = _dptr(lse) if lse is not None else None
         check(lib().kv_decode_attn(self.handle, layer, _dptr(q), _dptr(out), lp, _stream_ptr(stream)))
+        return out
+
+    def decode_attn_noalloc(self, layer, q, out, lse=None, stream=None):
+        """kv_decode_attn_noalloc: decode into caller-given `out` (and `lse`)
+        with the partials in the library's fixed device block; allocates
+        nothing."""
+        c = self.cfg
+        if q.dtype != self.act_dtype or tuple(q.shape) != (c.batch, c.n_q_heads, c.head_dim):
+            raise ValueError("q must be [B, Hq, D] in the activation dtype")
+        lp = _dptr(lse) if lse is not None else None
+        check(lib().kv_decode_attn_noalloc(self.handle, layer, _dptr(q), _dptr(out), lp, _stream_ptr(stream)))
         return out
 
     def stats(self, layer) -> dict:

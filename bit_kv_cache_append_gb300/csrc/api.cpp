@@ -391,8 +391,14 @@ kv_status kv_evict(kv_cache* cache, int layer, int64_t* evicted_begin, int64_t* 
   return KV_OK;
 }
 
-kv_status kv_decode_attn(kv_cache* cache, int layer, const void* q, float* out, float* lse_or_null,
-                         void* cuda_stream) {
+}  // extern "C"
+
+namespace kvq {
+
+kv_status report(kv_status s, const char* msg) { return fail(s, msg); }
+
+kv_status decode_attn_impl(kv_cache* cache, int layer, const void* q, float* out, float* lse_or_null,
+                           void* cuda_stream, void* partials, size_t partial_bytes) {
   kv_status st = check_layer(cache, layer);
   if (st != KV_OK) return st;
   if (!q || !out) return fail(KV_ERR_INVALID_ARG, "q/out is NULL");
@@ -404,8 +410,21 @@ kv_status kv_decode_attn(kv_cache* cache, int layer, const void* q, float* out, 
   a.lay = layer_dev(cache, layer);
   a.tab = tables_dev(cache);
   a.q = static_cast<const uint16_t*>(q);
-  a.part_o = reinterpret_cast<float*>(cache->arena + g.off_part_o);
-  a.part_ml = reinterpret_cast<float*>(cache->arena + g.off_part_ml);
+  if (partials) {  // caller-given partial storage: [part_o | part_ml], each 256-byte aligned
+    const size_t ns = static_cast<size_t>(g.max_splits) + 1, rows = static_cast<size_t>(g.B) * g.Hq;
+    const size_t o_bytes = align256(rows * ns * g.D * 4);
+    const size_t need = o_bytes + align256(rows * ns * 2 * 4);
+    if (need > partial_bytes)
+      return fail(KV_ERR_CAPACITY, "decode partials need " + std::to_string(need) +
+                                       " bytes (batch * n_q_heads * (max_splits + 1) * (head_dim + 2) * 4, "
+                                       "256-byte aligned); the scratch holds " +
+                                       std::to_string(partial_bytes));
+    a.part_o = static_cast<float*>(partials);
+    a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(partials) + o_bytes);
+  } else {
+    a.part_o = reinterpret_cast<float*>(cache->arena + g.off_part_o);
+    a.part_ml = reinterpret_cast<float*>(cache->arena + g.off_part_ml);
+  }
   a.out = out;
   a.lse = lse_or_null;
   a.L = ls.L;
@@ -447,6 +466,17 @@ kv_status kv_decode_attn(kv_cache* cache, int layer, const void* q, float* out, 
   g_launches += launches;
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return KV_OK;
+}
+
+int cache_device(const kv_cache* cache) { return cache->device; }
+
+}  // namespace kvq
+
+extern "C" {
+
+kv_status kv_decode_attn(kv_cache* cache, int layer, const void* q, float* out, float* lse_or_null,
+                         void* cuda_stream) {
+  return kvq::decode_attn_impl(cache, layer, q, out, lse_or_null, cuda_stream, nullptr, 0);
 }
 
 kv_status kv_cache_stats(kv_cache* cache, int layer, kv_cache_stats_t* out) {

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 
+#include "kvq.h"
 #include "kvq_layout.h"
 
 namespace kvq {
@@ -96,6 +97,17 @@ cudaError_t launch_decode(DecodeArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEv
                           int64_t* launches);
 cudaError_t launch_copy(const void* src, void* dst, size_t bytes, cudaStream_t s,
                         int64_t* launches);
+
+// Decode attention of one layer (the body of kv_decode_attn). With
+// `partials` NULL the split partials live in the cache's arena; otherwise in
+// `partials` (device, 256-byte aligned, `partial_bytes` long), and the call
+// fails with KV_ERR_CAPACITY before any launch when they do not fit.
+kv_status decode_attn_impl(kv_cache* cache, int layer, const void* q, float* out, float* lse_or_null,
+                           void* cuda_stream, void* partials, size_t partial_bytes);
+// Device ordinal the cache was created on.
+int cache_device(const kv_cache* cache);
+// Set the thread's last-error text and return `s`.
+kv_status report(kv_status s, const char* msg);
 
 // Host-built tables (independent of any other implementation).
 void build_rope_table(float* out, int64_t max_pos, int D, double base);

@@ -182,6 +182,37 @@ kv_status kv_evict(kv_cache* cache, int layer, int64_t* evicted_begin, int64_t* 
 kv_status kv_decode_attn(kv_cache* cache, int layer, const void* q, float* out,
                          float* lse_or_null, void* cuda_stream);
 
+/* Size in bytes of the library's own decode scratch block (32 MiB). */
+#define KV_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * kv_decode_attn with no allocation: the same computation, arguments and
+ * errors, but the split partials go to a fixed block of device memory that
+ * the library declares itself (KV_NOALLOC_SCRATCH_BYTES, reserved on every
+ * GPU that loads the library until the process exits) instead of the
+ * arena's partial region, which this call leaves untouched. The papers have
+ * no counterpart of this entry point: it is for callers that may not
+ * allocate device memory at decode time, such as a serving loop whose pool
+ * has already reserved the whole GPU, a plug-in or custom operator that its
+ * host framework gives no allocator, or a latency-bound loop that cannot
+ * afford the device-wide synchronisation a cudaMalloc or cudaFree brings.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ * Limit: the partials take
+ *   align256(batch * n_q_heads * (max_splits + 1) * head_dim * 4)
+ *   + align256(batch * n_q_heads * (max_splits + 1) * 2 * 4)
+ * bytes; a cache that needs more than KV_NOALLOC_SCRATCH_BYTES gets
+ * KV_ERR_CAPACITY before anything is launched.
+ * The cache's device must be current (KV_ERR_INVALID_ARG otherwise). The
+ * first call on a device looks up the block's device address once
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call shares the one block and it keeps the last call's contents
+ * (nothing in it needs clearing: each call writes every partial it reads).
+ * Calls whose kernels overlap on the GPU (unordered streams, several host
+ * threads) race on the block: order them on one stream or with events.
+ */
+kv_status kv_decode_attn_noalloc(kv_cache* cache, int layer, const void* q, float* out,
+                                 float* lse_or_null, void* cuda_stream);
+
 /* Host-only counters and byte accounting of one layer. In KVSink mode this
  * call reads the sink positions back (it synchronises the device). */
 kv_status kv_cache_stats(kv_cache* cache, int layer, kv_cache_stats_t* out);
