@@ -29,7 +29,8 @@
 //                                          one pt per V channel group)
 // and the zero points: the K zeros enter as a row of the MMA (sum_c zK[c]
 // q_j[c]), the V zeros as fp32 sums sum_t p_j[t] zV[t][c/32].
-// The codes enter the MMA exactly (small integers in f16). The 8 MMA columns
+// The codes enter the MMA exactly, as code * unit in f16 with a power-of-two
+// unit undone on the fp32 sums (code_pair). The 8 MMA columns
 // hold, for query head j, column 2j = the f16 value of the folded operand
 // and column 2j+1 its f16 residual, so each product is carried at about 22
 // bits and thread (g, t) of a C fragment owns query head t. The residuals of
@@ -73,39 +74,61 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Conversion constants of one code width, pinned in registers once per
-// kernel: the f16x2 magic 1024.0 and, per shift k used by the width, the
-// scale 2^-k and the offset -1024 * 2^-k.
+// Packed codes become exact f16 operands by the hardware's narrow-float
+// conversions, with the code bits laid out (kvq_layout.h) so that one mask
+// exposes them in the right format:
+//   2-bit: a code in the low two bits of an e2m1 nibble is the value code/2
+//          (subnormal 0.5, then 1.0, 1.5), a byte gives an f16x2;
+//   4-bit: a code in the low nibble of an e4m3 byte is code * 2^-9 (the
+//          subnormal and first normal binade are evenly spaced), two bytes
+//          give an f16x2;
+//   8-bit: the code is OR-ed into the mantissa of 1024.0 and 1024 is
+//          subtracted.
+// kCodeInv is the factor that turns sums over these values back into sums
+// over codes (a power of two, so the rescale is exact).
 template <int BITS>
 struct CodeConsts {
-  static constexpr int N = BITS == 2 ? 5 : (BITS == 4 ? 2 : 1);
-  uint32_t magic, scale[N], offset[N];
+  static constexpr float kCodeInv = BITS == 2 ? 2.0f : (BITS == 4 ? 512.0f : 1.0f);
+  uint32_t magic;
   __device__ __forceinline__ void load(const DecodeArgs& a) {
-    magic = pin(a.h2_magic);
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-      scale[i] = pin(a.h2_scale[i * (BITS == 2 ? 2 : 4)]);
-      offset[i] = pin(a.h2_offset[i * (BITS == 2 ? 2 : 4)]);
-    }
+    if (BITS == 8) magic = pin(a.h2_magic);
   }
 };
 
-// Pair j of a packed word (elements at bits BITS*j and BITS*j + 16) as an
-// exact f16x2 of the two codes. The code bits are OR-ed into the mantissa of
-// 1024.0 (0x6400), giving 1024 + c * 2^k exactly, and one f16x2 FMA by
-// 2^-k and -1024 * 2^-k leaves c exactly.
+template <int BYTE>
+__device__ __forceinline__ uint32_t cvt_e2m1x2(uint32_t m) {
+  uint32_t d;
+  if (BYTE == 0) asm("{.reg .b8 a, b, c, e; mov.b32 {a, b, c, e}, %1; cvt.rn.f16x2.e2m1x2 %0, a;}" : "=r"(d) : "r"(m));
+  if (BYTE == 1) asm("{.reg .b8 a, b, c, e; mov.b32 {a, b, c, e}, %1; cvt.rn.f16x2.e2m1x2 %0, b;}" : "=r"(d) : "r"(m));
+  if (BYTE == 2) asm("{.reg .b8 a, b, c, e; mov.b32 {a, b, c, e}, %1; cvt.rn.f16x2.e2m1x2 %0, c;}" : "=r"(d) : "r"(m));
+  if (BYTE == 3) asm("{.reg .b8 a, b, c, e; mov.b32 {a, b, c, e}, %1; cvt.rn.f16x2.e2m1x2 %0, e;}" : "=r"(d) : "r"(m));
+  return d;
+}
+
+template <int HALF>
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t m) {
+  uint32_t d;
+  if (HALF == 0) asm("{.reg .b16 l, h; mov.b32 {l, h}, %1; cvt.rn.f16x2.e4m3x2 %0, l;}" : "=r"(d) : "r"(m));
+  if (HALF == 1) asm("{.reg .b16 l, h; mov.b32 {l, h}, %1; cvt.rn.f16x2.e4m3x2 %0, h;}" : "=r"(d) : "r"(m));
+  return d;
+}
+
+// Pair j of a packed word (the lane's fragment elements 2P, 2P + 1 where
+// P = word * pairs-per-word + j) as an exact f16x2 of code * unit. j is a
+// constant after unrolling, so the selections below fold away.
 template <int BITS>
 __device__ __forceinline__ uint32_t code_pair(const CodeConsts<BITS>& k, uint32_t w, int j) {
   if (BITS == 2) {
-    const int jj = j < 5 ? j : j - 5;
-    const uint32_t x = j < 5 ? w : (w >> 10);
-    const uint32_t hv = (x & (0x00030003u << (2 * jj))) | k.magic;
-    return as_u32(__hfma2(as_h2(hv), as_h2(k.scale[jj]), as_h2(k.offset[jj])));
+    const uint32_t m = (j < 4 ? w : (w >> 2)) & 0x33333333u;
+    switch (j & 3) {
+      case 0: return cvt_e2m1x2<0>(m);
+      case 1: return cvt_e2m1x2<1>(m);
+      case 2: return cvt_e2m1x2<2>(m);
+      default: return cvt_e2m1x2<3>(m);
+    }
   } else if (BITS == 4) {
-    const int jj = j < 2 ? j : j - 2;
-    const uint32_t x = j < 2 ? w : (w >> 8);
-    const uint32_t hv = (x & (0x000F000Fu << (4 * jj))) | k.magic;
-    return as_u32(__hfma2(as_h2(hv), as_h2(k.scale[jj % CodeConsts<BITS>::N]), as_h2(k.offset[jj % CodeConsts<BITS>::N])));
+    const uint32_t m = (j < 2 ? w : (w >> 4)) & 0x0F0F0F0Fu;
+    return (j & 1) ? cvt_e4m3x2<1>(m) : cvt_e4m3x2<0>(m);
   } else {
     const uint32_t hv = __byte_perm(w, k.magic, static_cast<uint32_t>(j | 0x50 | ((j + 2) << 8) | 0x7000));
     return as_u32(__hsub2(as_h2(hv), as_h2(k.magic)));
@@ -353,8 +376,8 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float z = zb[0][e] + zb[1][e];
-            sc[0][e] = (sa[0][0][e] + sa[0][1][e]) + z;
-            sc[1][e] = (sa[1][0][e] + sa[1][1][e]) + z;
+            sc[0][e] = fmaf(sa[0][0][e] + sa[0][1][e], CodeConsts<KB>::kCodeInv, z);
+            sc[1][e] = fmaf(sa[1][0][e] + sa[1][1][e], CodeConsts<KB>::kCodeInv, z);
           }
         }
 
@@ -536,8 +559,8 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
         float* rj = red + (pair * kMaxGqa + t) * (D + 2);
 #pragma unroll
         for (int m = 0; m < MV; ++m) {
-          rj[16 * m + g] = oacc[m][0] + oacc[m][1] + zacc[m / 2];
-          rj[16 * m + g + 8] = oacc[m][2] + oacc[m][3] + zacc[m / 2];
+          rj[16 * m + g] = fmaf(oacc[m][0] + oacc[m][1], CodeConsts<VB>::kCodeInv, zacc[m / 2]);
+          rj[16 * m + g + 8] = fmaf(oacc[m][2] + oacc[m][3], CodeConsts<VB>::kCodeInv, zacc[m / 2]);
         }
       }
     }

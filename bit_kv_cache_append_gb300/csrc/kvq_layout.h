@@ -20,10 +20,11 @@
 //   V (A operand of O^T = V^T P^T, rows = channels, k = tokens):
 //     f = ((m * 2 + kb) * 4 + r) * 2 + e,  m in [0, D/16), kb in {0,1}
 //     channel = 16 m + g + 8 (r & 1);  token = 16 kb + 2 t + e + 8 (r >> 1)
-// Element f sits in 32-bit word w = f / (32/bits) of its lane at bit
-// bits * j + 16 e, j = (f % (32/bits)) / 2: the two elements of one f16x2
-// register are 16 bits apart, so a mask and an f16 magic-number OR turn a
-// pair of codes into an exact f16x2 value. Words are interleaved across
+// Element f sits in 32-bit word w = f / (32/bits) of its lane at the bit
+// frag_bits gives: placed so that one mask turns a pair of codes into a pair
+// of narrow floats (e2m1 for 2-bit, e4m3 for 4-bit) or, for 8-bit, into a
+// pair of bytes 16 bits apart, each converted to an exact f16x2 by one
+// instruction in the decode kernel. Words are interleaved across
 // lanes in 16-byte pieces (word w of lane L at byte ((w/4) * 32 + L) * 16 +
 // (w % 4) * 4) so that a warp's 16-byte loads are contiguous.
 // K scales are kept in the order the B operand is built: f16 position
@@ -104,12 +105,20 @@ KVQ_HD int kzero_pos(int D, int c) {
   return s * 16 + 2 * t + e + 8 * p;
 }
 
-// Word index and bit position of element f inside a lane block.
+// Word index and bit position of element f inside a lane block. Pair
+// j = (f % per_word) / 2 of a word holds elements e = 0, 1 (f = 2P + e):
+//   2-bit: byte j & 3, bits 2 (j >> 2) + 4 e   (an e2m1 nibble pair per byte
+//          after masking with 0x33 at shift 0 or 2)
+//   4-bit: half j & 1, bits 16 (j & 1) + 4 (j >> 1) + 8 e   (an e4m3 byte
+//          pair per half after masking with 0x0F at shift 0 or 4)
+//   8-bit: bits 8 j + 16 e
 KVQ_HD void frag_bits(int bits, int f, int* word, int* bit) {
   const int per_word = 32 / bits;
-  const int w = f / per_word, i = f % per_word;
+  const int w = f / per_word, i = f % per_word, j = i >> 1, e = i & 1;
   *word = w;
-  *bit = bits * (i >> 1) + 16 * (i & 1);
+  if (bits == 2) *bit = 8 * (j & 3) + 2 * (j >> 2) + 4 * e;
+  else if (bits == 4) *bit = 16 * (j & 1) + 4 * (j >> 1) + 8 * e;
+  else *bit = 8 * j + 16 * e;
 }
 
 // Arena geometry shared by every layer.
