@@ -11,9 +11,10 @@ than L2, so no flush is needed between steps.
 One step = kv_append of one new token (K, V) + kv_decode_attn, the whole
 hot path of a decode step for one layer. Reported:
   value      effective bandwidth over the step's algorithmic bytes (GB/s)
-  roofline   the split-KV decode kernel alone: algorithmic bytes / its
-             average duration (CUDA events the library records on the
-             launching stream), against the measured HBM peak
+  roofline   the decode kernels (split-KV partitions, then exact pools and
+             LSE merge): algorithmic bytes / their average duration (CUDA
+             events the library records on the launching stream around
+             both), against the measured HBM peak
   e2e        the same step through the public API with host buffers
              (pinned host -> device inputs, device -> host output)
   cpu_baseline  the CPU oracle timed on a bounded sample of the workload
@@ -256,7 +257,7 @@ def run_ours(args, rank, world, local):
         step(i)
     torch.cuda.synchronize()
     stats0 = cache.stats(0)
-    # per-step events around the split kernel (recorded by the library)
+    # per-step events around the decode kernels (split + merge, recorded by the library)
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a, b in kev:
         a.record(stream)
@@ -365,7 +366,7 @@ def run_ours(args, rank, world, local):
             "copy_kernel_gbs": round(copy_gbs, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
-                         "kernel": "decode_kivi_kernel<128,2,4> (split-KV partitions + exact pools)",
+                         "kernel": "decode_kivi_kernel<128,2,4> + merge_kernel<128> (split-KV partitions; exact pools and LSE merge)",
                          "algorithmic_bytes_per_launch": int(dec_bytes), "peak_kind": f"{peak_kind} hbm_gbs",
                          "kernel_us": round(kernel_avg_ms * 1e3, 2)},
             "cpu_baseline": {"value": round(cpu_gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",

@@ -1,5 +1,5 @@
-// TurboQuant split kernel, the log-sum-exp merge of the partials and the
-// decode dispatch.
+// TurboQuant split kernel, the merge kernel (exact pools of each unit and the
+// log-sum-exp merge of the partials) and the decode dispatch.
 #include "decode_common.cuh"
 
 namespace kvq {
@@ -48,11 +48,8 @@ __global__ void __launch_bounds__(128) decode_tq_kernel(DecodeArgs a) {
   __shared__ float red[NW * kMaxGqa * (D + 2)];
   __shared__ float ck[16], cv[16];
   const Geometry& G = a.geo;
-  const int split = static_cast<int>(blockIdx.x) - 1, h = blockIdx.y, b = blockIdx.z;
-  if (split < 0) {
-    exact_partition<D, NW>(a, b, h, red);
-    return;
-  }
+  pdl_launch_dependents();
+  const int split = static_cast<int>(blockIdx.x), h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = G.gqa;
   if (threadIdx.x < 16) {
@@ -132,60 +129,136 @@ __global__ void __launch_bounds__(128) decode_tq_kernel(DecodeArgs a) {
     }
   }
   __syncthreads();
-  write_partial<D, NW>(a, red, b, h, 1 + split);
+  write_partial<D, NW>(a, red, b, h, split);
 }
 
-// Number of partial slots of unit u (slot 0 = exact pools): stream-K parts
-// are the CTAs whose item ranges meet the unit's items.
+// Number of partial slots of unit u: TurboQuant partitions, or the stream-K
+// CTAs whose item ranges meet the unit's items.
 __device__ __forceinline__ int slots_of_unit(const DecodeArgs& a, int64_t u) {
-  if (a.geo.mode_tq) return a.n_splits + 1;
-  if (a.work <= 0 || a.n_groups <= 0) return 1;
+  if (a.geo.mode_tq) return a.n_splits;
+  if (a.work <= 0 || a.n_groups <= 0) return 0;
   const int64_t first = u * a.n_groups, last = first + a.n_groups - 1;
   const int c0 = static_cast<int>(((first + 1) * a.n_ctas - 1) / a.work);
   const int c1 = static_cast<int>(((last + 1) * a.n_ctas - 1) / a.work);
-  return 1 + (c1 - c0 + 1);
+  return c1 - c0 + 1;
 }
 
-// One warp per (b, query head): combine the partials by log-sum-exp
-// (M = max m_s, o = sum 2^(m_s - M) o_s / sum 2^(m_s - M) l_s) and, in
-// TurboQuant mode, rotate the output back (x = D FWHT(y) / sqrt(d)).
+constexpr int kMergeWarps = 8;
+
+// Shared memory of the merge kernel: the row stage, the warps' exact states,
+// an mbarrier and the abort flag.
 template <int D>
-__global__ void __launch_bounds__(128) merge_kernel(DecodeArgs a) {
-  constexpr int NS = D / 32;
+size_t merge_smem_bytes(int stage_bytes) {
+  return static_cast<size_t>(stage_bytes) + kMergeWarps * kMaxGqa * (D + 2) * 4 + 32;
+}
+
+// One CTA per (sequence, KV head) unit. First the unit's exact pools (sinks
+// and tail), staged through shared memory and run on the tensor cores
+// (exact_states_tc);
+// then warp j < gqa combines, for query head j, the exact states with the
+// split partials by log-sum-exp (M = max m, o = sum 2^(m - M) o / sum
+// 2^(m - M) l) and writes the output and lse. In TurboQuant mode the split
+// partials are in the rotated domain: their sum is rotated back
+// (x = D FWHT(y) / sqrt(d)) before the exact part, which is in the original
+// domain, is added (Foundry "TurboQuant KV Cache Compression - Spec",
+// "Optimization: Fused dequant-dot": rotate the accumulated output once).
+template <int D>
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(DecodeArgs a, int stage_bytes) {
+  constexpr int NS = D / 32, NW = kMergeWarps;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* red = reinterpret_cast<float*>(smem + stage_bytes);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + stage_bytes + NW * kMaxGqa * (D + 2) * 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 1);
   const Geometry& G = a.geo;
+  const int u = blockIdx.x, b = u / G.H, h = u % G.H;
+  const bool ok = G.act_bf16 ? exact_states_tc<D, NW, true>(a, b, h, red, smem, stage_bytes, bar, abort_flag)
+                             : exact_states_tc<D, NW, false>(a, b, h, red, smem, stage_bytes, bar, abort_flag);
+  if (!ok && threadIdx.x == 0) set_error(a.tab.err_flag, kErrTimeout);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + warp;
-  if (row >= G.B * G.Hq) return;
-  const int ns = slots_of_unit(a, row / G.Hq * G.H + (row % G.Hq) / G.gqa);
+  if (warp >= G.gqa) return;
+  pdl_wait_primary();  // the split partials are complete and visible from here on
+  const int j = warp;
+  const int row = b * G.Hq + h * G.gqa + j;
+  const int ns = slots_of_unit(a, u);
   const float* ml = a.part_ml + static_cast<size_t>(row) * a.ns * 2;
+  const float* rj = red + j * (D + 2);  // warp w's state at rj + w * kMaxGqa * (D + 2)
   float M = -INFINITY;
   for (int s = lane; s < ns; s += 32) M = fmaxf(M, ml[2 * s]);
+  if (lane < NW) M = fmaxf(M, rj[lane * kMaxGqa * (D + 2) + D]);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float L = 0.0f, o[NS];
+  float L = 0.0f, oq[NS], oe[NS];
 #pragma unroll
-  for (int i = 0; i < NS; ++i) o[i] = 0.0f;
-  for (int s = 0; s < ns; ++s) {
+  for (int i = 0; i < NS; ++i) oq[i] = oe[i] = 0.0f;
+#pragma unroll 4
+  for (int s = 0; s < ns; ++s) {  // a slot with m = -inf has o = 0 and l = 0
     const float ms = ml[2 * s];
-    if (ms == -INFINITY) continue;
-    const float w = exp2f(ms - M);
-    L += ml[2 * s + 1] * w;
+    const float w = ms == -INFINITY ? 0.0f : exp2f(ms - M);
+    L = fmaf(ml[2 * s + 1], w, L);
     const float* po = a.part_o + (static_cast<size_t>(row) * a.ns + s) * D;
 #pragma unroll
-    for (int i = 0; i < NS; ++i) o[i] = fmaf(po[i * 32 + lane], w, o[i]);
+    for (int i = 0; i < NS; ++i) oq[i] = fmaf(po[i * 32 + lane], w, oq[i]);
+  }
+  for (int w = 0; w < NW; ++w) {
+    const float* r = rj + w * kMaxGqa * (D + 2);
+    if (r[D] == -INFINITY) continue;
+    const float sc = exp2f(r[D] - M);
+    L += r[D + 1] * sc;
+#pragma unroll
+    for (int i = 0; i < NS; ++i) oe[i] = fmaf(r[i * 32 + lane], sc, oe[i]);
+  }
+  if (G.mode_tq) {
+    warp_fwht<D>(oq);
+    const float rsq = static_cast<float>(1.0 / sqrt(static_cast<double>(D)));
+#pragma unroll
+    for (int i = 0; i < NS; ++i) oq[i] = oq[i] * rsq * a.tab.signs[i * 32 + lane];
   }
   const float inv = 1.0f / L;
 #pragma unroll
-  for (int i = 0; i < NS; ++i) o[i] *= inv;
-  if (G.mode_tq) {
-    warp_fwht<D>(o);
-    const float rsq = static_cast<float>(1.0 / sqrt(static_cast<double>(D)));
-#pragma unroll
-    for (int i = 0; i < NS; ++i) o[i] = o[i] * rsq * a.tab.signs[i * 32 + lane];
-  }
-#pragma unroll
-  for (int i = 0; i < NS; ++i) a.out[static_cast<size_t>(row) * D + i * 32 + lane] = o[i];
+  for (int i = 0; i < NS; ++i) a.out[static_cast<size_t>(row) * D + i * 32 + lane] = (oq[i] + oe[i]) * inv;
   if (a.lse && lane == 0) a.lse[row] = (M + log2f(L)) * 0.69314718055994530942f;
+}
+
+// Rows (K and V) one merge CTA stages at once, in whole 32-row tiles: every
+// sink and tail row when they fit in 80 KB, else batches of that size.
+int merge_stage_bytes(const Geometry& G) {
+  const int row_pair = 4 * G.D;  // K and V rows of the activation dtype
+  int rows = G.n_sink_slots + G.tail_cap;
+  const int cap = (80 << 10) / row_pair;
+  if (rows > cap) rows = cap;
+  rows = (rows + kExactTile - 1) / kExactTile * kExactTile;
+  return rows * row_pair;
+}
+
+// `after_split`: the merge follows a split kernel on the stream and may be
+// scheduled before it ends (programmatic dependent launch); otherwise it is
+// an ordinary launch, since its exact pools read rows the appends before it
+// wrote.
+template <int D>
+cudaError_t launch_merge(DecodeArgs& a, cudaStream_t s, bool after_split) {
+  const int stage = merge_stage_bytes(a.geo);
+  const size_t smem = merge_smem_bytes<D>(stage);
+  static size_t configured[kMaxDevices] = {};  // per device: the attribute is per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (smem > configured[dev]) {
+    e = cudaFuncSetAttribute(merge_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured[dev] = smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.geo.B * a.geo.H);
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_split ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, merge_kernel<D>, a, stage);
 }
 
 }  // namespace
@@ -198,18 +271,22 @@ cudaError_t launch_decode(DecodeArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEv
   if (!G.mode_tq) {
     e = (G.D == 128) ? launch_kivi_d128(a, s, sm_count) : launch_kivi_d64(a, s, sm_count);
   } else {
-    dim3 grid(a.n_splits + 1, G.H, G.B);
-    if (G.D == 128) decode_tq_kernel<128><<<grid, 128, 0, s>>>(a);
-    else decode_tq_kernel<64><<<grid, 128, 0, s>>>(a);
-    e = cudaGetLastError();
+    e = cudaSuccess;
+    if (a.n_splits > 0) {
+      dim3 grid(a.n_splits, G.H, G.B);
+      if (G.D == 128) decode_tq_kernel<128><<<grid, 128, 0, s>>>(a);
+      else decode_tq_kernel<64><<<grid, 128, 0, s>>>(a);
+      e = cudaGetLastError();
+    }
   }
   if (e != cudaSuccess) return e;
+  const bool split_ran = a.work > 0;
+  if (split_ran) ++*launches;
+  e = (G.D == 128) ? launch_merge<128>(a, s, split_ran) : launch_merge<64>(a, s, split_ran);
+  if (e != cudaSuccess) return e;
+  ++*launches;
   if (ev1) cudaEventRecord(ev1, s);
-  const int rows = G.B * G.Hq;
-  if (G.D == 128) merge_kernel<128><<<(rows + 3) / 4, 128, 0, s>>>(a);
-  else merge_kernel<64><<<(rows + 3) / 4, 128, 0, s>>>(a);
-  *launches += 2;
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 // 16-byte vectorised grid-stride copy: the in-process bandwidth reference.

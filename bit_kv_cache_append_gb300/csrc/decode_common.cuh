@@ -76,6 +76,22 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* row_ad
                : "r"(smem_u32(row_addr)));
 }
 
+// 2^x by the hardware approximation (relative error about 2^-22; -inf -> 0),
+// enough for softmax weights.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Programmatic dependent launch: a split kernel lets the merge kernel that
+// follows it on the stream be scheduled early (its exact pools do not read
+// the partials), and the merge kernel waits for the split kernel's completion
+// and memory before it reads them. Without the launch attribute the wait is
+// a no-op.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // A value the compiler must keep in a register (it cannot re-derive it).
 __device__ __forceinline__ uint32_t pin(uint32_t x) {
   uint32_t y;
@@ -158,83 +174,259 @@ __device__ __forceinline__ void write_partial(const DecodeArgs& a, const float* 
   }
 }
 
+// Bounded wait that also gives up when another warp of the CTA has given up.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+// D += A B with A 16x16, B 16x8 of the activation type (bf16 or f16, the same
+// for both operands), D 16x8 f32.
+template <bool BF>
+__device__ __forceinline__ void mma_act(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  if (BF)
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    mma_f16(d, a0, a1, a2, a3, b0, b1);
+}
+
+// Four 8x8 b16 matrices, each stored as 8 rows of 16 bytes, transposed into
+// the MMA A-fragment layout; lane L gives the address of row L % 8 of matrix
+// L / 8.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void* row_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(row_addr)));
+}
+
+// Two floats as a pair of the activation type (x0 in the low half), rounded
+// to nearest, and back.
+template <bool BF>
+__device__ __forceinline__ uint32_t pack_act2(float x0, float x1) {
+  if (BF) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(x0, x1);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  return f2_to_h2(x0, x1);
+}
+template <bool BF>
+__device__ __forceinline__ float2 unpack_act2(uint32_t x) {
+  if (BF) return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&x));
+  return h2_to_f2(x);
+}
+
+// A pair of the activation type holding x split as hi + lo: lanes that own a
+// "lo" MMA column get the residual x - hi, the others hi.
+template <bool BF>
+__device__ __forceinline__ uint32_t split_act2(float x0, float x1, bool lo) {
+  const uint32_t h = pack_act2<BF>(x0, x1);
+  if (!lo) return h;
+  const float2 hf = unpack_act2<BF>(h);
+  return pack_act2<BF>(__fsub_rn(x0, hf.x), __fsub_rn(x1, hf.y));
+}
+
+// Rows per tile of the exact pools and the row capacity a stage of
+// `stage_bytes` gives (whole tiles).
+constexpr int kExactTile = 32;
+
 // The exact pools of one (b, h): the sinks read from the sink buffer and the
-// tail [F, L) read from the ring, at fp32 with the query at full precision.
-// NW warps take the tokens in turn; lane l holds channels i*32 + l. `red`
-// must hold NW * kMaxGqa * (D + 2) floats.
-template <int D, int NW>
-__device__ void exact_partition(const DecodeArgs& a, int b, int h, float* red) {
-  constexpr int NS = D / 32;
+// tail [F, L) read from the ring, with the query at full precision (RoPE at
+// L - 1 when the cache applies it). The rows are staged in shared memory:
+// batches of sink and tail rows (K and V) are fetched by 1-D bulk copies
+// (the tail ring in at most two contiguous runs) into `stage` (stage_bytes,
+// 128-byte aligned, a whole number of 32-row tiles of K and V), the first
+// batch requested before the query prologue. Each warp takes 32-row tiles in
+// turn and runs them on the tensor cores in the activation type, straight
+// from shared memory: scores^T = K_tile q^T with q split as hi + lo in the
+// two columns of each query head (about 16 bits for bf16, 22 for f16), then
+// an online softmax, then out^T += V_tile^T p^T with p split the same way.
+// Each warp leaves its state in `red` (NW * kMaxGqa * (D + 2) floats:
+// [w][j][0..D-1] = o, [w][j][D] = m in log2 units, [w][j][D+1] = l). `bar`
+// is an mbarrier this function initialises; `abort_flag` is the CTA's shared
+// give-up flag. Returns false (for every thread) when a wait gave up.
+template <int D, int NW, bool BF>
+__device__ bool exact_states_tc(const DecodeArgs& a, int b, int h, float* red, uint8_t* stage, int stage_bytes,
+                                uint64_t* bar, volatile int* abort_flag) {
+  constexpr int S = D / 16, MV = D / 16;
+  constexpr int ROW = D * 2;  // bytes of one act-dtype row
+  const unsigned full = 0xffffffffu;
   const Geometry& G = a.geo;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
   const int gq = G.gqa;
-  float qv[kMaxGqa][NS];
-#pragma unroll
-  for (int j = 0; j < kMaxGqa; ++j)
-#pragma unroll
-    for (int i = 0; i < NS; ++i) qv[j][i] = (j < gq) ? query_value(a, b, h * gq + j, i * 32 + lane) : 0.0f;
-  float m[kMaxGqa], l[kMaxGqa], o[kMaxGqa][NS];
-#pragma unroll
-  for (int j = 0; j < kMaxGqa; ++j) {
-    m[j] = -INFINITY;
-    l[j] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < NS; ++i) o[j][i] = 0.0f;
-  }
   const int bh = b * G.H + h;
   const int n_sink_items = G.n_dyn ? a.n_dyn_sel : a.n_sink_read;
-  const int64_t n_tail = a.L - a.F;
-  const int64_t n_items = n_sink_items + n_tail;
-  for (int64_t it = warp; it < n_items; it += NW) {
-    const uint16_t* kr;
-    const uint16_t* vr;
-    if (it < n_sink_items) {
-      if (G.n_dyn && a.lay.sink_pos[b * kMaxSinks + it] >= a.F) continue;  // read from the tail
-      const size_t t = (static_cast<size_t>(bh) * G.n_sink_slots + it) * D;
-      kr = a.lay.sink_k + t;
-      vr = a.lay.sink_v + t;
-    } else {
-      const int64_t pos = a.F + (it - n_sink_items);
-      const size_t t = (static_cast<size_t>(bh) * G.tail_cap + (pos & (G.tail_cap - 1))) * D;
-      kr = a.lay.tail_k + t;
-      vr = a.lay.tail_v + t;
+  const int n_items = n_sink_items + static_cast<int>(a.L - a.F);
+  const int cap = stage_bytes / (2 * ROW);  // rows per batch, a multiple of kExactTile
+  uint16_t* sk = reinterpret_cast<uint16_t*>(stage);
+  uint16_t* sv = sk + static_cast<size_t>(cap) * D;
+  // rows [i0, i1) of the item list (sinks, then the tail in position order)
+  auto issue = [&](int i0, int i1) {
+    mbar_expect_tx(bar, static_cast<uint32_t>((i1 - i0) * 2 * ROW));
+    int r = i0;
+    if (r < n_sink_items) {
+      const int e = i1 < n_sink_items ? i1 : n_sink_items;
+      const size_t off = (static_cast<size_t>(bh) * G.n_sink_slots + r) * D;
+      bulk_g2s(sk + (r - i0) * D, a.lay.sink_k + off, (e - r) * ROW, bar);
+      bulk_g2s(sv + (r - i0) * D, a.lay.sink_v + off, (e - r) * ROW, bar);
+      r = e;
     }
-    float kx[NS], vx[NS];
-#pragma unroll
-    for (int i = 0; i < NS; ++i) {
-      kx[i] = act_to_float(kr[i * 32 + lane], G.act_bf16);
-      vx[i] = act_to_float(vr[i * 32 + lane], G.act_bf16);
+    while (r < i1) {  // tail rows in ring order
+      const int slot = static_cast<int>((a.F + (r - n_sink_items)) & (G.tail_cap - 1));
+      const int n = (i1 - r) < (G.tail_cap - slot) ? (i1 - r) : (G.tail_cap - slot);
+      const size_t off = (static_cast<size_t>(bh) * G.tail_cap + slot) * D;
+      bulk_g2s(sk + (r - i0) * D, a.lay.tail_k + off, n * ROW, bar);
+      bulk_g2s(sv + (r - i0) * D, a.lay.tail_v + off, n * ROW, bar);
+      r += n;
     }
-#pragma unroll
-    for (int j = 0; j < kMaxGqa; ++j) {
-      if (j >= gq) break;
-      float s = 0.0f;
-#pragma unroll
-      for (int i = 0; i < NS; ++i) s = fmaf(qv[j][i], kx[i], s);
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      const float mn = fmaxf(m[j], s);
-      const float al = exp2f(m[j] - mn);
-      const float p = exp2f(s - mn);
-      l[j] = l[j] * al + p;
-#pragma unroll
-      for (int i = 0; i < NS; ++i) o[j][i] = fmaf(o[j][i], al, p * vx[i]);
-      m[j] = mn;
-    }
+  };
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar, 1);
+    mbar_fence_init();
+    if (n_items > 0) issue(0, n_items < cap ? n_items : cap);
   }
+  __syncthreads();
+  // B operand of the scores: column g = query head g / 2, value (g even) or
+  // residual (g odd); rows 2t, 2t + 1 and 2t + 8, 2t + 9 of k-step s are
+  // channels 16 s + 2t (+1) and 16 s + 2t + 8 (+1).
+  const int jc = g >> 1;
+  const bool col_lo = g & 1;
+  uint32_t qb[S][2];
 #pragma unroll
-  for (int j = 0; j < kMaxGqa; ++j) {
-    if (j >= gq) break;
-    float* r = red + (warp * kMaxGqa + j) * (D + 2);
+  for (int s = 0; s < S; ++s)
 #pragma unroll
-    for (int i = 0; i < NS; ++i) r[i * 32 + lane] = o[j][i];
-    if (lane == 0) {
-      r[D] = m[j];
-      r[D + 1] = l[j];
+    for (int p = 0; p < 2; ++p) {
+      const int c0 = 16 * s + 2 * t + 8 * p;
+      float x0 = 0.0f, x1 = 0.0f;
+      if (jc < gq) {
+        x0 = query_value(a, b, h * gq + jc, c0);
+        x1 = query_value(a, b, h * gq + jc, c0 + 1);
+      }
+      qb[s][p] = split_act2<BF>(x0, x1, col_lo);
+    }
+  float m_run = -INFINITY, l_run = 0.0f;  // of query head t (this lane's C columns)
+  float oacc[MV][4];
+#pragma unroll
+  for (int m = 0; m < MV; ++m) oacc[m][0] = oacc[m][1] = oacc[m][2] = oacc[m][3] = 0.0f;
+  uint32_t phase = 0;
+  bool ok = true;
+  for (int i0 = 0; i0 < n_items; i0 += cap) {
+    const int i1 = i0 + cap < n_items ? i0 + cap : n_items;
+    const int nb = i1 - i0;
+    ok = ok && wait_or_abort(bar, phase, abort_flag);
+    phase ^= 1;
+    if (ok) {
+      for (int tile = warp; tile * kExactTile < nb; tile += NW) {
+        const int rb = tile * kExactTile;
+        if (rb + kExactTile > nb) {
+          // rows past the batch hold stale bytes: zero their V so that a zero
+          // weight times them is zero
+          for (int i = (nb - rb) * (ROW / 16) + lane; i < kExactTile * (ROW / 16); i += 32)
+            reinterpret_cast<uint4*>(sv + static_cast<size_t>(rb) * D)[i] = make_uint4(0u, 0u, 0u, 0u);
+          __syncwarp();
+        }
+        float sc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int s = 0; s < S; ++s) {
+            uint32_t A[4];
+            ldmatrix_x4(A, sk + static_cast<size_t>(rb + 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1)) * D +
+                               16 * s + 8 * (lane >> 4));
+            mma_act<BF>(sc[mt], A[0], A[1], A[2], A[3], qb[s][0], qb[s][1]);
+          }
+        float pr[2][2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int it = i0 + rb + 16 * mt + g + 8 * r;
+            bool valid = (it < i1) && (t < gq);
+            if (valid && it < n_sink_items && G.n_dyn && a.lay.sink_pos[b * kMaxSinks + it] >= a.F)
+              valid = false;  // a KVSink sink still in the tail is read there
+            pr[mt][r] = valid ? sc[mt][2 * r] + sc[mt][2 * r + 1] : -INFINITY;
+            mx = fmaxf(mx, pr[mt][r]);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(full, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(full, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(full, mx, 16));
+        const float mn = fmaxf(m_run, mx);
+        const float mref = (mn == -INFINITY) ? 0.0f : mn;
+        const float al = fast_exp2(m_run - mref);  // 0 while nothing was valid
+        m_run = mn;
+        l_run *= al;
+#pragma unroll
+        for (int m = 0; m < MV; ++m) {
+          oacc[m][0] *= al;
+          oacc[m][1] *= al;
+          oacc[m][2] *= al;
+          oacc[m][3] *= al;
+        }
+        uint32_t R[4];  // weights of rows g (+8) of m-tile mt as (value, residual) in the C layout
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float p = fast_exp2(pr[mt][r] - mref);
+            l_run += p;
+            const uint32_t hv = pack_act2<BF>(p, 0.0f);
+            const float ph = unpack_act2<BF>(hv).x;
+            R[mt * 2 + r] = pack_act2<BF>(ph, __fsub_rn(p, ph));
+          }
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          const uint32_t b0 = movmatrix_t(R[2 * kb]);
+          const uint32_t b1 = movmatrix_t(R[2 * kb + 1]);
+#pragma unroll
+          for (int m = 0; m < MV; ++m) {
+            uint32_t A[4];
+            ldmatrix_x4_trans(A, sv + static_cast<size_t>(rb + 16 * kb + 8 * (lane >> 4) + (lane & 7)) * D +
+                                     16 * m + 8 * ((lane >> 3) & 1));
+            mma_act<BF>(oacc[m], A[0], A[1], A[2], A[3], b0, b1);
+          }
+        }
+      }
+    }
+    ok = __syncthreads_and(ok);  // the batch is consumed (and the verdict shared) before the next copy
+    if (!ok) break;
+    if (threadIdx.x == 0 && i1 < n_items) issue(i1, i1 + cap < n_items ? i1 + cap : n_items);
+  }
+  if (!ok) {
+    // copies of the failed batch may still be in flight: let them land
+    if (threadIdx.x == 0) (void)mbar_wait_bounded(bar, phase ^ 1);
+    __syncthreads();
+  }
+  l_run += __shfl_xor_sync(full, l_run, 4);
+  l_run += __shfl_xor_sync(full, l_run, 8);
+  l_run += __shfl_xor_sync(full, l_run, 16);
+  if (t < gq) {
+    float* rj = red + (warp * kMaxGqa + t) * (D + 2);
+#pragma unroll
+    for (int m = 0; m < MV; ++m) {
+      rj[16 * m + g] = oacc[m][0] + oacc[m][1];
+      rj[16 * m + g + 8] = oacc[m][2] + oacc[m][3];
+    }
+    if (g == 0) {
+      rj[D] = m_run;
+      rj[D + 1] = l_run;
     }
   }
   __syncthreads();
-  write_partial<D, NW>(a, red, b, h, 0);
+  return ok;
 }
 
 }  // namespace kvq

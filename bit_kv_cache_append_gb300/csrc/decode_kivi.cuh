@@ -7,9 +7,9 @@
 // (n_ctas = SM count x resident CTAs). A CTA walks its range unit by unit;
 // for each unit it touches, its 4 warp pairs take the unit's groups in turn
 // (p, p+4, ...) and the CTA merges the pairs into one partial (max, sum,
-// unnormalised output) per query head. The first B*Hkv CTAs instead handle
-// the exact pools of one unit each (sinks and tail, exact_partition). The
-// LSE merge kernel combines every partial of a (sequence, query head).
+// unnormalised output) per query head. The exact pools (sinks and tail) are
+// left to the merge kernel, which combines them with every partial of a
+// (sequence, query head).
 //
 // Warp specialisation: a pair is a QK warp and a PV warp working on the same
 // group stream. The QK warp turns the K codes into scores and softmax
@@ -59,13 +59,6 @@ __device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t 
   return d;
 }
 
-// 2^x by the hardware approximation (relative error about 2^-22; -inf -> 0),
-// enough for softmax weights.
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 __device__ __forceinline__ __half2 as_h2(uint32_t x) { return *reinterpret_cast<__half2*>(&x); }
 __device__ __forceinline__ uint32_t as_u32(__half2 x) { return *reinterpret_cast<uint32_t*>(&x); }
@@ -216,20 +209,6 @@ struct ItemCursor {
   }
 };
 
-// Bounded wait that also gives up when another warp of the CTA has given up.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
-      *abort_flag = 1;
-      return false;
-    }
-  }
-  return true;
-}
-
 #ifndef KVQ_DECODE_MIN_CTAS
 #define KVQ_DECODE_MIN_CTAS 2
 #endif
@@ -245,14 +224,10 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
   float* red = reinterpret_cast<float*>(smem + T::OFF_RED);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_ABORT);
 
+  pdl_launch_dependents();
   const Geometry& G = a.geo;
-  const int n_exact = G.B * G.H;
-  if (static_cast<int>(blockIdx.x) < n_exact) {
-    exact_partition<D, 8>(a, blockIdx.x / G.H, blockIdx.x % G.H, red);
-    return;
-  }
   const unsigned full = 0xffffffffu;
-  const int cta = blockIdx.x - n_exact;
+  const int cta = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pair = warp & (NP - 1);
   const bool is_pv = warp >= NP;
@@ -565,7 +540,7 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
       }
     }
     __syncthreads();  // (2) red complete
-    write_partial<D, 8>(a, red, b, h, 1 + cta - owner_cta(unit * ng, work, a.n_ctas), NP);
+    write_partial<D, 8>(a, red, b, h, cta - owner_cta(unit * ng, work, a.n_ctas), NP);
     seg = seg_e;
   }
   if ((failed || *abort_flag) && lane == 0) set_error(a.tab.err_flag, kErrTimeout);
@@ -580,25 +555,30 @@ template <int D, int KB, int VB>
 cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
   using T = KiviTile<D, KB, VB>;
   const size_t smem = T::smem_bytes();
-  static int occupancy = 0;
+  static int occ_of[kMaxDevices] = {};  // per device: the attribute is per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int& occupancy = occ_of[dev];
   if (!occupancy) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kivi_kernel<D, KB, VB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = cudaFuncSetAttribute(decode_kivi_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, decode_kivi_kernel<D, KB, VB>, 256, smem);
     if (e != cudaSuccess) return e;
     if (occupancy < 1) occupancy = 1;
   }
   // stream-K CTAs: fill the machine, never more than one per group, and at
-  // most max_splits - 1 per unit (partial slots per query head)
+  // most max_splits per unit (partial slots per query head)
   int64_t n = a.n_ctas_hint > 0 ? a.n_ctas_hint : static_cast<int64_t>(sm_count) * occupancy;
   const int64_t units = static_cast<int64_t>(a.geo.B) * a.geo.H;
   if (n > a.work) n = a.work;
-  if (n > units * (a.geo.max_splits - 2)) n = units * (a.geo.max_splits - 2);
+  if (n > units * (a.geo.max_splits - 1)) n = units * (a.geo.max_splits - 1);
   if (n < 1) n = 1;
   a.n_ctas = static_cast<int>(n);
-  const int n_exact = a.geo.B * a.geo.H;
-  decode_kivi_kernel<D, KB, VB><<<n_exact + (a.work > 0 ? a.n_ctas : 0), 256, smem, s>>>(a);
+  if (a.work <= 0) return cudaSuccess;  // nothing quantised to read: the merge does it all
+  decode_kivi_kernel<D, KB, VB><<<a.n_ctas, 256, smem, s>>>(a);
   return cudaGetLastError();
 }
 

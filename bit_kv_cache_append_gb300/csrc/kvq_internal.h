@@ -64,7 +64,7 @@ struct DecodeArgs {
   int n_ctas_hint;      // 0 = SM count x occupancy
   int groups_per_split; // TurboQuant: groups per partition
   int n_splits;         // TurboQuant: quantised partitions
-  int ns;               // partial slots per (sequence, query head); slot 0 = exact pools
+  int ns;               // partial slot stride per (sequence, query head)
   int n_sink_read;      // overlay: sink slots [0, n) read from the sink buffer
   int n_dyn_sel;        // KVSink: selected sinks (read when pos < F)
   float qscale;         // log2(e) / sqrt(D)

@@ -47,6 +47,7 @@ namespace kvq {
 constexpr int kGroup = 32;
 constexpr int kMaxSinks = 32;
 constexpr int kMaxGqa = 4;
+constexpr int kMaxDevices = 64;  // device ordinals the per-device launch settings cover
 
 struct Chunk {
   int kc_off, kmeta_off, vc_off, vmeta_off, bytes;

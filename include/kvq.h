@@ -257,7 +257,8 @@ kv_status kv_cache_check_device_error(kv_cache* cache, void* cuda_stream);
 
 /* Optional timing hook: when both are non-NULL, kv_decode_attn records
  * ev_begin (a cudaEvent_t) right before its split kernel and ev_end right
- * after it, on the call's stream. Pass NULLs to turn it off. */
+ * after its merge kernel (the whole decode), on the call's stream. Pass
+ * NULLs to turn it off. */
 kv_status kv_cache_set_timing_events(kv_cache* cache, void* ev_begin, void* ev_end);
 
 /* Number of kernels this library has launched in this process. */

@@ -98,6 +98,25 @@ def test_turboquant_codes_and_attention(kb, vb, D):
     _decode_both(gc, oc, 0, W.queries(w, 6), "f16")
 
 
+@pytest.mark.parametrize("D", [128, 64])
+def test_turboquant_with_sinks_and_window(D):
+    """TurboQuant with the exact overlay: sinks and the recent window are read
+    exact (original domain) while the quantised middle is decoded in the
+    rotated domain; the two parts meet in the merge."""
+    w = W.scaled(W.WORKLOADS["turboquant_k4v2"], batch=2, n_kv_heads=2, n_q_heads=8, head_dim=D,
+                 n_sink=4, window=40)
+    gc, oc = _pair(cache_kwargs(w, 1024, seed=77))
+    k, v = W.kv_tokens(w, 9, 300)
+    gc.prefill_quantize(0, torch_act(k, "f16"), torch_act(v, "f16"))
+    oc.prefill_quantize(0, k, v)
+    for i in range(6):
+        k, v = W.kv_tokens(w, 9, 1 + 7 * i, first_pos=300 + i)
+        gc.append(0, torch_act(k, "f16"), torch_act(v, "f16"))
+        oc.append(0, k, v)
+        _decode_both(gc, oc, 0, W.queries(w, 9, i), "f16")
+    compare_exports(gc, oc, 0)
+
+
 def test_turboquant_zero_rows():
     w = W.scaled(W.WORKLOADS["turboquant_k4v4"], batch=1, n_kv_heads=2, n_q_heads=2)
     gc, oc = _pair(cache_kwargs(w, 256))
