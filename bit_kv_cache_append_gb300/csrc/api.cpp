@@ -727,10 +727,11 @@ kv_status kv_cache_export(kv_cache* cache, int layer, int what, void* host_dst, 
           } else if (what == KV_EXPORT_V_SCALE || what == KV_EXPORT_V_ZERO) {
             const int nv = static_cast<int>(D) / kGroup;
             uint16_t* o = reinterpret_cast<uint16_t*>(dst) + (bh * p.n + gi * kGroup) * nv;
-            const int plane = what == KV_EXPORT_V_ZERO ? nv : 0;
             for (int r = 0; r < kGroup; ++r)
-              for (int vg = 0; vg < nv; ++vg)
-                std::memcpy(o + r * nv + vg, chunk.data() + g.chunk.vmeta_off + (r * 2 * nv + plane + vg) * 2, 2);
+              for (int vg = 0; vg < nv; ++vg) {
+                const int pos = what == KV_EXPORT_V_ZERO ? kvq::vzero_pos(nv, r, vg) : kvq::vscale_pos(nv, r, vg);
+                std::memcpy(o + r * nv + vg, chunk.data() + g.chunk.vmeta_off + pos * 2, 2);
+              }
           } else if (what == KV_EXPORT_K_NORM || what == KV_EXPORT_V_NORM) {
             float* o = reinterpret_cast<float*>(dst) + bh * p.n + gi * kGroup;
             const int off = what == KV_EXPORT_K_NORM ? g.chunk.kmeta_off : g.chunk.vmeta_off;

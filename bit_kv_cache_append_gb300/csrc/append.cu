@@ -192,9 +192,9 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
       const int c = base + ((i + 8 * vg) & 31);
       cv[r][c] = quantize_code(xv[r][c], s, z, G.vb);
     }
-    __half* vm = reinterpret_cast<__half*>(chunk + G.chunk.vmeta_off) + r * 2 * NV;
-    vm[vg] = sh;
-    vm[NV + vg] = zh;
+    __half* vm = reinterpret_cast<__half*>(chunk + G.chunk.vmeta_off);
+    vm[vscale_pos(NV, r, vg)] = sh;
+    vm[vzero_pos(NV, r, vg)] = zh;
   }
   __syncthreads();
 

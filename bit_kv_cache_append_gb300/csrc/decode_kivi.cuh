@@ -240,23 +240,25 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
   uint8_t* stages = smem + pair * NST * CHUNK;
   uint8_t* pbuf = smem + T::OFF_PBUF + pair * 2 * T::PBUF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR) + pair * (NST + 4);
-  uint64_t* full_bar = bars;            // [NST] chunk landed
-  uint64_t* pfull = bars + NST;         // [2] weights written
-  uint64_t* pempty = bars + NST + 2;    // [2] weights read
+  uint64_t* full_bar = bars;            // [NST] chunk landed (one arrival: the copy's issuer)
+  uint64_t* pfull = bars + NST;         // [2] weights written (32 arrivals: the QK warp's lanes)
+  uint64_t* pempty = bars + NST + 2;    // [2] weights read (32 arrivals: the PV warp's lanes)
   if (threadIdx.x == 0) *abort_flag = 0;
   if (is_pv && lane == 0) {
-    for (int i = 0; i < NST + 4; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < NST; ++i) mbar_init(&full_bar[i], 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&pfull[i], 32);
     mbar_fence_init();
   }
   __syncthreads();
 
-  ItemCursor pc;  // producer (PV lane 0): the next item whose chunk is to be fetched
+  // producer state (the PV warp: every lane keeps the same cursor, lane 0
+  // issues): the next item whose chunk is to be fetched
+  ItemCursor pc;
   int issued = 0;
-  if (is_pv && lane == 0) {
+  if (is_pv) {
     pc.enter(i0, i1, ng, pair, a.g_begin, n_slots, a.lay.chunks, CHUNK);
     for (int i = 0; i < NST && pc.item >= 0; ++i) {
-      mbar_expect_tx(&full_bar[i], CHUNK);
-      bulk_g2s(stages + i * CHUNK, pc.ptr, CHUNK, &full_bar[i]);
+      bulk_g2s_if(lane == 0, stages + i * CHUNK, pc.ptr, CHUNK, &full_bar[i]);
       pc.advance(i1, ng, pair, a.g_begin, n_slots, a.lay.chunks, CHUNK);
       ++issued;
     }
@@ -266,17 +268,21 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
 
   int64_t seg = i0;
   while (seg < i1) {
-    const int64_t unit = seg / ng;
-    const int64_t seg_e = (unit + 1) * ng < i1 ? (unit + 1) * ng : i1;
+    const int64_t unit = seg / ng, ubase = unit * ng;
+    const int64_t seg_e = ubase + ng < i1 ? ubase + ng : i1;
     const int b = static_cast<int>(unit / G.H), h = static_cast<int>(unit % G.H);
+    // this pair's items of the segment: my0, my0 + NP, ... (n_my of them)
+    const int64_t my0 = seg + pair;
+    const int n_my = my0 < seg_e ? static_cast<int>((seg_e - my0 + NP - 1) / NP) : 0;
 
     if (!is_pv) {
       // ------------------------------------------------------------ QK warp
-      int64_t grp = a.g_begin + (seg - unit * ng) + pair;  // group of this pair's first item
-      int slot = static_cast<int>(grp % n_slots);
       const int jc = g >> 1;        // query head of this lane's B column
       const bool col_lo = g & 1;    // B column holds the residual part
-      uint32_t qh[S][2], qa[S][2];  // q of the lane's column: f16 value, and value-or-residual
+      // qa: the column's operand (value, or residual on "lo" columns);
+      // qx: the value on "lo" columns, zero on the others, so that
+      //     qa s + (qx s - f16(qx s)) is the column's folded operand
+      uint32_t qx[S][2], qa[S][2];
 #pragma unroll
       for (int s = 0; s < S; ++s)
 #pragma unroll
@@ -289,14 +295,18 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
           }
           const uint32_t hi = f2_to_h2(x0, x1);
           const float2 hf = h2_to_f2(hi);
-          qh[s][p] = hi;
+          qx[s][p] = col_lo ? hi : 0u;
           qa[s][p] = col_lo ? f2_to_h2(x0 - hf.x, x1 - hf.y) : hi;
         }
       float m_run = -INFINITY, l_run = 0.0f;
-      const int64_t first_item = unit * ng, last_item = first_item + ng - 1;  // the unit's edge groups
+      // the unit's first and last groups are the only partial ones
+      const int k_lo = (my0 == ubase) ? 0 : -1;
+      const int k_hi = (seg_e == ubase + ng && n_my > 0 && my0 + static_cast<int64_t>(n_my - 1) * NP == ubase + ng - 1)
+                           ? n_my - 1 : -1;
+      const bool n_dyn = G.n_dyn != 0;
       CodeConsts<KB> kc;
       kc.load(a);
-      for (int64_t item = seg + pair; item < seg_e && !failed; item += NP, ++n_t) {
+      for (int k = 0; k < n_my && !failed; ++k, ++n_t) {
         const int st = n_t % NST, pb = n_t & 1;
         if (__any_sync(full, !wait_or_abort(&full_bar[st], static_cast<uint32_t>((n_t / NST) & 1), abort_flag))) {
           failed = true;
@@ -325,10 +335,9 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
 #pragma unroll
               for (int p = 0; p < 2; ++p) {
                 const __half2 sv = as_h2(sp[2 * hlf + p]);
-                const __half2 x = __hmul2(as_h2(qh[s][p]), sv);
-                const __half2 y = __hfma2(as_h2(qh[s][p]), sv, __hneg2(x));
-                const __half2 z = __hfma2(as_h2(qa[s][p]), sv, y);
-                bq[s][p] = col_lo ? as_u32(z) : as_u32(x);
+                const __half2 x = __hmul2(as_h2(qx[s][p]), sv);
+                const __half2 y = __hfma2(as_h2(qx[s][p]), sv, __hneg2(x));  // exact residual of x
+                bq[s][p] = as_u32(__hfma2(as_h2(qa[s][p]), sv, y));
               }
               uint32_t za[4];
               ldmatrix_x4(za, zrow + s * 32);
@@ -357,13 +366,13 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
         }
 
         // valid tokens: inside [qlo, F) and not a KVSink sink of this group
-        // (only the first and last group of the segment can be partial)
         uint32_t vbits = 0xffffffffu;
-        if (item == first_item || item == last_item || G.n_dyn) {
+        if (k == k_lo || k == k_hi || n_dyn) {
+          const int64_t grp = a.g_begin + (my0 - ubase) + static_cast<int64_t>(k) * NP;
           const int64_t p0 = grp * kGroup;
           if (p0 < a.qlo) vbits &= 0xffffffffu << static_cast<int>(a.qlo - p0);
           if (p0 + kGroup > a.F) vbits &= (1u << static_cast<int>(a.F - p0)) - 1u;
-          if (G.n_dyn) vbits &= ~a.lay.sink_mask[b * n_slots + slot];
+          if (n_dyn) vbits &= ~a.lay.sink_mask[b * n_slots + static_cast<int>(grp % n_slots)];
         }
         float pr[2][2];
 #pragma unroll
@@ -411,12 +420,8 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
         }
         uint8_t* pw = pbuf + pb * T::PBUF;
         *reinterpret_cast<uint4*>(pw + lane * 16) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-        if (g == 0) reinterpret_cast<float*>(pw + 32 * 16)[t] = al;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pfull[pb]);
-        grp += NP;
-        slot += NP;
-        while (slot >= n_slots) slot -= n_slots;
+        reinterpret_cast<float*>(pw + 32 * 16)[t] = al;  // the 8 lanes of query head t store the same value
+        mbar_arrive(&pfull[pb]);
       }
       l_run += __shfl_xor_sync(full, l_run, 4);
       l_run += __shfl_xor_sync(full, l_run, 8);
@@ -430,15 +435,14 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
     } else {
       // ------------------------------------------------------------ PV warp
       float oacc[MV][4];
-      float zacc[NVG];
+      // zero-point sums: rows = V channel groups (g < NVG), columns as oacc
+      float zacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int m = 0; m < MV; ++m) oacc[m][0] = oacc[m][1] = oacc[m][2] = oacc[m][3] = 0.0f;
-#pragma unroll
-      for (int v = 0; v < NVG; ++v) zacc[v] = 0.0f;
       const __half2 keep_lo = __halves2half2(__float2half_rn(0.0f), __float2half_rn(1.0f));
       CodeConsts<VB> vc;
       vc.load(a);
-      for (int64_t item = seg + pair; item < seg_e && !failed; item += NP, ++n_t) {
+      for (int k = 0; k < n_my && !failed; ++k, ++n_t) {
         const int st = n_t % NST, pb = n_t & 1;
         const bool ok = wait_or_abort(&pfull[pb], static_cast<uint32_t>((n_t >> 1) & 1), abort_flag) &&
                         wait_or_abort(&full_bar[st], static_cast<uint32_t>((n_t / NST) & 1), abort_flag);
@@ -450,8 +454,7 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
         const uint8_t* pw = pbuf + pb * T::PBUF;
         const uint4 pv4 = *reinterpret_cast<const uint4*>(pw + lane * 16);
         const float al = reinterpret_cast<const float*>(pw + 32 * 16)[t];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pempty[pb]);
+        mbar_arrive(&pempty[pb]);
         const uint32_t ph[4] = {pv4.x, pv4.y, pv4.z, pv4.w};
         if (__any_sync(full, al != 1.0f)) {
 #pragma unroll
@@ -462,41 +465,45 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
             oacc[m][3] *= al;
           }
 #pragma unroll
-          for (int v = 0; v < NVG; ++v) zacc[v] *= al;
+          for (int e = 0; e < 4; ++e) zacc[e] *= al;
         }
         uint32_t vr[VW];
 #pragma unroll
         for (int i = 0; i < VW / 4; ++i)
           *reinterpret_cast<uint4*>(&vr[4 * i]) = reinterpret_cast<const uint4*>(tile + T::VC)[i * 32 + lane];
-        // V scales and zeros of this thread's four tokens (NVG/2 f16x2 words
-        // of scales, then NVG/2 of zeros, per token)
-        __half2 vsp[4][NVG / 2], vzp[4][NVG / 2];
-        float pf[4];
+        // V scales of this thread's four tokens (NVG f16 per token)
+        uint32_t vsw[4][NVG / 2];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int tok = 16 * (k >> 1) + g + 8 * (k & 1);
-          const __half2* row = reinterpret_cast<const __half2*>(tile + T::VMETA) + tok * NVG;
+        for (int kk = 0; kk < 4; ++kk) {
+          const int tok = 16 * (kk >> 1) + g + 8 * (kk & 1);
+          const uint32_t* row = reinterpret_cast<const uint32_t*>(tile + T::VMETA) + tok * (NVG / 2);
 #pragma unroll
-          for (int i = 0; i < NVG / 2; ++i) {
-            vsp[k][i] = row[i];
-            vzp[k][i] = row[NVG / 2 + i];
+          for (int i = 0; i < NVG / 2; ++i) vsw[kk][i] = row[i];
+        }
+        // zero points: zsum[v][j] += sum_t zV[t][v] p_j[t] as one MMA per
+        // 16 tokens with the groups as rows (the zeros are stored group-major)
+        {
+          const uint32_t* zw = reinterpret_cast<const uint32_t*>(tile + T::VMETA + 64 * NVG);
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            const uint32_t bz0 = movmatrix_t(ph[2 * kb]);
+            const uint32_t bz1 = movmatrix_t(ph[2 * kb + 1]);
+            const uint32_t z0 = g < NVG ? zw[g * 16 + 8 * kb + t] : 0u;
+            const uint32_t z2 = g < NVG ? zw[g * 16 + 8 * kb + t + 4] : 0u;
+            mma_f16(zacc, z0, 0u, z2, 0u, bz0, bz1);
           }
-          const __half2 pk = as_h2(ph[k]);
-          pf[k] = __low2float(pk) + __high2float(pk);
         }
 #pragma unroll
         for (int v = 0; v < NVG; ++v) {
           uint32_t R[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const __half2 s2 = (v & 1) ? __high2half2(vsp[k][v >> 1]) : __low2half2(vsp[k][v >> 1]);
-            const float zv = (v & 1) ? __high2float(vzp[k][v >> 1]) : __low2float(vzp[k][v >> 1]);
+          for (int kk = 0; kk < 4; ++kk) {
+            const __half2 s2 = (v & 1) ? __high2half2(as_h2(vsw[kk][v >> 1])) : __low2half2(as_h2(vsw[kk][v >> 1]));
             // (p_hi s, p_lo s), the exact residual of p_hi s, and their sum
-            const __half2 pk = as_h2(ph[k]);
+            const __half2 pk = as_h2(ph[kk]);
             const __half2 x = __hmul2(pk, s2);
             const __half2 e = __hfma2(__low2half2(pk), s2, __hneg2(__low2half2(x)));
-            R[k] = as_u32(__hfma2(e, keep_lo, x));
-            zacc[v] = fmaf(pf[k], zv, zacc[v]);
+            R[kk] = as_u32(__hfma2(e, keep_lo, x));
           }
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
@@ -516,31 +523,27 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
         }
         // this pair is done with the stage: refill it with the next chunk
         __syncwarp();
-        if (lane == 0 && pc.item >= 0) {
-          mbar_expect_tx(&full_bar[st], CHUNK);
-          bulk_g2s(stages + st * CHUNK, pc.ptr, CHUNK, &full_bar[st]);
+        if (pc.item >= 0) {
+          bulk_g2s_if(lane == 0, stages + st * CHUNK, pc.ptr, CHUNK, &full_bar[st]);
           pc.advance(i1, ng, pair, a.g_begin, n_slots, a.lay.chunks, CHUNK);
           ++issued;
         }
       }
-#pragma unroll
-      for (int v = 0; v < NVG; ++v) {
-        zacc[v] += __shfl_xor_sync(full, zacc[v], 4);
-        zacc[v] += __shfl_xor_sync(full, zacc[v], 8);
-        zacc[v] += __shfl_xor_sync(full, zacc[v], 16);
-      }
+      // zero sum of group v, query head t, is in lane (v, t)
+      const float zt = zacc[0] + zacc[1];
       __syncthreads();  // (1) the previous unit's partial has been written
-      if (t < gq) {
-        float* rj = red + (pair * kMaxGqa + t) * (D + 2);
 #pragma unroll
-        for (int m = 0; m < MV; ++m) {
-          rj[16 * m + g] = fmaf(oacc[m][0] + oacc[m][1], CodeConsts<VB>::kCodeInv, zacc[m / 2]);
-          rj[16 * m + g + 8] = fmaf(oacc[m][2] + oacc[m][3], CodeConsts<VB>::kCodeInv, zacc[m / 2]);
+      for (int m = 0; m < MV; ++m) {
+        const float zg = __shfl_sync(full, zt, (m >> 1) * 4 + t);
+        if (t < gq) {
+          float* rj = red + (pair * kMaxGqa + t) * (D + 2);
+          rj[16 * m + g] = fmaf(oacc[m][0] + oacc[m][1], CodeConsts<VB>::kCodeInv, zg);
+          rj[16 * m + g + 8] = fmaf(oacc[m][2] + oacc[m][3], CodeConsts<VB>::kCodeInv, zg);
         }
       }
     }
     __syncthreads();  // (2) red complete
-    write_partial<D, 8>(a, red, b, h, cta - owner_cta(unit * ng, work, a.n_ctas), NP);
+    write_partial<D, 8>(a, red, b, h, cta - owner_cta(ubase, work, a.n_ctas), NP);
     seg = seg_e;
   }
   if ((failed || *abort_flag) && lane == 0) set_error(a.tab.err_flag, kErrTimeout);

@@ -4,7 +4,8 @@
 //
 // A "chunk" holds one 32-token group of one (layer, b, kv-head):
 //   KIVI:       [K codes 32*D*kb/8][K scales D f16][K zeros D f16]
-//               [V codes 32*D*vb/8][V meta 32 x (scales D/32 f16, zeros D/32 f16)]
+//               [V codes 32*D*vb/8][V scales 32 x D/32 f16][V zeros D/32 x 32 f16]
+//               (V scales token-major, V zeros group-major: vscale_pos, vzero_pos)
 //   TurboQuant: [K codes 32 x D*kb/8 row-major][K norms 32 f32]
 //               [V codes 32 x D*vb/8 row-major][V norms 32 f32]
 // Chunk sizes are multiples of 16 bytes so one 1-D bulk copy moves a chunk.
@@ -105,6 +106,13 @@ KVQ_HD int kzero_pos(int D, int c) {
   const int s = r >> 2, p = (r >> 1) & 1, e = r & 1;
   return s * 16 + 2 * t + e + 8 * p;
 }
+
+// f16 positions inside the V meta of token r, channel group vg (NV groups):
+// the scales token by token, then the zeros group by group (so that one
+// 32-bit word holds the zeros of two consecutive tokens of a group, the A
+// operand of the decode kernel's zero-point MMA).
+KVQ_HD int vscale_pos(int NV, int r, int vg) { return r * NV + vg; }
+KVQ_HD int vzero_pos(int NV, int r, int vg) { return 32 * NV + vg * 32 + r; }
 
 // Word index and bit position of element f inside a lane block. Pair
 // j = (f % per_word) / 2 of a word holds elements e = 0, 1 (f = 2P + e):
