@@ -39,6 +39,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test for completion of phase `parity`.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` for at most about one second of SM clock.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -254,6 +267,25 @@ __device__ __forceinline__ uint32_t split_act2(float x0, float x1, bool lo) {
 // Rows per tile of the exact pools and the row capacity a stage of
 // `stage_bytes` gives (whole tiles).
 constexpr int kExactTile = 32;
+
+// Warp-wide bounded wait for phase `parity` of `bar`: every decision is taken
+// by warp votes, so the warp stays converged and the common case (the phase
+// is already complete) costs one test and one vote. Gives up, raising the
+// CTA's abort flag, after about one second of SM clock or as soon as another
+// warp has raised it.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const unsigned full = 0xffffffffu;
+  if (__all_sync(full, mbar_test(bar, parity))) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (__all_sync(full, mbar_try_wait(bar, parity))) return true;
+    if (__any_sync(full, *abort_flag != 0)) return false;
+    if (__any_sync(full, clock64() - t0 > kWaitCycles)) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
 
 // The exact pools of one (b, h): the sinks read from the sink buffer and the
 // tail [F, L) read from the ring, with the query at full precision (RoPE at

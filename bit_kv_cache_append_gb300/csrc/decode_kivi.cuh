@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
       kc.load(a);
       for (int k = 0; k < n_my && !failed; ++k, ++n_t) {
         const int st = n_t % NST, pb = n_t & 1;
-        if (__any_sync(full, !wait_or_abort(&full_bar[st], static_cast<uint32_t>((n_t / NST) & 1), abort_flag))) {
+        if (!warp_wait(&full_bar[st], static_cast<uint32_t>((n_t / NST) & 1), abort_flag)) {
           failed = true;
           break;
         }
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
 
         // valid tokens: inside [qlo, F) and not a KVSink sink of this group
         uint32_t vbits = 0xffffffffu;
-        if (k == k_lo || k == k_hi || n_dyn) {
+        if (__any_sync(full, k == k_lo || k == k_hi) || n_dyn) {
           const int64_t grp = a.g_begin + (my0 - ubase) + static_cast<int64_t>(k) * NP;
           const int64_t p0 = grp * kGroup;
           if (p0 < a.qlo) vbits &= 0xffffffffu << static_cast<int>(a.qlo - p0);
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
             ph[mt * 2 + r] = as_u32(__halves2half2(hp, __float2half_rn(p - __half2float(hp))));
           }
         // hand the weights to the PV warp
-        if (__any_sync(full, !wait_or_abort(&pempty[pb], static_cast<uint32_t>(((n_t >> 1) & 1) ^ 1), abort_flag))) {
+        if (!warp_wait(&pempty[pb], static_cast<uint32_t>(((n_t >> 1) & 1) ^ 1), abort_flag)) {
           failed = true;
           break;
         }
@@ -444,9 +444,8 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
       vc.load(a);
       for (int k = 0; k < n_my && !failed; ++k, ++n_t) {
         const int st = n_t % NST, pb = n_t & 1;
-        const bool ok = wait_or_abort(&pfull[pb], static_cast<uint32_t>((n_t >> 1) & 1), abort_flag) &&
-                        wait_or_abort(&full_bar[st], static_cast<uint32_t>((n_t / NST) & 1), abort_flag);
-        if (__any_sync(full, !ok)) {
+        if (!warp_wait(&pfull[pb], static_cast<uint32_t>((n_t >> 1) & 1), abort_flag) ||
+            !warp_wait(&full_bar[st], static_cast<uint32_t>((n_t / NST) & 1), abort_flag)) {
           failed = true;
           break;
         }
