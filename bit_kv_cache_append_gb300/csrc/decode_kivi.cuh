@@ -134,6 +134,15 @@ __device__ __forceinline__ uint32_t code_pair(const CodeConsts<BITS>& k, uint32_
 // Headroom (log2 units) the running softmax max may lag behind the scores.
 constexpr float kLazyRescale = KVQ_LAZY_RESCALE;
 
+// CTA shape: KVQ_DECODE_PAIRS warp pairs per CTA, at least
+// KVQ_DECODE_MIN_CTAS CTAs resident per SM (the register budget follows).
+#ifndef KVQ_DECODE_PAIRS
+#define KVQ_DECODE_PAIRS 4
+#endif
+#ifndef KVQ_DECODE_MIN_CTAS
+#define KVQ_DECODE_MIN_CTAS (8 / KVQ_DECODE_PAIRS)
+#endif
+
 template <int D, int KB, int VB>
 struct KiviTile {
   static constexpr int KC = 32 * D * KB / 8;
@@ -141,9 +150,9 @@ struct KiviTile {
   static constexpr int VC = KMETA + 4 * D;
   static constexpr int VMETA = VC + 32 * D * VB / 8;
   static constexpr int CHUNK = VMETA + 4 * D;
-  static constexpr int NP = 4;                          // warp pairs per CTA
+  static constexpr int NP = KVQ_DECODE_PAIRS;           // warp pairs per CTA
 #ifndef KVQ_DECODE_STAGES
-  static constexpr int NST = CHUNK <= 6144 ? 4 : 3;      // bulk-copy stages per pair
+  static constexpr int NST = 3;                          // bulk-copy stages per pair (3 measured best)
 #else
   static constexpr int NST = KVQ_DECODE_STAGES;
 #endif
@@ -151,7 +160,7 @@ struct KiviTile {
   // shared memory: stages | weight buffers | red | barriers | abort flag
   static constexpr int OFF_PBUF = NP * NST * CHUNK;
   static constexpr int OFF_RED = OFF_PBUF + NP * 2 * PBUF;
-  static constexpr int RED_FLOATS = 8 * kMaxGqa * (D + 2);  // also the exact partition's 8 warps
+  static constexpr int RED_FLOATS = NP * kMaxGqa * (D + 2);  // one merged state per pair
   static constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
   static constexpr int NBAR = NP * (NST + 4);             // full[NST], pfull[2], pempty[2]
   static constexpr int OFF_ABORT = OFF_BAR + NBAR * 8;
@@ -165,9 +174,10 @@ __device__ __forceinline__ int owner_cta(int64_t i, int64_t work, int n) {
 }
 
 // Walks the items of pair p inside its CTA's range [i0, i1): per unit (run of
-// ng items), the unit's items s + p, s + p + 4, ... where s is the first item
-// of the unit inside the range. The group index and its ring slot advance by
-// additions; divisions happen only when the walk enters a new unit.
+// ng items), the unit's items s + p, s + p + NP, ... where s is the first
+// item of the unit inside the range. The group index and its ring slot
+// advance by additions; divisions happen only when the walk enters a new unit.
+template <int NP>
 struct ItemCursor {
   int64_t item;       // current item (-1: exhausted)
   int64_t seg_end;    // end of the current unit inside the range
@@ -194,11 +204,11 @@ struct ItemCursor {
   }
   __device__ __forceinline__ void advance(int64_t i1, int64_t ng, int w, int64_t g_begin, int n_slots,
                                           const uint8_t* chunks, int chunk_bytes) {
-    if (item + 4 < seg_end) {
-      item += 4;
-      grp += 4;
-      slot += 4;
-      ptr += 4 * chunk_bytes;
+    if (item + NP < seg_end) {
+      item += NP;
+      grp += NP;
+      slot += NP;
+      ptr += NP * chunk_bytes;
       while (slot >= n_slots) {
         slot -= n_slots;
         ptr -= static_cast<size_t>(n_slots) * chunk_bytes;
@@ -209,12 +219,9 @@ struct ItemCursor {
   }
 };
 
-#ifndef KVQ_DECODE_MIN_CTAS
-#define KVQ_DECODE_MIN_CTAS 2
-#endif
 
 template <int D, int KB, int VB>
-__global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(DecodeArgs a) {
   using T = KiviTile<D, KB, VB>;
   constexpr int NP = T::NP, NST = T::NST, CHUNK = T::CHUNK;
   constexpr int S = D / 16, MV = D / 16, NVG = D / 32;
@@ -229,7 +236,7 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
   const unsigned full = 0xffffffffu;
   const int cta = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = warp & (NP - 1);
+  const int pair = warp % NP;
   const bool is_pv = warp >= NP;
   const int g = lane >> 2, t = lane & 3;
   const int gq = G.gqa;
@@ -253,7 +260,7 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
 
   // producer state (the PV warp: every lane keeps the same cursor, lane 0
   // issues): the next item whose chunk is to be fetched
-  ItemCursor pc;
+  ItemCursor<NP> pc;
   int issued = 0;
   if (is_pv) {
     pc.enter(i0, i1, ng, pair, a.g_begin, n_slots, a.lay.chunks, CHUNK);
@@ -542,7 +549,7 @@ __global__ void __launch_bounds__(256, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(D
       }
     }
     __syncthreads();  // (2) red complete
-    write_partial<D, 8>(a, red, b, h, cta - owner_cta(ubase, work, a.n_ctas), NP);
+    write_partial<D, 2 * NP>(a, red, b, h, cta - owner_cta(ubase, work, a.n_ctas), NP);
     seg = seg_e;
   }
   if ((failed || *abort_flag) && lane == 0) set_error(a.tab.err_flag, kErrTimeout);
@@ -567,7 +574,7 @@ cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
     e = cudaFuncSetAttribute(decode_kivi_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, decode_kivi_kernel<D, KB, VB>, 256, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, decode_kivi_kernel<D, KB, VB>, 64 * T::NP, smem);
     if (e != cudaSuccess) return e;
     if (occupancy < 1) occupancy = 1;
   }
@@ -580,7 +587,7 @@ cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
   if (n < 1) n = 1;
   a.n_ctas = static_cast<int>(n);
   if (a.work <= 0) return cudaSuccess;  // nothing quantised to read: the merge does it all
-  decode_kivi_kernel<D, KB, VB><<<a.n_ctas, 256, smem, s>>>(a);
+  decode_kivi_kernel<D, KB, VB><<<a.n_ctas, 64 * T::NP, smem, s>>>(a);
   return cudaGetLastError();
 }
 
