@@ -1,6 +1,8 @@
 // Append-side kernels: exact tail ring and sink buffer writes, KIVI group
 // quantisation (with KVSink calibration exclusion), TurboQuant per-token
 // quantisation, and the KVSink sink-row gather.
+#include <algorithm>
+
 #include "kvq_device.cuh"
 
 namespace kvq {
@@ -83,20 +85,43 @@ __device__ __forceinline__ void quantize_slice_params(float mn, float mx, int bi
   *z = __half2float(*zh);
 }
 
-__device__ __forceinline__ uint8_t quantize_code(float x, float s, float z, int bits) {
-  const float lb = static_cast<float>((1 << bits) - 1);
-  float q = rintf(__fdiv_rn(__fsub_rn(x, z), s));
-  q = fminf(fmaxf(q, 0.0f), lb);
-  return static_cast<uint8_t>(q);
+// Code of x for a slice with stored scale s, zero z and reciprocal rs =
+// 1/s (correctly rounded): rint of the correctly rounded quotient (x - z) / s
+// (x - z rounded on its own), clamped to [0, LB]. The quotient is formed as
+// (x - z) * rs, whose distance to the correctly rounded quotient is at most
+// about 2^-22 of its magnitude (two roundings of 2^-24 each, plus the
+// quotient's own): below 6.2e-5 while |q| <= 257. Away from a half-integer by
+// more than 1e-4 the two round to the same integer, and beyond 257 the clamp
+// decides; within 1e-4 of a half-integer the correctly rounded division is
+// taken, so the code equals rint(fl((x - z) / s)) in every case.
+template <int LB>
+__device__ __forceinline__ uint32_t quantize_code(float x, float s, float z, float rs) {
+  const float d = __fsub_rn(x, z);
+  const float q = __fmul_rn(d, rs);
+  float qr = rintf(q);
+  if (fabsf(__fsub_rn(q, qr)) > 0.4999f) qr = rintf(__fdiv_rn(d, s));  // within 1e-4 of a half-integer
+  qr = fminf(fmaxf(qr, 0.0f), static_cast<float>(LB));
+  return static_cast<uint32_t>(qr);
 }
 
-template <int D>
+// Bit position of the element i (0 .. 32/BITS - 1) of a packed word (the
+// frag_bits layout: pair j = i / 2, element e = i % 2).
+template <int BITS>
+__device__ __forceinline__ int word_bit(int i) {
+  const int j = i >> 1, e = i & 1;
+  if (BITS == 2) return 8 * (j & 3) + 2 * (j >> 2) + 4 * e;
+  if (BITS == 4) return 16 * (j & 1) + 4 * (j >> 1) + 8 * e;
+  return 8 * j + 16 * e;
+}
+
+template <int D, int KB, int VB>
 __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
   constexpr int HALF = D / 2, NV = D / 32, CPR = HALF / 8;
+  constexpr int LK = (1 << KB) - 1, LV = (1 << VB) - 1;
   __shared__ float xk[32][D + 1];
   __shared__ float xv[32][D + 1];
-  __shared__ uint8_t ck[32][D];
-  __shared__ uint8_t cv[32][D];
+  __shared__ uint8_t ck[32][D + 4];  // rows padded by a word: the packing gathers down columns
+  __shared__ uint8_t cv[32][D + 4];
   __shared__ int sub[32];
   __shared__ uint32_t smask;
   const Geometry& G = a.geo;
@@ -107,7 +132,7 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
   const int slot = static_cast<int>(g % G.n_slots);
   const int bf16 = G.act_bf16;
 
-  if (tid == 0) {
+  if (tid < 32) {  // KVSink: the nearest non-sink row of each row (ties to the earlier)
     uint32_t m = 0;
     if (a.dyn_active) {
       for (int j = 0; j < a.n_dyn_sel; ++j) {
@@ -115,20 +140,20 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
         if (p >= p0 && p < p0 + kGroup) m |= 1u << (p - p0);
       }
     }
-    smask = m;
-    for (int r = 0; r < 32; ++r) {
-      int s = r;
-      if (((m >> r) & 1u) && m != 0xFFFFFFFFu) {
-        for (int d = 1; d < 32; ++d) {
-          if (r - d >= 0 && !((m >> (r - d)) & 1u)) { s = r - d; break; }
-          if (r + d < 32 && !((m >> (r + d)) & 1u)) { s = r + d; break; }
-        }
+    const int r = tid;
+    int sr = r;
+    if (((m >> r) & 1u) && m != 0xFFFFFFFFu) {
+      for (int d = 1; d < 32; ++d) {
+        if (r - d >= 0 && !((m >> (r - d)) & 1u)) { sr = r - d; break; }
+        if (r + d < 32 && !((m >> (r + d)) & 1u)) { sr = r + d; break; }
       }
-      sub[r] = s;
     }
+    sub[r] = sr;
+    if (r == 0) smask = m;
   }
   __syncthreads();
 
+#pragma unroll
   for (int idx = tid; idx < 32 * CPR; idx += D) {
     const int r = idx / CPR, c0 = (idx % CPR) * 8;
     const int64_t pos = p0 + sub[r];
@@ -165,21 +190,25 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
   {  // K: channel tid over the 32 tokens
     const int c = tid;
     float mn = xk[0][c], mx = mn;
+#pragma unroll 8
     for (int r = 1; r < 32; ++r) {
       mn = fminf(mn, xk[r][c]);
       mx = fmaxf(mx, xk[r][c]);
     }
     __half sh, zh;
     float s, z;
-    quantize_slice_params(mn, mx, G.kb, &sh, &zh, &s, &z);
-    for (int r = 0; r < 32; ++r) ck[r][c] = quantize_code(xk[r][c], s, z, G.kb);
+    quantize_slice_params(mn, mx, KB, &sh, &zh, &s, &z);
+    const float rs = __frcp_rn(s);
+#pragma unroll 8
+    for (int r = 0; r < 32; ++r) ck[r][c] = static_cast<uint8_t>(quantize_code<LK>(xk[r][c], s, z, rs));
     __half* km = reinterpret_cast<__half*>(chunk + G.chunk.kmeta_off);
     km[kmeta_pos(D, c)] = sh;
     km[D + kzero_pos(D, c)] = zh;
   }
   {  // V: token r, channel group vg (index rotated by 8 vg to spread banks)
     const int r = tid / NV, vg = tid % NV, base = 32 * vg;
-    float mn = xv[r][base], mx = mn;
+    float mn = xv[r][base + ((8 * vg) & 31)], mx = mn;
+#pragma unroll 8
     for (int i = 0; i < 32; ++i) {
       const float x = xv[r][base + ((i + 8 * vg) & 31)];
       mn = fminf(mn, x);
@@ -187,10 +216,12 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
     }
     __half sh, zh;
     float s, z;
-    quantize_slice_params(mn, mx, G.vb, &sh, &zh, &s, &z);
+    quantize_slice_params(mn, mx, VB, &sh, &zh, &s, &z);
+    const float rs = __frcp_rn(s);
+#pragma unroll 8
     for (int i = 0; i < 32; ++i) {
       const int c = base + ((i + 8 * vg) & 31);
-      cv[r][c] = quantize_code(xv[r][c], s, z, G.vb);
+      cv[r][c] = static_cast<uint8_t>(quantize_code<LV>(xv[r][c], s, z, rs));
     }
     __half* vm = reinterpret_cast<__half*>(chunk + G.chunk.vmeta_off);
     vm[vscale_pos(NV, r, vg)] = sh;
@@ -198,32 +229,43 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
   }
   __syncthreads();
 
-  const int kwpl = D * G.kb / 32, vwpl = D * G.vb / 32;  // words per lane block
-  for (int wi = tid; wi < 32 * kwpl; wi += D) {
-    const int lane = wi / kwpl, w = wi % kwpl, per = 32 / G.kb;
+  // pack in the decode kernel's fragment order (kvq_layout.h)
+  constexpr int KPER = 32 / KB, VPER = 32 / VB;
+  constexpr int KWPL = D * KB / 32, VWPL = D * VB / 32;  // words per lane block
+  for (int wi = tid; wi < 32 * KWPL; wi += D) {
+    const int lane = wi / KWPL, w = wi % KWPL;
     uint32_t word = 0;
-    for (int i = 0; i < per; ++i) {
-      int tok, ch, wd, bit;
-      const int f = w * per + i;
-      k_frag_pos(D, lane, f, &tok, &ch);
-      frag_bits(G.kb, f, &wd, &bit);
-      word |= static_cast<uint32_t>(ck[tok][ch]) << bit;
+#pragma unroll
+    for (int i = 0; i < KPER; ++i) {
+      int tok, ch;
+      k_frag_pos(D, lane, w * KPER + i, &tok, &ch);
+      word |= static_cast<uint32_t>(ck[tok][ch]) << word_bit<KB>(i);
     }
     *reinterpret_cast<uint32_t*>(chunk + G.chunk.kc_off + code_word_offset(lane, w)) = word;
   }
-  for (int wi = tid; wi < 32 * vwpl; wi += D) {
-    const int lane = wi / vwpl, w = wi % vwpl, per = 32 / G.vb;
+  for (int wi = tid; wi < 32 * VWPL; wi += D) {
+    const int lane = wi / VWPL, w = wi % VWPL;
     uint32_t word = 0;
-    for (int i = 0; i < per; ++i) {
-      int tok, ch, wd, bit;
-      const int f = w * per + i;
-      v_frag_pos(D, lane, f, &tok, &ch);
-      frag_bits(G.vb, f, &wd, &bit);
-      word |= static_cast<uint32_t>(cv[tok][ch]) << bit;
+#pragma unroll
+    for (int i = 0; i < VPER; ++i) {
+      int tok, ch;
+      v_frag_pos(D, lane, w * VPER + i, &tok, &ch);
+      word |= static_cast<uint32_t>(cv[tok][ch]) << word_bit<VB>(i);
     }
     *reinterpret_cast<uint32_t*>(chunk + G.chunk.vc_off + code_word_offset(lane, w)) = word;
   }
   if (G.n_dyn && h == 0 && tid == 0) a.lay.sink_mask[b * G.n_slots + slot] = smask;
+}
+
+template <int D>
+void launch_flush(const AppendArgs& a, dim3 grid, cudaStream_t s) {
+  const int kb = a.geo.kb, vb = a.geo.vb;
+#define KVQ_FLUSH(K, V) \
+  if (kb == K && vb == V) { kivi_flush_kernel<D, K, V><<<grid, D, 0, s>>>(a); return; }
+  KVQ_FLUSH(2, 2) KVQ_FLUSH(2, 4) KVQ_FLUSH(2, 8)
+  KVQ_FLUSH(4, 2) KVQ_FLUSH(4, 4) KVQ_FLUSH(4, 8)
+  KVQ_FLUSH(8, 2) KVQ_FLUSH(8, 4) KVQ_FLUSH(8, 8)
+#undef KVQ_FLUSH
 }
 
 // ---------------------------------------------------------------- TurboQuant
@@ -382,8 +424,8 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int64_t* launches
   const int BH = G.B * G.H;
   if (!G.mode_tq && a.n_groups > 0) {
     dim3 grid(a.n_groups, BH);
-    if (G.D == 128) kivi_flush_kernel<128><<<grid, 128, 0, s>>>(a);
-    else kivi_flush_kernel<64><<<grid, 64, 0, s>>>(a);
+    if (G.D == 128) launch_flush<128>(a, grid, s);
+    else launch_flush<64>(a, grid, s);
     ++*launches;
   }
   if (G.mode_tq && a.n > 0) {
@@ -392,16 +434,24 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int64_t* launches
     else tq_quantize_kernel<64><<<grid, 128, 0, s>>>(a, 0, a.n);
     ++*launches;
   }
-  int64_t first = a.n;
-  if (a.L0 < G.n_sink) first = 0;
-  else if (a.tail_from < a.L0 + a.n) first = a.tail_from > a.L0 ? a.tail_from - a.L0 : 0;
-  if (first < a.n) {
-    const int rows = static_cast<int>(a.n - first);
+  // rows [r0, r1) of the append that go to the sink buffer or the tail: the
+  // overlay sinks at the front, then everything from tail_from on
+  auto write_rows = [&](int64_t r0, int64_t r1) {
+    if (r0 >= r1) return;
+    const int rows = static_cast<int>(r1 - r0);
     const int cpr = G.D / 16;
     const int threads = 128;
     dim3 grid(static_cast<unsigned>((static_cast<int64_t>(rows) * cpr + threads - 1) / threads), BH);
-    tail_write_kernel<<<grid, threads, 0, s>>>(a, static_cast<int>(first), rows);
+    tail_write_kernel<<<grid, threads, 0, s>>>(a, static_cast<int>(r0), rows);
     ++*launches;
+  };
+  const int64_t n_front = a.L0 < G.n_sink ? std::min<int64_t>(a.n, G.n_sink - a.L0) : 0;
+  const int64_t t0 = std::min<int64_t>(a.n, std::max<int64_t>(0, a.tail_from - a.L0));
+  if (t0 <= n_front) {
+    write_rows(0, t0 < a.n ? a.n : n_front);  // one run
+  } else {
+    write_rows(0, n_front);
+    write_rows(t0, a.n);
   }
   return cudaGetLastError();
 }
