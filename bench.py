@@ -55,6 +55,23 @@ def dist_env():
     return rank, world, local
 
 
+def slowest_rank(pg, values, device):
+    """Every rank's timings replaced by the maximum over ranks (the job is
+    as slow as its slowest replica); identity without a process group."""
+    if pg is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_gbs(world, bytes_per_rank_step, ms_per_step):
+    """Aggregate bandwidth of `world` replicas each moving bytes_per_rank_step
+    per step of ms_per_step (the slowest rank's)."""
+    return world * bytes_per_rank_step / (ms_per_step / 1e3) / 1e9
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -114,6 +131,35 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+DECODE_SOURCES = ("decode_kivi.cuh", "decode_common.cuh", "decode.cu", "decode_d128.cu", "kvq_layout.h",
+                  "kvq_internal.h", "kvq_device.cuh")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "decode_llama8b_b8.md")
+
+
+def recorded_traffic():
+    """DRAM bytes (read + write) of one decode (split + merge) at batch 16,
+    from the committed ncu summary, if that capture was taken on the decode
+    sources as they are now (their sha256 is recorded beside the figure);
+    None otherwise."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "bit_kv_cache_append_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    fields = {}
+    try:
+        with open(TRAFFIC_RECORD) as fh:
+            for line in fh:
+                if line.startswith("- ") and ": " in line:
+                    k, v = line[2:].split(": ", 1)
+                    fields[k.strip()] = v.strip()
+    except OSError:
+        return None
+    if fields.get("decode_sources_sha256") != h.hexdigest() or "dram_bytes_per_launch_b16" not in fields:
+        return None
+    return int(fields["dram_bytes_per_launch_b16"])
 
 
 def make_inputs(torch, w, seed, n_tokens, device):
@@ -340,12 +386,8 @@ def run_ours(args, rank, world, local):
     copy_gbs = 2 * (1 << 30) / (statistics.median(cts) / 1e3) / 1e9
     del src, dst
 
-    ms_step = ms_total / args.steps
-    if pg:
-        t = torch.tensor([ms_step, e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_step, e2e_ms = float(t[0]), float(t[1])
-    value = world * step_bytes / (ms_step / 1e3) / 1e9
+    ms_step, e2e_ms = slowest_rank(pg, [ms_total / args.steps, e2e_ms], dev)
+    value = whole_job_gbs(world, step_bytes, ms_step)
     peak, peak_kind = measured_peaks()
     achieved = dec_bytes / (kernel_avg_ms / 1e3) / 1e9
     if rank == 0:
@@ -365,14 +407,17 @@ def run_ours(args, rank, world, local):
             "prefill_tokens_per_s": round(prefill_tok_s, 1),
             "copy_kernel_gbs": round(copy_gbs, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "frac": round(achieved / peak, 4),
+                         "traffic": recorded_traffic() if w["batch"] == 16 else None,
+                         "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of split + merge "
+                                           "at batch 8, scaled by units to batch 16 (profiles/decode_llama8b_b8.md)",
                          "kernel": "decode_kivi_kernel<128,2,4> + merge_kernel<128> (split-KV partitions; exact pools and LSE merge)",
                          "algorithmic_bytes_per_launch": int(dec_bytes), "peak_kind": f"{peak_kind} hbm_gbs",
                          "kernel_us": round(kernel_avg_ms * 1e3, 2)},
             "cpu_baseline": {"value": round(cpu_gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"{cpu_n} (sequence, KV head) units with 4 query heads each, "
                                        f"32768-token context, decode only ({cpu_t:.1f} s)"},
-            "e2e": {"value": round(world * step_bytes / (e2e_ms / 1e3) / 1e9, 3), "unit": "GB/s",
+            "e2e": {"value": round(whole_job_gbs(world, step_bytes, e2e_ms), 3), "unit": "GB/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
             "gpu_launches": int(launches),
             "clocks": clocks,
