@@ -119,6 +119,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Barrier `id` (1..15) over the first `threads` threads of the CTA.
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // A value the compiler must keep in a register (it cannot re-derive it).
 __device__ __forceinline__ uint32_t pin(uint32_t x) {
   uint32_t y;

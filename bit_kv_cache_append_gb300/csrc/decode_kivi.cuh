@@ -157,9 +157,10 @@ struct KiviTile {
   static constexpr int NST = KVQ_DECODE_STAGES;
 #endif
   static constexpr int PBUF = 32 * 16 + 16;              // weights (16 B per lane) + 4 rescale factors
-  // shared memory: stages | weight buffers | red | barriers | abort flag
+  // shared memory: stages | weight buffers | query operand | red | barriers | abort flag
   static constexpr int OFF_PBUF = NP * NST * CHUNK;
-  static constexpr int OFF_RED = OFF_PBUF + NP * 2 * PBUF;
+  static constexpr int OFF_Q = OFF_PBUF + NP * 2 * PBUF;  // [D/16 k-steps][32 lanes] x 16 B
+  static constexpr int OFF_RED = OFF_Q + (D / 16) * 32 * 16;
   static constexpr int RED_FLOATS = NP * kMaxGqa * (D + 2);  // one merged state per pair
   static constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
   static constexpr int NBAR = NP * (NST + 4);             // full[NST], pfull[2], pempty[2]
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
   using T = KiviTile<D, KB, VB>;
   constexpr int NP = T::NP, NST = T::NST, CHUNK = T::CHUNK;
   constexpr int S = D / 16, MV = D / 16, NVG = D / 32;
-  constexpr int KW = D * KB / 32, VW = D * VB / 32;
+  constexpr int KW = D * KB / 32;
   constexpr int KPPW = 16 / KB, VPPW = 16 / VB;  // code pairs per 32-bit word
   extern __shared__ __align__(128) uint8_t smem[];
   float* red = reinterpret_cast<float*>(smem + T::OFF_RED);
@@ -284,27 +285,34 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
 
     if (!is_pv) {
       // ------------------------------------------------------------ QK warp
-      const int jc = g >> 1;        // query head of this lane's B column
-      const bool col_lo = g & 1;    // B column holds the residual part
-      // qa: the column's operand (value, or residual on "lo" columns);
-      // qx: the value on "lo" columns, zero on the others, so that
-      //     qa s + (qx s - f16(qx s)) is the column's folded operand
-      uint32_t qx[S][2], qa[S][2];
+      // the query operand of the unit, shared by the CTA's QK warps: per
+      // k-step s and lane, {qx, qa} of the lane's two k-pairs, where qa is
+      // the column's operand (value, or residual on "lo" columns) and qx the
+      // value on "lo" columns, zero on the others, so that
+      // qa s + (qx s - f16(qx s)) is the column's folded operand
+      uint4* qsm = reinterpret_cast<uint4*>(smem + T::OFF_Q);
+      {
+        const int jc = g >> 1;        // query head of this lane's B column
+        const bool col_lo = g & 1;    // B column holds the residual part
+        for (int s = pair; s < S; s += NP) {
+          uint32_t v[4];
 #pragma unroll
-      for (int s = 0; s < S; ++s)
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-          const int c0 = t * (D / 4) + 4 * s + 2 * p;
-          float x0 = 0.0f, x1 = 0.0f;
-          if (jc < gq) {
-            x0 = query_value(a, b, h * gq + jc, c0);
-            x1 = query_value(a, b, h * gq + jc, c0 + 1);
+          for (int p = 0; p < 2; ++p) {
+            const int c0 = t * (D / 4) + 4 * s + 2 * p;
+            float x0 = 0.0f, x1 = 0.0f;
+            if (jc < gq) {
+              x0 = query_value(a, b, h * gq + jc, c0);
+              x1 = query_value(a, b, h * gq + jc, c0 + 1);
+            }
+            const uint32_t hi = f2_to_h2(x0, x1);
+            const float2 hf = h2_to_f2(hi);
+            v[2 * p] = col_lo ? hi : 0u;
+            v[2 * p + 1] = col_lo ? f2_to_h2(x0 - hf.x, x1 - hf.y) : hi;
           }
-          const uint32_t hi = f2_to_h2(x0, x1);
-          const float2 hf = h2_to_f2(hi);
-          qx[s][p] = col_lo ? hi : 0u;
-          qa[s][p] = col_lo ? f2_to_h2(x0 - hf.x, x1 - hf.y) : hi;
+          qsm[s * 32 + lane] = make_uint4(v[0], v[1], v[2], v[3]);
         }
+        named_barrier_sync(1, NP * 32);  // the QK warps only
+      }
       float m_run = -INFINITY, l_run = 0.0f;
       // the unit's first and last groups are the only partial ones
       const int k_lo = (my0 == ubase) ? 0 : -1;
@@ -330,8 +338,8 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           const uint4* ks = reinterpret_cast<const uint4*>(tile + T::KMETA);
           // the zero-point operand: every row is the k-step's zero row
           const uint8_t* zrow = tile + T::KMETA + 2 * D + ((lane >> 4) & 1) * 16;
-          uint32_t bq[S][2];
           float zb[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+          float sa[2][2][4] = {};
 #pragma unroll
           for (int u = 0; u < S / 2; ++u) {
             const uint4 s4 = ks[u * 4 + t];
@@ -339,29 +347,28 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
 #pragma unroll
             for (int hlf = 0; hlf < 2; ++hlf) {
               const int s = 2 * u + hlf;
+              const uint4 q4 = qsm[s * 32 + lane];
+              const uint32_t qx[2] = {q4.x, q4.z}, qa[2] = {q4.y, q4.w};
+              uint32_t bq[2];
 #pragma unroll
               for (int p = 0; p < 2; ++p) {
                 const __half2 sv = as_h2(sp[2 * hlf + p]);
-                const __half2 x = __hmul2(as_h2(qx[s][p]), sv);
-                const __half2 y = __hfma2(as_h2(qx[s][p]), sv, __hneg2(x));  // exact residual of x
-                bq[s][p] = as_u32(__hfma2(as_h2(qa[s][p]), sv, y));
+                const __half2 x = __hmul2(as_h2(qx[p]), sv);
+                const __half2 y = __hfma2(as_h2(qx[p]), sv, __hneg2(x));  // exact residual of x
+                bq[p] = as_u32(__hfma2(as_h2(qa[p]), sv, y));
               }
               uint32_t za[4];
               ldmatrix_x4(za, zrow + s * 32);
-              mma_f16(zb[hlf], za[0], za[1], za[2], za[3], qa[s][0], qa[s][1]);
-            }
-          }
-          float sa[2][2][4] = {};
+              mma_f16(zb[hlf], za[0], za[1], za[2], za[3], qa[0], qa[1]);
 #pragma unroll
-          for (int s = 0; s < S; ++s) {
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-              const int pbase = (mt * S + s) * 4;
-              const uint32_t a0 = code_pair<KB>(kc, kr[(pbase + 0) / KPPW], (pbase + 0) % KPPW);
-              const uint32_t a1 = code_pair<KB>(kc, kr[(pbase + 1) / KPPW], (pbase + 1) % KPPW);
-              const uint32_t a2 = code_pair<KB>(kc, kr[(pbase + 2) / KPPW], (pbase + 2) % KPPW);
-              const uint32_t a3 = code_pair<KB>(kc, kr[(pbase + 3) / KPPW], (pbase + 3) % KPPW);
-              mma_f16(sa[mt][s & 1], a0, a1, a2, a3, bq[s][0], bq[s][1]);
+              for (int mt = 0; mt < 2; ++mt) {
+                const int pbase = (mt * S + s) * 4;
+                const uint32_t a0 = code_pair<KB>(kc, kr[(pbase + 0) / KPPW], (pbase + 0) % KPPW);
+                const uint32_t a1 = code_pair<KB>(kc, kr[(pbase + 1) / KPPW], (pbase + 1) % KPPW);
+                const uint32_t a2 = code_pair<KB>(kc, kr[(pbase + 2) / KPPW], (pbase + 2) % KPPW);
+                const uint32_t a3 = code_pair<KB>(kc, kr[(pbase + 3) / KPPW], (pbase + 3) % KPPW);
+                mma_f16(sa[mt][s & 1], a0, a1, a2, a3, bq[0], bq[1]);
+              }
             }
           }
 #pragma unroll
@@ -473,10 +480,6 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
 #pragma unroll
           for (int e = 0; e < 4; ++e) zacc[e] *= al;
         }
-        uint32_t vr[VW];
-#pragma unroll
-        for (int i = 0; i < VW / 4; ++i)
-          *reinterpret_cast<uint4*>(&vr[4 * i]) = reinterpret_cast<const uint4*>(tile + T::VC)[i * 32 + lane];
         // V scales of this thread's four tokens (NVG f16 per token)
         uint32_t vsw[4][NVG / 2];
 #pragma unroll
@@ -499,8 +502,22 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
             mma_f16(zacc, z0, 0u, z2, 0u, bz0, bz1);
           }
         }
+        const uint4* vcode = reinterpret_cast<const uint4*>(tile + T::VC);
 #pragma unroll
         for (int v = 0; v < NVG; ++v) {
+          // the VB code words of channel group v (m-tiles 2v, 2v + 1), loaded
+          // when first needed to keep them live briefly
+          uint32_t vr[VB];
+#pragma unroll
+          for (int i = 0; i < (VB + 3) / 4; ++i) {
+            const uint4 w4 = vcode[((v * VB) / 4 + i) * 32 + lane];
+            const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+              const int wi = i * 4 + k2 - (v * VB) % 4;
+              if (wi >= 0 && wi < VB) vr[wi] = ww[k2];
+            }
+          }
           uint32_t R[4];
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
@@ -519,10 +536,10 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
             for (int hh = 0; hh < 2; ++hh) {
               const int m = 2 * v + hh;
               const int pbase = (m * 2 + kb) * 4;
-              const uint32_t a0 = code_pair<VB>(vc, vr[(pbase + 0) / VPPW], (pbase + 0) % VPPW);
-              const uint32_t a1 = code_pair<VB>(vc, vr[(pbase + 1) / VPPW], (pbase + 1) % VPPW);
-              const uint32_t a2 = code_pair<VB>(vc, vr[(pbase + 2) / VPPW], (pbase + 2) % VPPW);
-              const uint32_t a3 = code_pair<VB>(vc, vr[(pbase + 3) / VPPW], (pbase + 3) % VPPW);
+              const uint32_t a0 = code_pair<VB>(vc, vr[(pbase + 0) / VPPW - v * VB], (pbase + 0) % VPPW);
+              const uint32_t a1 = code_pair<VB>(vc, vr[(pbase + 1) / VPPW - v * VB], (pbase + 1) % VPPW);
+              const uint32_t a2 = code_pair<VB>(vc, vr[(pbase + 2) / VPPW - v * VB], (pbase + 2) % VPPW);
+              const uint32_t a3 = code_pair<VB>(vc, vr[(pbase + 3) / VPPW - v * VB], (pbase + 3) % VPPW);
               mma_f16(oacc[m], a0, a1, a2, a3, b0, b1);
             }
           }
