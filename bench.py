@@ -427,6 +427,103 @@ def run_ours(args, rank, world, local):
         pg.destroy_process_group()
 
 
+OTHER_WORKLOADS = {
+    # name: cache shape, mode and bits, overlay, context, activation dtype
+    "turboquant_k4v2": dict(batch=32, n_kv_heads=8, n_q_heads=32, head_dim=128, context=16384, act_dtype="f16",
+                            mode="turboquant", k_bits=4, v_bits=2),
+    "turboquant_k4v4": dict(batch=32, n_kv_heads=8, n_q_heads=32, head_dim=128, context=16384, act_dtype="f16",
+                            mode="turboquant", k_bits=4, v_bits=4),
+    "kvsink": dict(batch=4, n_kv_heads=8, n_q_heads=32, head_dim=128, context=131072, act_dtype="f16",
+                   mode="kivi", k_bits=2, v_bits=2, n_dyn_sinks=5),
+    "ring_int8": dict(batch=64, n_kv_heads=8, n_q_heads=8, head_dim=64, context=4100, act_dtype="f16",
+                      mode="kivi", k_bits=8, v_bits=8, n_sink=4, evict_window=4096, rope_base=10000.0, layers=12),
+    "ring_int4": dict(batch=64, n_kv_heads=8, n_q_heads=8, head_dim=64, context=4100, act_dtype="f16",
+                      mode="kivi", k_bits=4, v_bits=4, n_sink=4, evict_window=4096, rope_base=10000.0, layers=12),
+}
+
+
+def run_workload(args):
+    """One of the other workloads of the method on one GPU: prefill-quantise
+    the context (tokens/s), then time steps of one append (with eviction for
+    the ring) and one decode of one layer. Inputs are N(0, 1) drawn on the
+    device (timing does not depend on the values). Prints one JSON line."""
+    import torch
+    from bit_kv_cache_append_gb300 import binding
+    w = OTHER_WORKLOADS[args.workload]
+    dev = torch.device("cuda", 0)
+    dt = torch.float16 if w["act_dtype"] == "f16" else torch.bfloat16
+    B, H, Hq, D, L = w["batch"], w["n_kv_heads"], w["n_q_heads"], w["head_dim"], w["context"]
+    n_total = args.warmup + args.steps + 2
+    ring = w.get("evict_window", 0) > 0
+    cfg = dict(n_layers=1, batch=B, n_kv_heads=H, n_q_heads=Hq, head_dim=D,
+               max_tokens=(w["evict_window"] + 64 if ring else L + n_total + 64), mode=w["mode"],
+               k_bits=w["k_bits"], v_bits=w["v_bits"], n_sink=w.get("n_sink", 0), window=0,
+               evict_window=w.get("evict_window", 0), n_dyn_sinks=w.get("n_dyn_sinks", 0), act_dtype=w["act_dtype"],
+               rope_base=w.get("rope_base", 0.0), rope_max_pos=(L + n_total + 64 if w.get("rope_base") else 0))
+    cache = binding.KVCache(device=dev, **cfg)
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    k = torch.randn((B, H, L, D), generator=g, device=dev).to(dt)
+    v = torch.randn((B, H, L, D), generator=g, device=dev).to(dt)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    cache.prefill_quantize(0, k, v)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prefill_ms = e0.elapsed_time(e1)
+    del k, v
+    if ring:
+        cache.evict(0)
+    nk = torch.randn((n_total, B, H, 1, D), generator=g, device=dev).to(dt)
+    nv = torch.randn((n_total, B, H, 1, D), generator=g, device=dev).to(dt)
+    q = torch.randn((B, Hq, D), generator=g, device=dev).to(dt)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+
+    def step(i):
+        cache.append(0, nk[i], nv[i])
+        if ring:
+            cache.evict(0)
+        cache.decode_attn(0, q, out=out)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    stats0 = cache.stats(0)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_, b_ in kev:
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        cache.set_timing_events(*kev[i])
+        step(args.warmup + i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    cache.set_timing_events(None, None)
+    cache.check_device_error()
+    stats1 = cache.stats(0)
+    ms_step = t0.elapsed_time(t1) / args.steps
+    dec_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in kev)
+    wb = dict(batch=B, n_q_heads=Hq, head_dim=D)
+    dec_bytes = (algorithmic_bytes(stats0, wb) + algorithmic_bytes(stats1, wb)) / 2
+    peak, peak_kind = measured_peaks()
+    layers = w.get("layers", 1)
+    line = {"workload": args.workload, "config": w, "data": "synthetic N(0,1) on the device",
+            "prefill_tokens": B * L, "prefill_ms": round(prefill_ms, 3),
+            "prefill_tokens_per_s": round(B * L / (prefill_ms / 1e3), 1),
+            "steps": args.steps, "warmup": args.warmup, "us_per_step": round(ms_step * 1e3, 2),
+            "decode_us": round(dec_ms * 1e3, 2), "decode_bytes": int(dec_bytes),
+            "decode_gbs": round(dec_bytes / (dec_ms / 1e3) / 1e9, 1),
+            "decode_frac_of_peak": round(dec_bytes / (dec_ms / 1e3) / 1e9 / peak, 4), "peak_kind": peak_kind,
+            "tokens_per_s": round(B / (ms_step / 1e3 * layers), 1),
+            "tokens_per_s_note": f"B / (per-layer step x {layers} layers)" if layers > 1 else "B / step"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -439,11 +536,15 @@ def main():
                     help="time the steps only (no e2e, copy or CPU legs); prints a short line")
     ap.add_argument("--cpu-repeats", type=int, default=6,
                     help="decodes of one oracle sequence (8 KV-head units each) in the CPU sample")
+    ap.add_argument("--workload", choices=["llama8b"] + sorted(OTHER_WORKLOADS), default="llama8b",
+                    help="llama8b is the benchmark line; the others print their own measurement line")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.workload != "llama8b":
+        run_workload(args)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local)
