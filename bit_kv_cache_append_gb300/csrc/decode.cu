@@ -1,5 +1,6 @@
-// TurboQuant split kernel, the merge kernel (exact pools of each unit and the
-// log-sum-exp merge of the partials) and the decode dispatch.
+// The merge kernel (exact pools of each unit and the log-sum-exp merge of
+// the partials) and the decode dispatch; the split kernels (KIVI and
+// TurboQuant) are in decode_kivi.cuh.
 #include "decode_common.cuh"
 
 namespace kvq {
@@ -9,133 +10,9 @@ cudaError_t launch_kivi_d128(DecodeArgs& a, cudaStream_t s, int sm_count);
 
 namespace {
 
-// Walsh-Hadamard butterflies (stage length 1, 2, ..., D/2) over a vector held
-// as lane l -> elements i*32 + l.
-template <int D>
-__device__ __forceinline__ void warp_fwht(float (&y)[D / 32]) {
-  constexpr int NS = D / 32;
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int len = 1; len < 32; len <<= 1) {
-#pragma unroll
-    for (int i = 0; i < NS; ++i) {
-      const float o = __shfl_xor_sync(0xffffffffu, y[i], len);
-      y[i] = (lane & len) ? o - y[i] : y[i] + o;
-    }
-  }
-#pragma unroll
-  for (int sl = 1; sl < NS; sl <<= 1) {
-#pragma unroll
-    for (int i = 0; i < NS; ++i) {
-      if ((i & sl) == 0) {
-        const float u = y[i], v = y[i + sl];
-        y[i] = u + v;
-        y[i + sl] = u - v;
-      }
-    }
-  }
-}
-
-// TurboQuant decode in the rotated domain (Foundry "TurboQuant KV Cache
-// Compression - Spec", "Optimization: Fused dequant-dot"): the query is
-// rotated once (R q, R = H D / sqrt(d)), dotted with n_k (2 c[code] - 1) per
-// coordinate, and the values are accumulated as n_v (2 c[code] - 1) in the
-// rotated domain; the merge kernel rotates the output back once.
-// One warp per token in turn over the partition's tokens.
-template <int D>
-__global__ void __launch_bounds__(128) decode_tq_kernel(DecodeArgs a) {
-  constexpr int NS = D / 32, NW = 4;
-  __shared__ float red[NW * kMaxGqa * (D + 2)];
-  __shared__ float ck[16], cv[16];
-  const Geometry& G = a.geo;
-  pdl_launch_dependents();
-  const int split = static_cast<int>(blockIdx.x), h = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = G.gqa;
-  if (threadIdx.x < 16) {
-    const int nk = 1 << G.kb, nv = 1 << G.vb;
-    ck[threadIdx.x] = threadIdx.x < nk ? 2.0f * a.tab.cb_k[nk - 1 + threadIdx.x] - 1.0f : 0.0f;
-    cv[threadIdx.x] = threadIdx.x < nv ? 2.0f * a.tab.cb_v[nv - 1 + threadIdx.x] - 1.0f : 0.0f;
-  }
-  __syncthreads();
-  const float rsq = static_cast<float>(1.0 / sqrt(static_cast<double>(D)));
-  float qr[kMaxGqa][NS];
-#pragma unroll
-  for (int j = 0; j < kMaxGqa; ++j) {
-#pragma unroll
-    for (int i = 0; i < NS; ++i)
-      qr[j][i] = (j < gq) ? query_value(a, b, h * gq + j, i * 32 + lane) * a.tab.signs[i * 32 + lane] : 0.0f;
-    warp_fwht<D>(qr[j]);
-#pragma unroll
-    for (int i = 0; i < NS; ++i) qr[j][i] *= rsq;
-  }
-  float m[kMaxGqa], l[kMaxGqa], o[kMaxGqa][NS];
-#pragma unroll
-  for (int j = 0; j < kMaxGqa; ++j) {
-    m[j] = -INFINITY;
-    l[j] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < NS; ++i) o[j][i] = 0.0f;
-  }
-  const int64_t gs0 = a.g_begin + static_cast<int64_t>(split) * a.groups_per_split;
-  const int64_t gend = a.g_begin + a.n_groups;
-  const int64_t gs1 = gs0 + a.groups_per_split < gend ? gs0 + a.groups_per_split : gend;
-  const int64_t t0 = gs0 * kGroup > a.qlo ? gs0 * kGroup : a.qlo;
-  const int64_t t1 = gs1 * kGroup < a.F ? gs1 * kGroup : a.F;
-  const int bh = b * G.H + h;
-  const int kmask = (1 << G.kb) - 1, vmask = (1 << G.vb) - 1;
-  for (int64_t p = t0 + warp; p < t1; p += NW) {
-    const int slot = static_cast<int>((p / kGroup) % G.n_slots), r = static_cast<int>(p % kGroup);
-    const uint8_t* chunk = a.lay.chunks + (static_cast<size_t>(bh) * G.n_slots + slot) * G.chunk.bytes;
-    const uint8_t* krow = chunk + G.chunk.kc_off + r * (D * G.kb / 8);
-    const uint8_t* vrow = chunk + G.chunk.vc_off + r * (D * G.vb / 8);
-    const float kn = reinterpret_cast<const float*>(chunk + G.chunk.kmeta_off)[r];
-    const float vn = reinterpret_cast<const float*>(chunk + G.chunk.vmeta_off)[r];
-    float ky[NS], vy[NS];
-#pragma unroll
-    for (int i = 0; i < NS; ++i) {
-      const int c = i * 32 + lane;
-      const int kc = (krow[c * G.kb / 8] >> ((c % (8 / G.kb)) * G.kb)) & kmask;
-      const int vc = (vrow[c * G.vb / 8] >> ((c % (8 / G.vb)) * G.vb)) & vmask;
-      ky[i] = kn * ck[kc];
-      vy[i] = vn * cv[vc];
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxGqa; ++j) {
-      if (j >= gq) break;
-      float s = 0.0f;
-#pragma unroll
-      for (int i = 0; i < NS; ++i) s = fmaf(qr[j][i], ky[i], s);
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      const float mn = fmaxf(m[j], s);
-      const float al = exp2f(m[j] - mn);
-      const float pp = exp2f(s - mn);
-      l[j] = l[j] * al + pp;
-#pragma unroll
-      for (int i = 0; i < NS; ++i) o[j][i] = fmaf(o[j][i], al, pp * vy[i]);
-      m[j] = mn;
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < kMaxGqa; ++j) {
-    if (j >= gq) break;
-    float* rj = red + (warp * kMaxGqa + j) * (D + 2);
-#pragma unroll
-    for (int i = 0; i < NS; ++i) rj[i * 32 + lane] = o[j][i];
-    if (lane == 0) {
-      rj[D] = m[j];
-      rj[D + 1] = l[j];
-    }
-  }
-  __syncthreads();
-  write_partial<D, NW>(a, red, b, h, split);
-}
-
-// Number of partial slots of unit u: TurboQuant partitions, or the stream-K
-// CTAs whose item ranges meet the unit's items.
+// Number of partial slots of unit u: the stream-K CTAs whose item ranges
+// meet the unit's items.
 __device__ __forceinline__ int slots_of_unit(const DecodeArgs& a, int64_t u) {
-  if (a.geo.mode_tq) return a.n_splits;
   if (a.work <= 0 || a.n_groups <= 0) return 0;
   const int64_t first = u * a.n_groups, last = first + a.n_groups - 1;
   const int c0 = static_cast<int>(((first + 1) * a.n_ctas - 1) / a.work);
@@ -268,17 +145,7 @@ cudaError_t launch_decode(DecodeArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEv
   const Geometry& G = a.geo;
   cudaError_t e;
   if (ev0) cudaEventRecord(ev0, s);
-  if (!G.mode_tq) {
-    e = (G.D == 128) ? launch_kivi_d128(a, s, sm_count) : launch_kivi_d64(a, s, sm_count);
-  } else {
-    e = cudaSuccess;
-    if (a.n_splits > 0) {
-      dim3 grid(a.n_splits, G.H, G.B);
-      if (G.D == 128) decode_tq_kernel<128><<<grid, 128, 0, s>>>(a);
-      else decode_tq_kernel<64><<<grid, 128, 0, s>>>(a);
-      e = cudaGetLastError();
-    }
-  }
+  e = (G.D == 128) ? launch_kivi_d128(a, s, sm_count) : launch_kivi_d64(a, s, sm_count);
   if (e != cudaSuccess) return e;
   const bool split_ran = a.work > 0;
   if (split_ran) ++*launches;

@@ -206,6 +206,33 @@ __device__ __forceinline__ void write_partial(const DecodeArgs& a, const float* 
   }
 }
 
+// Walsh-Hadamard butterflies (stage length 1, 2, ..., D/2) over a vector held
+// as lane l -> elements i*32 + l.
+template <int D>
+__device__ __forceinline__ void warp_fwht(float (&y)[D / 32]) {
+  constexpr int NS = D / 32;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int len = 1; len < 32; len <<= 1) {
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, y[i], len);
+      y[i] = (lane & len) ? o - y[i] : y[i] + o;
+    }
+  }
+#pragma unroll
+  for (int sl = 1; sl < NS; sl <<= 1) {
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      if ((i & sl) == 0) {
+        const float u = y[i], v = y[i + sl];
+        y[i] = u + v;
+        y[i + sl] = u - v;
+      }
+    }
+  }
+}
+
 // Bounded wait that also gives up when another warp of the CTA has given up.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;

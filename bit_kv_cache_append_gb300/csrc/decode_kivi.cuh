@@ -143,13 +143,15 @@ constexpr float kLazyRescale = KVQ_LAZY_RESCALE;
 #define KVQ_DECODE_MIN_CTAS (8 / KVQ_DECODE_PAIRS)
 #endif
 
-template <int D, int KB, int VB>
+template <int D, int KB, int VB, bool TQ = false>
 struct KiviTile {
+  // chunk layout (kvq_layout.h): KIVI codes and meta, or TurboQuant
+  // row-major codes with one f32 norm per token
   static constexpr int KC = 32 * D * KB / 8;
   static constexpr int KMETA = KC;
-  static constexpr int VC = KMETA + 4 * D;
+  static constexpr int VC = KMETA + (TQ ? 4 * 32 : 4 * D);
   static constexpr int VMETA = VC + 32 * D * VB / 8;
-  static constexpr int CHUNK = VMETA + 4 * D;
+  static constexpr int CHUNK = VMETA + (TQ ? 4 * 32 : 4 * D);
   static constexpr int NP = KVQ_DECODE_PAIRS;           // warp pairs per CTA
 #ifndef KVQ_DECODE_STAGES
   static constexpr int NST = 3;                          // bulk-copy stages per pair (3 measured best)
@@ -157,16 +159,32 @@ struct KiviTile {
   static constexpr int NST = KVQ_DECODE_STAGES;
 #endif
   static constexpr int PBUF = 32 * 16 + 16;              // weights (16 B per lane) + 4 rescale factors
-  // shared memory: stages | weight buffers | query operand | red | barriers | abort flag
+  // TurboQuant codebook tables: code pair -> f16x2 of the two values
+  // 2 c[code] - 1, NLUT interleaved copies (lane & 7 picks one) against
+  // bank conflicts
+  static constexpr int NLUT = 8;
+  static constexpr int LUTK = TQ ? (1 << (2 * KB)) * NLUT * 4 : 0;
+  static constexpr int LUTV = TQ ? (1 << (2 * VB)) * NLUT * 4 : 0;
+  // shared memory: stages | weight buffers | query operand | query scratch |
+  // tables | red | barriers | abort flag
   static constexpr int OFF_PBUF = NP * NST * CHUNK;
   static constexpr int OFF_Q = OFF_PBUF + NP * 2 * PBUF;  // [D/16 k-steps][32 lanes] x 16 B
-  static constexpr int OFF_RED = OFF_Q + (D / 16) * 32 * 16;
+  static constexpr int OFF_QF = OFF_Q + (D / 16) * 32 * 16;  // TurboQuant: rotated queries [kMaxGqa][D] f32
+  static constexpr int OFF_LUT = OFF_QF + (TQ ? kMaxGqa * D * 4 : 0);
+  static constexpr int OFF_RED = OFF_LUT + LUTK + LUTV;
   static constexpr int RED_FLOATS = NP * kMaxGqa * (D + 2);  // one merged state per pair
   static constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
   static constexpr int NBAR = NP * (NST + 4);             // full[NST], pfull[2], pempty[2]
   static constexpr int OFF_ABORT = OFF_BAR + NBAR * 8;
   static constexpr size_t smem_bytes() { return OFF_ABORT + 16; }
 };
+
+// TurboQuant: the codebook table entry of a code pair (index = low code |
+// high code << BITS), in copy `cp`.
+template <int BITS>
+__device__ __forceinline__ uint32_t tq_lut(const uint32_t* lut, uint32_t idx, int cp) {
+  return lut[idx * 8 + cp];
+}
 
 // CTA that owns flattened item i under the equal split of `work` items into
 // `n` ranges [floor(c work / n), floor((c+1) work / n)).
@@ -221,9 +239,9 @@ struct ItemCursor {
 };
 
 
-template <int D, int KB, int VB>
+template <int D, int KB, int VB, bool TQ>
 __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(DecodeArgs a) {
-  using T = KiviTile<D, KB, VB>;
+  using T = KiviTile<D, KB, VB, TQ>;
   constexpr int NP = T::NP, NST = T::NST, CHUNK = T::CHUNK;
   constexpr int S = D / 16, MV = D / 16, NVG = D / 32;
   constexpr int KW = D * KB / 32;
@@ -256,6 +274,23 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
     for (int i = 0; i < NST; ++i) mbar_init(&full_bar[i], 1);
     for (int i = 0; i < 4; ++i) mbar_init(&pfull[i], 32);
     mbar_fence_init();
+  }
+  uint32_t* lut_k = reinterpret_cast<uint32_t*>(smem + T::OFF_LUT);
+  uint32_t* lut_v = reinterpret_cast<uint32_t*>(smem + T::OFF_LUT + T::LUTK);
+  if constexpr (TQ) {  // value of code c: 2 c[c] - 1 (Foundry TurboQuant spec, "Algorithm Detail")
+    const int nk = 1 << KB, nv = 1 << VB;
+    for (int i = threadIdx.x; i < (1 << (2 * KB)) * T::NLUT; i += blockDim.x) {
+      const int e = i / T::NLUT;
+      const float lo = 2.0f * a.tab.cb_k[nk - 1 + (e & (nk - 1))] - 1.0f;
+      const float hi = 2.0f * a.tab.cb_k[nk - 1 + (e >> KB)] - 1.0f;
+      lut_k[i] = f2_to_h2(lo, hi);
+    }
+    for (int i = threadIdx.x; i < (1 << (2 * VB)) * T::NLUT; i += blockDim.x) {
+      const int e = i / T::NLUT;
+      const float lo = 2.0f * a.tab.cb_v[nv - 1 + (e & (nv - 1))] - 1.0f;
+      const float hi = 2.0f * a.tab.cb_v[nv - 1 + (e >> VB)] - 1.0f;
+      lut_v[i] = f2_to_h2(lo, hi);
+    }
   }
   __syncthreads();
 
@@ -291,7 +326,42 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
       // value on "lo" columns, zero on the others, so that
       // qa s + (qx s - f16(qx s)) is the column's folded operand
       uint4* qsm = reinterpret_cast<uint4*>(smem + T::OFF_Q);
-      {
+      if constexpr (TQ) {
+        // rotated queries R q = FWHT(signs q) / sqrt(D) (Foundry TurboQuant
+        // spec, "Optimization: Fused dequant-dot"), one QK warp per query
+        // head, then the operand in natural channel order: k-step s, lane
+        // (g, t) holds channels 16 s + 2t (+1) and 16 s + 2t + 8 (+1) of
+        // column g (query head g / 2, value or residual)
+        float* qf = reinterpret_cast<float*>(smem + T::OFF_QF);
+        constexpr int NS = D / 32;
+        const float rsq = static_cast<float>(1.0 / sqrt(static_cast<double>(D)));
+        for (int j = pair; j < kMaxGqa; j += NP) {
+          float y[NS];
+#pragma unroll
+          for (int i = 0; i < NS; ++i)
+            y[i] = (j < gq) ? query_value(a, b, h * gq + j, i * 32 + lane) * a.tab.signs[i * 32 + lane] : 0.0f;
+          warp_fwht<D>(y);
+#pragma unroll
+          for (int i = 0; i < NS; ++i) qf[j * D + i * 32 + lane] = y[i] * rsq;
+        }
+        named_barrier_sync(1, NP * 32);
+        const int jc = g >> 1;
+        const bool col_lo = g & 1;
+        for (int s = pair; s < S; s += NP) {
+          uint32_t v[4];
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            const int c0 = 16 * s + 2 * t + 8 * p;
+            const float x0 = qf[jc * D + c0], x1 = qf[jc * D + c0 + 1];
+            const uint32_t hi = f2_to_h2(x0, x1);
+            const float2 hf = h2_to_f2(hi);
+            v[2 * p] = 0u;
+            v[2 * p + 1] = col_lo ? f2_to_h2(x0 - hf.x, x1 - hf.y) : hi;
+          }
+          qsm[s * 32 + lane] = make_uint4(v[0], v[1], v[2], v[3]);
+        }
+        named_barrier_sync(1, NP * 32);  // the QK warps only
+      } else {
         const int jc = g >> 1;        // query head of this lane's B column
         const bool col_lo = g & 1;    // B column holds the residual part
         for (int s = pair; s < S; s += NP) {
@@ -328,13 +398,57 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           break;
         }
         const uint8_t* tile = stages + st * CHUNK;
-        uint32_t kr[KW];
-#pragma unroll
-        for (int i = 0; i < KW / 4; ++i)
-          *reinterpret_cast<uint4*>(&kr[4 * i]) = reinterpret_cast<const uint4*>(tile)[i * 32 + lane];
-
         float sc[2][4];
-        {
+        if constexpr (TQ) {
+          // scores in the rotated domain: codes row-major, token rows of RW
+          // words; the pair of channels (16 s + 2t, +1) of a row is byte t
+          // of word 2s (4-bit) or nibble t of word s (2-bit), the pair
+          // (+8, +9) the next byte / nibble t + 4; the table turns a pair
+          // into its f16x2 values; the K norm of each token scales its row
+          constexpr int RW = D * KB / 32;
+          const uint32_t* krows = reinterpret_cast<const uint32_t*>(tile);
+          const uint32_t* lk = lut_k + (lane & 7);
+          float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            uint32_t w0[RW], w1[RW];  // token rows 16 mt + g and 16 mt + g + 8
+#pragma unroll
+            for (int i = 0; i < RW / 4; ++i) {
+              *reinterpret_cast<uint4*>(&w0[4 * i]) = reinterpret_cast<const uint4*>(krows + (16 * mt + g) * RW)[i];
+              *reinterpret_cast<uint4*>(&w1[4 * i]) = reinterpret_cast<const uint4*>(krows + (16 * mt + g + 8) * RW)[i];
+            }
+#pragma unroll
+            for (int s = 0; s < S; ++s) {
+              const uint4 q4 = qsm[s * 32 + lane];
+              uint32_t i00, i10, i01, i11;  // pair index of (row 0 / 1, channel pair +0 / +8)
+              if (KB == 4) {
+                i00 = (w0[2 * s] >> (8 * t)) & 0xFFu;
+                i10 = (w1[2 * s] >> (8 * t)) & 0xFFu;
+                i01 = (w0[2 * s + 1] >> (8 * t)) & 0xFFu;
+                i11 = (w1[2 * s + 1] >> (8 * t)) & 0xFFu;
+              } else {
+                i00 = (w0[s] >> (4 * t)) & 0xFu;
+                i10 = (w1[s] >> (4 * t)) & 0xFu;
+                i01 = (w0[s] >> (4 * t + 16)) & 0xFu;
+                i11 = (w1[s] >> (4 * t + 16)) & 0xFu;
+              }
+              mma_f16(acc[mt], lk[i00 * 8], lk[i10 * 8], lk[i01 * 8], lk[i11 * 8], q4.y, q4.w);
+            }
+          }
+          const float* kn = reinterpret_cast<const float*>(tile + T::KMETA);
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            const float n0 = kn[16 * mt + g], n1 = kn[16 * mt + g + 8];
+            sc[mt][0] = acc[mt][0] * n0;
+            sc[mt][1] = acc[mt][1] * n0;
+            sc[mt][2] = acc[mt][2] * n1;
+            sc[mt][3] = acc[mt][3] * n1;
+          }
+        } else {
+          uint32_t kr[KW];
+#pragma unroll
+          for (int i = 0; i < KW / 4; ++i)
+            *reinterpret_cast<uint4*>(&kr[4 * i]) = reinterpret_cast<const uint4*>(tile)[i * 32 + lane];
           const uint4* ks = reinterpret_cast<const uint4*>(tile + T::KMETA);
           // the zero-point operand: every row is the k-step's zero row
           const uint8_t* zrow = tile + T::KMETA + 2 * D + ((lane >> 4) & 1) * 16;
@@ -424,8 +538,13 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           for (int r = 0; r < 2; ++r) {
             const float p = fast_exp2(pr[mt][r] - mref);
             l_run += p;
-            const __half hp = __float2half_rn(p);
-            ph[mt * 2 + r] = as_u32(__halves2half2(hp, __float2half_rn(p - __half2float(hp))));
+            float w = p;
+            if constexpr (TQ) {  // the V norm of the token folded in (rows past F hold no data: weight 0)
+              const float nv = reinterpret_cast<const float*>(tile + T::VMETA)[16 * mt + g + 8 * r];
+              w = p > 0.0f ? p * nv : 0.0f;
+            }
+            const __half hp = __float2half_rn(w);
+            ph[mt * 2 + r] = as_u32(__halves2half2(hp, __float2half_rn(w - __half2float(hp))));
           }
         // hand the weights to the PV warp
         if (!warp_wait(&pempty[pb], static_cast<uint32_t>(((n_t >> 1) & 1) ^ 1), abort_flag)) {
@@ -480,6 +599,39 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
 #pragma unroll
           for (int e = 0; e < 4; ++e) zacc[e] *= al;
         }
+        if constexpr (TQ) {
+          // out^T += codes_V^T (p n_v) with one B operand for every m-tile;
+          // the A operand pairs two tokens of one channel: token rows of RWV
+          // words, channel c at word c * VB / 32, bit (c * VB) % 32
+          constexpr int RWV = D * VB / 32;
+          const uint32_t* vrows = reinterpret_cast<const uint32_t*>(tile + T::VC);
+          const uint32_t* lv = lut_v + (lane & 7);
+          uint32_t bb[2][2];
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            bb[kb][0] = movmatrix_t(ph[2 * kb]);
+            bb[kb][1] = movmatrix_t(ph[2 * kb + 1]);
+          }
+          constexpr uint32_t VM = (1u << VB) - 1u;
+#pragma unroll
+          for (int m = 0; m < MV; ++m) {
+            const int c0 = 16 * m + g, c1 = c0 + 8;
+            const int wd0 = c0 * VB / 32, bt0 = (c0 * VB) % 32, wd1 = c1 * VB / 32, bt1 = (c1 * VB) % 32;
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+              const int ta = 16 * kb + 2 * t, tb = ta + 8;  // tokens ta, ta + 1 and tb, tb + 1
+              const uint32_t* ra0 = vrows + ta * RWV;
+              const uint32_t* ra1 = ra0 + RWV;
+              const uint32_t* rb0 = vrows + tb * RWV;
+              const uint32_t* rb1 = rb0 + RWV;
+              const uint32_t x0 = ((ra0[wd0] >> bt0) & VM) | (((ra1[wd0] >> bt0) & VM) << VB);
+              const uint32_t x1 = ((ra0[wd1] >> bt1) & VM) | (((ra1[wd1] >> bt1) & VM) << VB);
+              const uint32_t x2 = ((rb0[wd0] >> bt0) & VM) | (((rb1[wd0] >> bt0) & VM) << VB);
+              const uint32_t x3 = ((rb0[wd1] >> bt1) & VM) | (((rb1[wd1] >> bt1) & VM) << VB);
+              mma_f16(oacc[m], lv[x0 * 8], lv[x1 * 8], lv[x2 * 8], lv[x3 * 8], bb[kb][0], bb[kb][1]);
+            }
+          }
+        } else {
         // V scales of this thread's four tokens (NVG f16 per token)
         uint32_t vsw[4][NVG / 2];
 #pragma unroll
@@ -544,6 +696,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
             }
           }
         }
+        }
         // this pair is done with the stage: refill it with the next chunk
         __syncwarp();
         if (pc.item >= 0) {
@@ -553,15 +706,16 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
         }
       }
       // zero sum of group v, query head t, is in lane (v, t)
-      const float zt = zacc[0] + zacc[1];
+      const float zt = TQ ? 0.0f : zacc[0] + zacc[1];
       __syncthreads();  // (1) the previous unit's partial has been written
 #pragma unroll
       for (int m = 0; m < MV; ++m) {
         const float zg = __shfl_sync(full, zt, (m >> 1) * 4 + t);
         if (t < gq) {
           float* rj = red + (pair * kMaxGqa + t) * (D + 2);
-          rj[16 * m + g] = fmaf(oacc[m][0] + oacc[m][1], CodeConsts<VB>::kCodeInv, zg);
-          rj[16 * m + g + 8] = fmaf(oacc[m][2] + oacc[m][3], CodeConsts<VB>::kCodeInv, zg);
+          const float cu = TQ ? 1.0f : CodeConsts<VB>::kCodeInv;
+          rj[16 * m + g] = fmaf(oacc[m][0] + oacc[m][1], cu, zg);
+          rj[16 * m + g + 8] = fmaf(oacc[m][2] + oacc[m][3], cu, zg);
         }
       }
     }
@@ -577,9 +731,9 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
   }
 }
 
-template <int D, int KB, int VB>
+template <int D, int KB, int VB, bool TQ>
 cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
-  using T = KiviTile<D, KB, VB>;
+  using T = KiviTile<D, KB, VB, TQ>;
   const size_t smem = T::smem_bytes();
   static int occ_of[kMaxDevices] = {};  // per device: the attribute is per device
   int dev = 0;
@@ -588,10 +742,10 @@ cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   int& occupancy = occ_of[dev];
   if (!occupancy) {
-    e = cudaFuncSetAttribute(decode_kivi_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kivi_kernel<D, KB, VB, TQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, decode_kivi_kernel<D, KB, VB>, 64 * T::NP, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, decode_kivi_kernel<D, KB, VB, TQ>, 64 * T::NP, smem);
     if (e != cudaSuccess) return e;
     if (occupancy < 1) occupancy = 1;
   }
@@ -604,15 +758,22 @@ cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
   if (n < 1) n = 1;
   a.n_ctas = static_cast<int>(n);
   if (a.work <= 0) return cudaSuccess;  // nothing quantised to read: the merge does it all
-  decode_kivi_kernel<D, KB, VB><<<a.n_ctas, 64 * T::NP, smem, s>>>(a);
+  decode_kivi_kernel<D, KB, VB, TQ><<<a.n_ctas, 64 * T::NP, smem, s>>>(a);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_kivi_d(DecodeArgs& a, cudaStream_t s, int sm_count) {
   const int kb = a.geo.kb, vb = a.geo.vb;
+  if (a.geo.mode_tq) {
 #define KVQ_CASE(K, V) \
-  if (kb == K && vb == V) return launch_kivi_instance<D, K, V>(a, s, sm_count);
+  if (kb == K && vb == V) return launch_kivi_instance<D, K, V, true>(a, s, sm_count);
+    KVQ_CASE(2, 2) KVQ_CASE(2, 4) KVQ_CASE(4, 2) KVQ_CASE(4, 4)
+#undef KVQ_CASE
+    return cudaErrorInvalidValue;
+  }
+#define KVQ_CASE(K, V) \
+  if (kb == K && vb == V) return launch_kivi_instance<D, K, V, false>(a, s, sm_count);
   KVQ_CASE(2, 2) KVQ_CASE(2, 4) KVQ_CASE(2, 8)
   KVQ_CASE(4, 2) KVQ_CASE(4, 4) KVQ_CASE(4, 8)
   KVQ_CASE(8, 2) KVQ_CASE(8, 4) KVQ_CASE(8, 8)
