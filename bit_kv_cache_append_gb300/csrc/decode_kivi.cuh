@@ -154,7 +154,9 @@ struct KiviTile {
   static constexpr int CHUNK = VMETA + (TQ ? 4 * 32 : 4 * D);
   static constexpr int NP = KVQ_DECODE_PAIRS;           // warp pairs per CTA
 #ifndef KVQ_DECODE_STAGES
-  static constexpr int NST = 3;                          // bulk-copy stages per pair (3 measured best)
+  // bulk-copy stages per pair (3 measured best; 2 where the TurboQuant
+  // K4/V4 tables and tiles would not leave room for two CTAs per SM)
+  static constexpr int NST = (TQ && KB == 4 && VB == 4) ? 2 : 3;
 #else
   static constexpr int NST = KVQ_DECODE_STAGES;
 #endif
@@ -171,7 +173,11 @@ struct KiviTile {
   static constexpr int OFF_Q = OFF_PBUF + NP * 2 * PBUF;  // [D/16 k-steps][32 lanes] x 16 B
   static constexpr int OFF_QF = OFF_Q + (D / 16) * 32 * 16;  // TurboQuant: rotated queries [kMaxGqa][D] f32
   static constexpr int OFF_LUT = OFF_QF + (TQ ? kMaxGqa * D * 4 : 0);
-  static constexpr int OFF_RED = OFF_LUT + LUTK + LUTV;
+  // TurboQuant: each PV warp's dequantised V tile, 32 token rows of D f16
+  // padded by 8 halves (conflict-free row stores and transposed ldmatrix)
+  static constexpr int VT_ROW = D + 8;
+  static constexpr int OFF_VT = OFF_LUT + LUTK + LUTV;
+  static constexpr int OFF_RED = OFF_VT + (TQ ? NP * 32 * VT_ROW * 2 : 0);
   static constexpr int RED_FLOATS = NP * kMaxGqa * (D + 2);  // one merged state per pair
   static constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
   static constexpr int NBAR = NP * (NST + 4);             // full[NST], pfull[2], pempty[2]
@@ -600,37 +606,50 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           for (int e = 0; e < 4; ++e) zacc[e] *= al;
         }
         if constexpr (TQ) {
-          // out^T += codes_V^T (p n_v) with one B operand for every m-tile;
-          // the A operand pairs two tokens of one channel: token rows of RWV
-          // words, channel c at word c * VB / 32, bit (c * VB) % 32
+          // out^T += V^T (p n_v) with one B operand for every m-tile. The V
+          // rows are dequantised into this warp's f16 tile first (lane r
+          // takes token row r; a pair of adjacent channels is one table
+          // entry), then read back transposed by ldmatrix.
           constexpr int RWV = D * VB / 32;
-          const uint32_t* vrows = reinterpret_cast<const uint32_t*>(tile + T::VC);
-          const uint32_t* lv = lut_v + (lane & 7);
+          constexpr int PPW = 16 / VB;  // channel pairs per code word
+          constexpr uint32_t PM = (1u << (2 * VB)) - 1u;
+          uint16_t* vt = reinterpret_cast<uint16_t*>(smem + T::OFF_VT) + pair * 32 * T::VT_ROW;
+          {
+            const uint32_t* row = reinterpret_cast<const uint32_t*>(tile + T::VC) + lane * RWV;
+            const uint32_t* lv = lut_v + (lane & 7);
+            uint16_t* dst = vt + lane * T::VT_ROW;
+#pragma unroll
+            for (int w4 = 0; w4 < RWV / 4; ++w4) {
+              const uint4 cw = reinterpret_cast<const uint4*>(row)[w4];
+              const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+              for (int k2 = 0; k2 < 4; ++k2) {
+                uint32_t hv[PPW];
+#pragma unroll
+                for (int j = 0; j < PPW; ++j) hv[j] = lv[((wv[k2] >> (2 * VB * j)) & PM) * 8];
+                uint4* d4 = reinterpret_cast<uint4*>(dst + ((w4 * 4 + k2) * PPW) * 2);
+#pragma unroll
+                for (int j = 0; j < PPW / 4; ++j) d4[j] = make_uint4(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3]);
+              }
+            }
+          }
+          __syncwarp();
           uint32_t bb[2][2];
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
             bb[kb][0] = movmatrix_t(ph[2 * kb]);
             bb[kb][1] = movmatrix_t(ph[2 * kb + 1]);
           }
-          constexpr uint32_t VM = (1u << VB) - 1u;
 #pragma unroll
-          for (int m = 0; m < MV; ++m) {
-            const int c0 = 16 * m + g, c1 = c0 + 8;
-            const int wd0 = c0 * VB / 32, bt0 = (c0 * VB) % 32, wd1 = c1 * VB / 32, bt1 = (c1 * VB) % 32;
+          for (int m = 0; m < MV; ++m)
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
-              const int ta = 16 * kb + 2 * t, tb = ta + 8;  // tokens ta, ta + 1 and tb, tb + 1
-              const uint32_t* ra0 = vrows + ta * RWV;
-              const uint32_t* ra1 = ra0 + RWV;
-              const uint32_t* rb0 = vrows + tb * RWV;
-              const uint32_t* rb1 = rb0 + RWV;
-              const uint32_t x0 = ((ra0[wd0] >> bt0) & VM) | (((ra1[wd0] >> bt0) & VM) << VB);
-              const uint32_t x1 = ((ra0[wd1] >> bt1) & VM) | (((ra1[wd1] >> bt1) & VM) << VB);
-              const uint32_t x2 = ((rb0[wd0] >> bt0) & VM) | (((rb1[wd0] >> bt0) & VM) << VB);
-              const uint32_t x3 = ((rb0[wd1] >> bt1) & VM) | (((rb1[wd1] >> bt1) & VM) << VB);
-              mma_f16(oacc[m], lv[x0 * 8], lv[x1 * 8], lv[x2 * 8], lv[x3 * 8], bb[kb][0], bb[kb][1]);
+              uint32_t A[4];
+              ldmatrix_x4_trans(A, vt + (16 * kb + 8 * (lane >> 4) + (lane & 7)) * T::VT_ROW + 16 * m +
+                                       8 * ((lane >> 3) & 1));
+              mma_f16(oacc[m], A[0], A[1], A[2], A[3], bb[kb][0], bb[kb][1]);
             }
-          }
+          __syncwarp();  // the tile is read before the next group overwrites it
         } else {
         // V scales of this thread's four tokens (NVG f16 per token)
         uint32_t vsw[4][NVG / 2];
