@@ -118,8 +118,10 @@ template <int D, int KB, int VB>
 __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
   constexpr int HALF = D / 2, NV = D / 32, CPR = HALF / 8;
   constexpr int LK = (1 << KB) - 1, LV = (1 << VB) - 1;
-  __shared__ float xk[32][D + 1];
-  __shared__ float xv[32][D + 1];
+  // the group's rows as activation-dtype bits (rows padded by 16 bytes so
+  // that 16-byte row stores stay aligned and column reads spread over banks)
+  __shared__ __align__(16) uint16_t xk[32][D + 8];
+  __shared__ __align__(16) uint16_t xv[32][D + 8];
   __shared__ uint8_t ck[32][D + 4];  // rows padded by a word: the packing gathers down columns
   __shared__ uint8_t cv[32][D + 4];
   __shared__ int sub[32];
@@ -172,45 +174,40 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
       vhi = *reinterpret_cast<const uint4*>(a.v + t + HALF + c0);
       if (a.tab.rope) rotate8(klo, khi, a.tab.rope + static_cast<size_t>(pos) * D, c0, bf16);
     }
-    const uint16_t* pkl = reinterpret_cast<const uint16_t*>(&klo);
-    const uint16_t* pkh = reinterpret_cast<const uint16_t*>(&khi);
-    const uint16_t* pvl = reinterpret_cast<const uint16_t*>(&vlo);
-    const uint16_t* pvh = reinterpret_cast<const uint16_t*>(&vhi);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      xk[r][c0 + i] = act_to_float(pkl[i], bf16);
-      xk[r][HALF + c0 + i] = act_to_float(pkh[i], bf16);
-      xv[r][c0 + i] = act_to_float(pvl[i], bf16);
-      xv[r][HALF + c0 + i] = act_to_float(pvh[i], bf16);
-    }
+    *reinterpret_cast<uint4*>(&xk[r][c0]) = klo;
+    *reinterpret_cast<uint4*>(&xk[r][HALF + c0]) = khi;
+    *reinterpret_cast<uint4*>(&xv[r][c0]) = vlo;
+    *reinterpret_cast<uint4*>(&xv[r][HALF + c0]) = vhi;
   }
   __syncthreads();
 
   uint8_t* chunk = a.lay.chunks + (static_cast<size_t>(bh) * G.n_slots + slot) * G.chunk.bytes;
   {  // K: channel tid over the 32 tokens
     const int c = tid;
-    float mn = xk[0][c], mx = mn;
+    float mn = act_to_float(xk[0][c], bf16), mx = mn;
 #pragma unroll 8
     for (int r = 1; r < 32; ++r) {
-      mn = fminf(mn, xk[r][c]);
-      mx = fmaxf(mx, xk[r][c]);
+      const float x = act_to_float(xk[r][c], bf16);
+      mn = fminf(mn, x);
+      mx = fmaxf(mx, x);
     }
     __half sh, zh;
     float s, z;
     quantize_slice_params(mn, mx, KB, &sh, &zh, &s, &z);
     const float rs = __frcp_rn(s);
 #pragma unroll 8
-    for (int r = 0; r < 32; ++r) ck[r][c] = static_cast<uint8_t>(quantize_code<LK>(xk[r][c], s, z, rs));
+    for (int r = 0; r < 32; ++r)
+      ck[r][c] = static_cast<uint8_t>(quantize_code<LK>(act_to_float(xk[r][c], bf16), s, z, rs));
     __half* km = reinterpret_cast<__half*>(chunk + G.chunk.kmeta_off);
     km[kmeta_pos(D, c)] = sh;
     km[D + kzero_pos(D, c)] = zh;
   }
   {  // V: token r, channel group vg (index rotated by 8 vg to spread banks)
     const int r = tid / NV, vg = tid % NV, base = 32 * vg;
-    float mn = xv[r][base + ((8 * vg) & 31)], mx = mn;
+    float mn = act_to_float(xv[r][base + ((8 * vg) & 31)], bf16), mx = mn;
 #pragma unroll 8
     for (int i = 0; i < 32; ++i) {
-      const float x = xv[r][base + ((i + 8 * vg) & 31)];
+      const float x = act_to_float(xv[r][base + ((i + 8 * vg) & 31)], bf16);
       mn = fminf(mn, x);
       mx = fmaxf(mx, x);
     }
@@ -221,7 +218,7 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
 #pragma unroll 8
     for (int i = 0; i < 32; ++i) {
       const int c = base + ((i + 8 * vg) & 31);
-      cv[r][c] = static_cast<uint8_t>(quantize_code<LV>(xv[r][c], s, z, rs));
+      cv[r][c] = static_cast<uint8_t>(quantize_code<LV>(act_to_float(xv[r][c], bf16), s, z, rs));
     }
     __half* vm = reinterpret_cast<__half*>(chunk + G.chunk.vmeta_off);
     vm[vscale_pos(NV, r, vg)] = sh;
