@@ -62,3 +62,42 @@ def test_kvsink_full_size_selection():
     heads = _sample_heads(w.batch, w.n_q_heads, 4, 2)
     o_ref, _ = oc.decode_attn(0, q, heads=heads)
     compare_attention(out.cpu().numpy(), o_ref, heads)
+
+
+def test_turboquant_full_size_sampled_sequences():
+    """TurboQuant K4/V2 at full size (batch 32, 8 KV heads, 16384 tokens,
+    AR(1) channels): the GPU holds every sequence; the oracle takes three
+    sampled sequences (the sequences are independent), whose codes and
+    norms must match bit for bit and whose attention is compared."""
+    import torch
+    from bit_kv_cache_append_gb300.binding import KVCache
+    from oracle import OracleCache
+    w = W.WORKLOADS["turboquant_k4v2"]
+    bs = [0, 13, 31]
+    kw = cache_kwargs(w, w.context + 64, seed=99)
+    gc = KVCache(**kw)
+    oc = OracleCache(oracle_config(dict(kw, batch=len(bs))))
+    k, v = W.kv_tokens(w, 31, w.context - 1)
+    gc.prefill_quantize(0, torch_act(k, "f16"), torch_act(v, "f16"))
+    oc.prefill_quantize(0, k[bs], v[bs])
+    del k, v
+    k1, v1 = W.kv_tokens(w, 31, 1, first_pos=w.context - 1)
+    gc.append(0, torch_act(k1, "f16"), torch_act(v1, "f16"))
+    oc.append(0, k1[bs], v1[bs])
+    ref = oc.export(0)
+    for name in ("k_codes", "k_norm", "v_codes", "v_norm"):
+        got = gc.export(0, name)[bs]
+        want = ref[name]
+        if name.endswith("norm"):
+            got, want = got.view(np.uint32), want.astype(np.float32).view(np.uint32)
+        assert got.shape == want.shape, (name, got.shape, want.shape)
+        bad = np.argwhere(got != want)
+        assert bad.size == 0, f"{name}: {len(bad)} mismatches, first at {bad[:5].tolist()}"
+    q = W.queries(w, 31)
+    out = gc.decode_attn(0, torch_act(q, "f16"))
+    torch.cuda.synchronize()
+    gc.check_device_error()
+    heads = [(i, hq) for i in range(len(bs)) for hq in (0, 9, 22, 31)]
+    o_ref, _ = oc.decode_attn(0, q[bs], heads=heads)
+    got = out.cpu().numpy()[bs]
+    compare_attention(got, o_ref, heads)

@@ -74,11 +74,12 @@ def test_ring_capacity_requires_eviction():
 
 # ------------------------------------------------------------------ TurboQuant
 
+@pytest.mark.parametrize("act", ["f16", "bf16"])
 @pytest.mark.parametrize("D", [128, 64])
-@pytest.mark.parametrize("kb,vb", [(4, 2), (4, 4), (2, 2)])
-def test_turboquant_codes_and_attention(kb, vb, D):
+@pytest.mark.parametrize("kb,vb", [(4, 2), (4, 4), (2, 2), (2, 4)])
+def test_turboquant_codes_and_attention(kb, vb, D, act):
     w = W.scaled(W.WORKLOADS["turboquant_k4v2"], batch=2, n_kv_heads=2, n_q_heads=8, head_dim=D,
-                 k_bits=kb, v_bits=vb)
+                 k_bits=kb, v_bits=vb, act_dtype=act)
     kw = cache_kwargs(w, 1024, seed=1234)
     gc, oc = _pair(kw)
     assert np.array_equal(gc.export(0, "tq_signs"), oc.sgn)
@@ -88,14 +89,14 @@ def test_turboquant_codes_and_attention(kb, vb, D):
         assert np.array_equal(cb[: (1 << bits) - 1], bnd), which
         assert np.array_equal(cb[(1 << bits) - 1:], cen), which
     k, v = W.kv_tokens(w, 6, 700)
-    gc.prefill_quantize(0, torch_act(k, "f16"), torch_act(v, "f16"))
+    gc.prefill_quantize(0, torch_act(k, act), torch_act(v, act))
     oc.prefill_quantize(0, k, v)
     for i in range(5):
         k, v = W.kv_tokens(w, 6, 1 + 10 * i, first_pos=700 + i)
-        gc.append(0, torch_act(k, "f16"), torch_act(v, "f16"))
+        gc.append(0, torch_act(k, act), torch_act(v, act))
         oc.append(0, k, v)
     compare_exports(gc, oc, 0)
-    _decode_both(gc, oc, 0, W.queries(w, 6), "f16")
+    _decode_both(gc, oc, 0, W.queries(w, 6), act)
 
 
 @pytest.mark.parametrize("D", [128, 64])
