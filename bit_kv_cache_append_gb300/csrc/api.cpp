@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
+#include <cstdint>
 #include <cstring>
 #include <new>
 #include <string>
@@ -402,6 +403,8 @@ kv_status decode_attn_impl(kv_cache* cache, int layer, const void* q, float* out
   kv_status st = check_layer(cache, layer);
   if (st != KV_OK) return st;
   if (!q || !out) return fail(KV_ERR_INVALID_ARG, "q/out is NULL");
+  if (reinterpret_cast<uintptr_t>(q) % 4 || reinterpret_cast<uintptr_t>(out) % 4)
+    return fail(KV_ERR_INVALID_ARG, "q and out must be 4-byte aligned");
   const Geometry& g = cache->geo;
   const LayerState& ls = cache->layers[layer];
   if (ls.L == 0) return fail(KV_ERR_STATE, "decode on an empty layer");

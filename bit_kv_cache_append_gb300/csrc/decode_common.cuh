@@ -174,6 +174,36 @@ __device__ __forceinline__ float query_value(const DecodeArgs& a, int b, int hq,
   return x * a.qscale;
 }
 
+// query_value of the channel pair (c0, c0 + 1), c0 even: one 32-bit load of
+// the pair (q must be 4-byte aligned) and, with RoPE, of its rotation
+// partner and one 16-byte load of the two table entries; the same
+// arithmetic element by element.
+__device__ __forceinline__ float2 query_pair(const DecodeArgs& a, int b, int hq, int c0) {
+  const Geometry& G = a.geo;
+  const int D = G.D, half = D / 2;
+  const uint16_t* qrow = a.q + (static_cast<size_t>(b) * G.Hq + hq) * D;
+  const uint32_t xw = *reinterpret_cast<const uint32_t*>(qrow + c0);
+  float x0 = act_to_float(static_cast<uint16_t>(xw & 0xffffu), G.act_bf16);
+  float x1 = act_to_float(static_cast<uint16_t>(xw >> 16), G.act_bf16);
+  if (a.tab.rope) {
+    const bool lo = c0 < half;
+    const int i = lo ? c0 : c0 - half;
+    const uint32_t yw = *reinterpret_cast<const uint32_t*>(qrow + (lo ? c0 + half : c0 - half));
+    const float y0 = act_to_float(static_cast<uint16_t>(yw & 0xffffu), G.act_bf16);
+    const float y1 = act_to_float(static_cast<uint16_t>(yw >> 16), G.act_bf16);
+    const float4 tr = *reinterpret_cast<const float4*>(a.tab.rope + static_cast<size_t>(a.L - 1) * D + 2 * i);
+    float ra, rb;
+    if (lo) {
+      rope_pair(x0, y0, tr.x, tr.y, &ra, &rb), x0 = ra;
+      rope_pair(x1, y1, tr.z, tr.w, &ra, &rb), x1 = ra;
+    } else {
+      rope_pair(y0, x0, tr.x, tr.y, &ra, &rb), x0 = rb;
+      rope_pair(y1, x1, tr.z, tr.w, &ra, &rb), x1 = rb;
+    }
+  }
+  return make_float2(x0 * a.qscale, x1 * a.qscale);
+}
+
 // Per-warp online-softmax states of one CTA merged through shared memory and
 // written as partial `slot` of each of the G query heads: m (log2 units), l,
 // and the unnormalised output o[D]. NW warps do the writing; `red` holds
@@ -388,12 +418,8 @@ __device__ bool exact_states_tc(const DecodeArgs& a, int b, int h, float* red, u
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
       const int c0 = 16 * s + 2 * t + 8 * p;
-      float x0 = 0.0f, x1 = 0.0f;
-      if (jc < gq) {
-        x0 = query_value(a, b, h * gq + jc, c0);
-        x1 = query_value(a, b, h * gq + jc, c0 + 1);
-      }
-      qb[s][p] = split_act2<BF>(x0, x1, col_lo);
+      const float2 x = jc < gq ? query_pair(a, b, h * gq + jc, c0) : make_float2(0.0f, 0.0f);
+      qb[s][p] = split_act2<BF>(x.x, x.y, col_lo);
     }
   float m_run = -INFINITY, l_run = 0.0f;  // of query head t (this lane's C columns)
   float oacc[MV][4];

@@ -375,11 +375,8 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             const int c0 = t * (D / 4) + 4 * s + 2 * p;
-            float x0 = 0.0f, x1 = 0.0f;
-            if (jc < gq) {
-              x0 = query_value(a, b, h * gq + jc, c0);
-              x1 = query_value(a, b, h * gq + jc, c0 + 1);
-            }
+            const float2 x = jc < gq ? query_pair(a, b, h * gq + jc, c0) : make_float2(0.0f, 0.0f);
+            const float x0 = x.x, x1 = x.y;
             const uint32_t hi = f2_to_h2(x0, x1);
             const float2 hf = h2_to_f2(hi);
             v[2 * p] = col_lo ? hi : 0u;

@@ -171,8 +171,9 @@ kv_status kv_evict(kv_cache* cache, int layer, int64_t* evicted_begin, int64_t* 
 /*
  * Decode attention for one layer (P2 "Optimization: Fused dequant-dot";
  * P3 "Summary": sinks and the recent window read exact, the rest quantised).
- * q: device [B, Hq, D] act_dtype (un-rotated when the cache applies RoPE;
- * it is rotated at position L-1). out: device [B, Hq, D] fp32 =
+ * q: device [B, Hq, D] act_dtype, 4-byte aligned (un-rotated when the cache
+ * applies RoPE; it is rotated at position L-1). out: device [B, Hq, D] fp32
+ * (4-byte aligned) =
  * softmax(q K^T / sqrt(D)) V over every retained position; query head j
  * reads KV head j / (Hq / Hkv). lse_or_null: device [B, Hq] fp32 natural-log
  * softmax denominator, or NULL. Split-KV: the quantised segment is cut into
