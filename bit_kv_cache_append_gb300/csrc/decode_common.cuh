@@ -86,6 +86,27 @@ __device__ __forceinline__ void bulk_g2s_if(bool pred, void* dst, const void* sr
       : "memory");
 }
 
+// The transaction count of a coming copy armed on `bar` (with this thread's
+// arrival), and a 1-D bulk copy completing on `bar`: each done only where
+// `pred` holds (predicated instructions, no divergence).
+__device__ __forceinline__ void expect_tx_if(bool pred, uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\t"
+      "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes), "r"(static_cast<int>(pred))
+      : "memory");
+}
+__device__ __forceinline__ void copy_g2s_if(bool pred, void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "r"(static_cast<int>(pred))
+      : "memory");
+}
+
 // D += A B with A 16x16 f16 (row), B 16x8 f16 (col), D 16x8 f32.
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {

@@ -153,14 +153,21 @@ struct KiviTile {
   static constexpr int VMETA = VC + 32 * D * VB / 8;
   static constexpr int CHUNK = VMETA + (TQ ? 4 * 32 : 4 * D);
   static constexpr int NP = KVQ_DECODE_PAIRS;           // warp pairs per CTA
+  // groups per stage: a pair takes runs of GPB consecutive groups, so the
+  // waits, hand-off and rescale decision are paid once per run (KIVI chunks
+  // up to 6 KB); one for TurboQuant, whose tables and tiles leave less
+  // shared memory, and for larger chunks
+  static constexpr int GPB = (TQ || CHUNK > 6144) ? 1 : 2;
 #ifndef KVQ_DECODE_STAGES
-  // bulk-copy stages per pair (3 measured best; 2 where the TurboQuant
-  // K4/V4 tables and tiles would not leave room for two CTAs per SM)
-  static constexpr int NST = (TQ && KB == 4 && VB == 4) ? 2 : 3;
+  // bulk-copy stages per pair: 2 runs of 2 groups; else 3 groups, or 2
+  // where the TurboQuant K4/V4 tables and tiles would not leave room for two
+  // CTAs per SM
+  static constexpr int NST = GPB == 2 ? 2 : ((TQ && KB == 4 && VB == 4) ? 2 : 3);
 #else
   static constexpr int NST = KVQ_DECODE_STAGES;
 #endif
-  static constexpr int PBUF = 32 * 16 + 16;              // weights (16 B per lane) + 4 rescale factors
+  static constexpr int STAGE = GPB * CHUNK;
+  static constexpr int PBUF = GPB * 32 * 16 + 16;        // weights (16 B per lane per group) + 4 rescale factors
   // TurboQuant codebook tables: code pair -> f16x2 of the two values
   // 2 c[code] - 1, NLUT interleaved copies (lane & 7 picks one) against
   // bank conflicts
@@ -169,7 +176,7 @@ struct KiviTile {
   static constexpr int LUTV = TQ ? (1 << (2 * VB)) * NLUT * 4 : 0;
   // shared memory: stages | weight buffers | query operand | query scratch |
   // tables | red | barriers | abort flag
-  static constexpr int OFF_PBUF = NP * NST * CHUNK;
+  static constexpr int OFF_PBUF = NP * NST * STAGE;
   static constexpr int OFF_Q = OFF_PBUF + NP * 2 * PBUF;  // [D/16 k-steps][32 lanes] x 16 B
   static constexpr int OFF_QF = OFF_Q + (D / 16) * 32 * 16;  // TurboQuant: rotated queries [kMaxGqa][D] f32
   static constexpr int OFF_LUT = OFF_QF + (TQ ? kMaxGqa * D * 4 : 0);
@@ -198,29 +205,36 @@ __device__ __forceinline__ int owner_cta(int64_t i, int64_t work, int n) {
   return static_cast<int>(((i + 1) * n - 1) / work);
 }
 
-// Walks the items of pair p inside its CTA's range [i0, i1): per unit (run of
-// ng items), the unit's items s + p, s + p + NP, ... where s is the first
-// item of the unit inside the range. The group index and its ring slot
-// advance by additions; divisions happen only when the walk enters a new unit.
-template <int NP>
-struct ItemCursor {
-  int64_t item;       // current item (-1: exhausted)
-  int64_t seg_end;    // end of the current unit inside the range
-  int64_t grp;        // absolute group index of `item`
-  int slot;           // grp mod n_slots
-  const uint8_t* ptr; // chunk of `item`
+// Walks the runs of pair p inside its CTA's range [i0, i1): per unit (run of
+// ng items), the unit's items from s on (s = the first item of the unit
+// inside the range) are cut into runs of GPB consecutive items; the pair
+// takes runs p, p + NP, ... The group index and its ring slot advance by
+// additions; divisions happen only when the walk enters a new unit. The
+// chunks of a run are consecutive ring slots (wrapping to the unit's first
+// slot).
+template <int NP, int GPB>
+struct RunCursor {
+  int64_t item;        // first item of the current run (-1: exhausted)
+  int64_t seg_end;     // end of the current unit inside the range
+  int64_t grp;         // absolute group index of `item`
+  int slot;            // grp mod n_slots
+  int cnt;             // items in the run (1 .. GPB)
+  const uint8_t* base; // the unit's first chunk
+  const uint8_t* ptr;  // chunk of `item`
 
   __device__ __forceinline__ void enter(int64_t s, int64_t i1, int64_t ng, int w, int64_t g_begin, int n_slots,
                                         const uint8_t* chunks, int chunk_bytes) {
     while (s < i1) {
       const int64_t u = s / ng;
       const int64_t e = (u + 1) * ng < i1 ? (u + 1) * ng : i1;
-      if (s + w < e) {
-        item = s + w;
+      if (s + GPB * w < e) {
+        item = s + GPB * w;
         seg_end = e;
         grp = g_begin + (item - u * ng);
         slot = static_cast<int>(grp % n_slots);
-        ptr = chunks + (static_cast<size_t>(u) * n_slots + slot) * chunk_bytes;
+        base = chunks + static_cast<size_t>(u) * n_slots * chunk_bytes;
+        ptr = base + static_cast<size_t>(slot) * chunk_bytes;
+        cnt = (e - item) < GPB ? static_cast<int>(e - item) : GPB;
         return;
       }
       s = e;
@@ -229,21 +243,22 @@ struct ItemCursor {
   }
   __device__ __forceinline__ void advance(int64_t i1, int64_t ng, int w, int64_t g_begin, int n_slots,
                                           const uint8_t* chunks, int chunk_bytes) {
-    if (item + NP < seg_end) {
-      item += NP;
-      grp += NP;
-      slot += NP;
-      ptr += NP * chunk_bytes;
-      while (slot >= n_slots) {
-        slot -= n_slots;
-        ptr -= static_cast<size_t>(n_slots) * chunk_bytes;
-      }
+    if (item + GPB * NP < seg_end) {
+      item += GPB * NP;
+      grp += GPB * NP;
+      slot += GPB * NP;
+      while (slot >= n_slots) slot -= n_slots;
+      ptr = base + static_cast<size_t>(slot) * chunk_bytes;
+      cnt = (seg_end - item) < GPB ? static_cast<int>(seg_end - item) : GPB;
     } else {
       enter(seg_end, i1, ng, w, g_begin, n_slots, chunks, chunk_bytes);
     }
   }
+  // chunk q (< cnt) of the run
+  __device__ __forceinline__ const uint8_t* chunk(int q, int n_slots, int chunk_bytes) const {
+    return q == 0 ? ptr : base + static_cast<size_t>(slot + q < n_slots ? slot + q : slot + q - n_slots) * chunk_bytes;
+  }
 };
-
 
 template <int D, int KB, int VB, bool TQ>
 __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(DecodeArgs a) {
@@ -269,7 +284,8 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
   const int64_t i0 = cta * work / a.n_ctas, i1 = (cta + 1) * work / a.n_ctas;
   const int n_slots = G.n_slots;
 
-  uint8_t* stages = smem + pair * NST * CHUNK;
+  constexpr int GPB = T::GPB, STAGE = T::STAGE;
+  uint8_t* stages = smem + pair * NST * STAGE;
   uint8_t* pbuf = smem + T::OFF_PBUF + pair * 2 * T::PBUF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR) + pair * (NST + 4);
   uint64_t* full_bar = bars;            // [NST] chunk landed (one arrival: the copy's issuer)
@@ -301,18 +317,23 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
   __syncthreads();
 
   // producer state (the PV warp: every lane keeps the same cursor, lane 0
-  // issues): the next item whose chunk is to be fetched
-  ItemCursor<NP> pc;
+  // issues): the next run whose chunks are to be fetched
+  RunCursor<NP, GPB> pc{};
   int issued = 0;
+  auto fetch = [&](int st) {  // the cursor's run into stage st, then advance
+    expect_tx_if(lane == 0, &full_bar[st], static_cast<uint32_t>(pc.cnt * CHUNK));
+#pragma unroll
+    for (int q = 0; q < GPB; ++q)
+      if (q < pc.cnt) copy_g2s_if(lane == 0, stages + st * STAGE + q * CHUNK, pc.chunk(q, n_slots, CHUNK), CHUNK,
+                                  &full_bar[st]);
+    pc.advance(i1, ng, pair, a.g_begin, n_slots, a.lay.chunks, CHUNK);
+    ++issued;
+  };
   if (is_pv) {
     pc.enter(i0, i1, ng, pair, a.g_begin, n_slots, a.lay.chunks, CHUNK);
-    for (int i = 0; i < NST && pc.item >= 0; ++i) {
-      bulk_g2s_if(lane == 0, stages + i * CHUNK, pc.ptr, CHUNK, &full_bar[i]);
-      pc.advance(i1, ng, pair, a.g_begin, n_slots, a.lay.chunks, CHUNK);
-      ++issued;
-    }
+    for (int i = 0; i < NST && pc.item >= 0; ++i) fetch(i);
   }
-  int n_t = 0;  // groups this pair has processed (stage and buffer phases)
+  int n_t = 0;  // runs this pair has processed (stage and buffer phases)
   bool failed = false;
 
   int64_t seg = i0;
@@ -320,9 +341,10 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
     const int64_t unit = seg / ng, ubase = unit * ng;
     const int64_t seg_e = ubase + ng < i1 ? ubase + ng : i1;
     const int b = static_cast<int>(unit / G.H), h = static_cast<int>(unit % G.H);
-    // this pair's items of the segment: my0, my0 + NP, ... (n_my of them)
-    const int64_t my0 = seg + pair;
-    const int n_my = my0 < seg_e ? static_cast<int>((seg_e - my0 + NP - 1) / NP) : 0;
+    // this pair's runs of the segment: run j starts at item my0 + j GPB NP
+    // and holds min(GPB, seg_e - start) items (n_my runs)
+    const int64_t my0 = seg + GPB * pair;
+    const int n_my = my0 < seg_e ? static_cast<int>((seg_e - my0 + GPB * NP - 1) / (GPB * NP)) : 0;
 
     if (!is_pv) {
       // ------------------------------------------------------------ QK warp
@@ -387,21 +409,11 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
         named_barrier_sync(1, NP * 32);  // the QK warps only
       }
       float m_run = -INFINITY, l_run = 0.0f;
-      // the unit's first and last groups are the only partial ones
-      const int k_lo = (my0 == ubase) ? 0 : -1;
-      const int k_hi = (seg_e == ubase + ng && n_my > 0 && my0 + static_cast<int64_t>(n_my - 1) * NP == ubase + ng - 1)
-                           ? n_my - 1 : -1;
       const bool n_dyn = G.n_dyn != 0;
       CodeConsts<KB> kc;
       kc.load(a);
-      for (int k = 0; k < n_my && !failed; ++k, ++n_t) {
-        const int st = n_t % NST, pb = n_t & 1;
-        if (!warp_wait(&full_bar[st], static_cast<uint32_t>((n_t / NST) & 1), abort_flag)) {
-          failed = true;
-          break;
-        }
-        const uint8_t* tile = stages + st * CHUNK;
-        float sc[2][4];
+      // scores of one group into the lane's C fragment
+      auto qk_scores = [&](const uint8_t* tile, float (&sc)[2][4]) {
         if constexpr (TQ) {
           // scores in the rotated domain: codes row-major, token rows of RW
           // words; the pair of channels (16 s + 2t, +1) of a row is byte t
@@ -495,35 +507,56 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
             sc[1][e] = fmaf(sa[1][0][e] + sa[1][1][e], CodeConsts<KB>::kCodeInv, z);
           }
         }
-
-        // valid tokens: inside [qlo, F) and not a KVSink sink of this group
-        uint32_t vbits = 0xffffffffu;
-        if (__any_sync(full, k == k_lo || k == k_hi) || n_dyn) {
-          const int64_t grp = a.g_begin + (my0 - ubase) + static_cast<int64_t>(k) * NP;
-          const int64_t p0 = grp * kGroup;
-          if (p0 < a.qlo) vbits &= 0xffffffffu << static_cast<int>(a.qlo - p0);
-          if (p0 + kGroup > a.F) vbits &= (1u << static_cast<int>(a.F - p0)) - 1u;
-          if (n_dyn) vbits &= ~a.lay.sink_mask[b * n_slots + static_cast<int>(grp % n_slots)];
+      };
+      for (int k = 0; k < n_my && !failed; ++k, ++n_t) {
+        const int st = n_t % NST, pb = n_t & 1;
+        const int64_t f = my0 + static_cast<int64_t>(k) * GPB * NP;  // first item of the run
+        const int cnt = (seg_e - f) < GPB ? static_cast<int>(seg_e - f) : GPB;
+        if (!warp_wait(&full_bar[st], static_cast<uint32_t>((n_t / NST) & 1), abort_flag)) {
+          failed = true;
+          break;
         }
-        float pr[2][2];
+        float pr[GPB][2][2];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int r = 0; r < 2; ++r) pr[mt][r] = sc[mt][2 * r] + sc[mt][2 * r + 1];
-        if (vbits != 0xffffffffu || gq < kMaxGqa) {  // uniform: only edge groups pay for masking
+        for (int q = 0; q < GPB; ++q) {
+          if (q >= cnt) {  // a short run: no group here
+            pr[q][0][0] = pr[q][0][1] = pr[q][1][0] = pr[q][1][1] = -INFINITY;
+            continue;
+          }
+          float sc[2][4];
+          qk_scores(stages + st * STAGE + q * CHUNK, sc);
+          // valid tokens: inside [qlo, F) and not a KVSink sink of this group
+          // (only the unit's first and last groups can be partial)
+          const int64_t it = f + q;
+          uint32_t vbits = 0xffffffffu;
+          if (__any_sync(full, it == ubase || it == ubase + ng - 1) || n_dyn) {
+            const int64_t grp = a.g_begin + (it - ubase);
+            const int64_t p0 = grp * kGroup;
+            if (p0 < a.qlo) vbits &= 0xffffffffu << static_cast<int>(a.qlo - p0);
+            if (p0 + kGroup > a.F) vbits &= (1u << static_cast<int>(a.F - p0)) - 1u;
+            if (n_dyn) vbits &= ~a.lay.sink_mask[b * n_slots + static_cast<int>(grp % n_slots)];
+          }
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const int tok = 16 * mt + g + 8 * r;
-              if (t >= gq || !((vbits >> tok) & 1u)) pr[mt][r] = -INFINITY;
-            }
+            for (int r = 0; r < 2; ++r) pr[q][mt][r] = sc[mt][2 * r] + sc[mt][2 * r + 1];
+          if (vbits != 0xffffffffu || gq < kMaxGqa) {  // uniform: only edge groups pay for masking
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                const int tok = 16 * mt + g + 8 * r;
+                if (t >= gq || !((vbits >> tok) & 1u)) pr[q][mt][r] = -INFINITY;
+              }
+          }
         }
         // lazy rescaling: the running max only moves when some score exceeds
         // it by more than the headroom, so weights stay below 2^8 and the
-        // common path needs one warp vote instead of a max reduction
+        // common path needs one warp vote (per run) instead of a max reduction
         float al = 1.0f;
-        float mx = fmaxf(fmaxf(pr[0][0], pr[0][1]), fmaxf(pr[1][0], pr[1][1]));
+        float mx = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < GPB; ++q) mx = fmaxf(mx, fmaxf(fmaxf(pr[q][0][0], pr[q][0][1]), fmaxf(pr[q][1][0], pr[q][1][1])));
         if (__any_sync(full, mx > m_run + kLazyRescale)) {
           mx = fmaxf(mx, __shfl_xor_sync(full, mx, 4));
           mx = fmaxf(mx, __shfl_xor_sync(full, mx, 8));
@@ -534,29 +567,34 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           m_run = mn;
         }
         const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
-        uint32_t ph[4];  // weights as (f16 value, f16 residual) per token
+        uint32_t ph[GPB][4];  // weights as (f16 value, f16 residual) per token
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int q = 0; q < GPB; ++q)
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const float p = fast_exp2(pr[mt][r] - mref);
-            l_run += p;
-            float w = p;
-            if constexpr (TQ) {  // the V norm of the token folded in (rows past F hold no data: weight 0)
-              const float nv = reinterpret_cast<const float*>(tile + T::VMETA)[16 * mt + g + 8 * r];
-              w = p > 0.0f ? p * nv : 0.0f;
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const float p = fast_exp2(pr[q][mt][r] - mref);
+              l_run += p;
+              float w = p;
+              if constexpr (TQ) {  // the V norm of the token folded in (rows past F hold no data: weight 0)
+                const float nv = reinterpret_cast<const float*>(stages + st * STAGE + q * CHUNK +
+                                                                T::VMETA)[16 * mt + g + 8 * r];
+                w = p > 0.0f ? p * nv : 0.0f;
+              }
+              const __half hp = __float2half_rn(w);
+              ph[q][mt * 2 + r] = as_u32(__halves2half2(hp, __float2half_rn(w - __half2float(hp))));
             }
-            const __half hp = __float2half_rn(w);
-            ph[mt * 2 + r] = as_u32(__halves2half2(hp, __float2half_rn(w - __half2float(hp))));
-          }
         // hand the weights to the PV warp
         if (!warp_wait(&pempty[pb], static_cast<uint32_t>(((n_t >> 1) & 1) ^ 1), abort_flag)) {
           failed = true;
           break;
         }
         uint8_t* pw = pbuf + pb * T::PBUF;
-        *reinterpret_cast<uint4*>(pw + lane * 16) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-        reinterpret_cast<float*>(pw + 32 * 16)[t] = al;  // the 8 lanes of query head t store the same value
+#pragma unroll
+        for (int q = 0; q < GPB; ++q)
+          *reinterpret_cast<uint4*>(pw + (q * 32 + lane) * 16) = make_uint4(ph[q][0], ph[q][1], ph[q][2], ph[q][3]);
+        reinterpret_cast<float*>(pw + GPB * 32 * 16)[t] = al;  // the 8 lanes of query head t store the same value
         mbar_arrive(&pfull[pb]);
       }
       l_run += __shfl_xor_sync(full, l_run, 4);
@@ -578,30 +616,8 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
       const __half2 keep_lo = __halves2half2(__float2half_rn(0.0f), __float2half_rn(1.0f));
       CodeConsts<VB> vc;
       vc.load(a);
-      for (int k = 0; k < n_my && !failed; ++k, ++n_t) {
-        const int st = n_t % NST, pb = n_t & 1;
-        if (!warp_wait(&pfull[pb], static_cast<uint32_t>((n_t >> 1) & 1), abort_flag) ||
-            !warp_wait(&full_bar[st], static_cast<uint32_t>((n_t / NST) & 1), abort_flag)) {
-          failed = true;
-          break;
-        }
-        const uint8_t* tile = stages + st * CHUNK;
-        const uint8_t* pw = pbuf + pb * T::PBUF;
-        const uint4 pv4 = *reinterpret_cast<const uint4*>(pw + lane * 16);
-        const float al = reinterpret_cast<const float*>(pw + 32 * 16)[t];
-        mbar_arrive(&pempty[pb]);
-        const uint32_t ph[4] = {pv4.x, pv4.y, pv4.z, pv4.w};
-        if (__any_sync(full, al != 1.0f)) {
-#pragma unroll
-          for (int m = 0; m < MV; ++m) {
-            oacc[m][0] *= al;
-            oacc[m][1] *= al;
-            oacc[m][2] *= al;
-            oacc[m][3] *= al;
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) zacc[e] *= al;
-        }
+      // values of one group with its weights ph into oacc, zacc
+      auto pv_values = [&](const uint8_t* tile, const uint32_t (&ph)[4]) {
         if constexpr (TQ) {
           // out^T += V^T (p n_v) with one B operand for every m-tile. The V
           // rows are dequantised into this warp's f16 tile first (lane r
@@ -713,13 +729,45 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           }
         }
         }
-        // this pair is done with the stage: refill it with the next chunk
-        __syncwarp();
-        if (pc.item >= 0) {
-          bulk_g2s_if(lane == 0, stages + st * CHUNK, pc.ptr, CHUNK, &full_bar[st]);
-          pc.advance(i1, ng, pair, a.g_begin, n_slots, a.lay.chunks, CHUNK);
-          ++issued;
+      };
+      for (int k = 0; k < n_my && !failed; ++k, ++n_t) {
+        const int st = n_t % NST, pb = n_t & 1;
+        const int64_t f = my0 + static_cast<int64_t>(k) * GPB * NP;
+        const int cnt = (seg_e - f) < GPB ? static_cast<int>(seg_e - f) : GPB;
+        if (!warp_wait(&pfull[pb], static_cast<uint32_t>((n_t >> 1) & 1), abort_flag) ||
+            !warp_wait(&full_bar[st], static_cast<uint32_t>((n_t / NST) & 1), abort_flag)) {
+          failed = true;
+          break;
         }
+        const uint8_t* pw = pbuf + pb * T::PBUF;
+        uint32_t ph[GPB][4];
+#pragma unroll
+        for (int q = 0; q < GPB; ++q) {
+          const uint4 pv4 = *reinterpret_cast<const uint4*>(pw + (q * 32 + lane) * 16);
+          ph[q][0] = pv4.x;
+          ph[q][1] = pv4.y;
+          ph[q][2] = pv4.z;
+          ph[q][3] = pv4.w;
+        }
+        const float al = reinterpret_cast<const float*>(pw + GPB * 32 * 16)[t];
+        mbar_arrive(&pempty[pb]);
+        if (__any_sync(full, al != 1.0f)) {
+#pragma unroll
+          for (int m = 0; m < MV; ++m) {
+            oacc[m][0] *= al;
+            oacc[m][1] *= al;
+            oacc[m][2] *= al;
+            oacc[m][3] *= al;
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) zacc[e] *= al;
+        }
+#pragma unroll
+        for (int q = 0; q < GPB; ++q)
+          if (q < cnt) pv_values(stages + st * STAGE + q * CHUNK, ph[q]);
+        // this pair is done with the stage: refill it with the next run
+        __syncwarp();
+        if (pc.item >= 0) fetch(st);
       }
       // zero sum of group v, query head t, is in lane (v, t)
       const float zt = TQ ? 0.0f : zacc[0] + zacc[1];
