@@ -322,10 +322,14 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
   int issued = 0;
   auto fetch = [&](int st) {  // the cursor's run into stage st, then advance
     expect_tx_if(lane == 0, &full_bar[st], static_cast<uint32_t>(pc.cnt * CHUNK));
+    if (GPB == 1 || pc.cnt == 1 || pc.slot + 1 < n_slots) {  // the run's chunks are adjacent: one copy
+      copy_g2s_if(lane == 0, stages + st * STAGE, pc.ptr, pc.cnt * CHUNK, &full_bar[st]);
+    } else {
 #pragma unroll
-    for (int q = 0; q < GPB; ++q)
-      if (q < pc.cnt) copy_g2s_if(lane == 0, stages + st * STAGE + q * CHUNK, pc.chunk(q, n_slots, CHUNK), CHUNK,
-                                  &full_bar[st]);
+      for (int q = 0; q < GPB; ++q)
+        if (q < pc.cnt) copy_g2s_if(lane == 0, stages + st * STAGE + q * CHUNK, pc.chunk(q, n_slots, CHUNK), CHUNK,
+                                    &full_bar[st]);
+    }
     pc.advance(i1, ng, pair, a.g_begin, n_slots, a.lay.chunks, CHUNK);
     ++issued;
   };
