@@ -512,6 +512,68 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           }
         }
       };
+      // scores of the two groups of a run, k-step by k-step: one read of
+      // the query operand per k-step serves both, and their MMA chains are
+      // independent (KIVI runs of two groups only)
+      auto qk_scores_pair = [&](const uint8_t* t0, const uint8_t* t1, float (&sc)[2][2][4]) {
+        const uint8_t* tl[2] = {t0, t1};
+        uint32_t kr[2][KW];
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int i = 0; i < KW / 4; ++i)
+            *reinterpret_cast<uint4*>(&kr[q][4 * i]) = reinterpret_cast<const uint4*>(tl[q])[i * 32 + lane];
+        float zb[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+        float sa[2][2][4] = {};
+#pragma unroll
+        for (int u = 0; u < S / 2; ++u) {
+          uint32_t sp[2][4];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const uint4 s4 = reinterpret_cast<const uint4*>(tl[q] + T::KMETA)[u * 4 + t];
+            sp[q][0] = s4.x;
+            sp[q][1] = s4.y;
+            sp[q][2] = s4.z;
+            sp[q][3] = s4.w;
+          }
+#pragma unroll
+          for (int hlf = 0; hlf < 2; ++hlf) {
+            const int s = 2 * u + hlf;
+            const uint4 q4 = qsm[s * 32 + lane];
+            const uint32_t qx[2] = {q4.x, q4.z}, qa[2] = {q4.y, q4.w};
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              uint32_t bq[2];
+#pragma unroll
+              for (int p = 0; p < 2; ++p) {
+                const __half2 sv = as_h2(sp[q][2 * hlf + p]);
+                const __half2 x = __hmul2(as_h2(qx[p]), sv);
+                const __half2 y = __hfma2(as_h2(qx[p]), sv, __hneg2(x));  // exact residual of x
+                bq[p] = as_u32(__hfma2(as_h2(qa[p]), sv, y));
+              }
+              uint32_t za[4];
+              ldmatrix_x4(za, tl[q] + T::KMETA + 2 * D + ((lane >> 4) & 1) * 16 + s * 32);
+              mma_f16(zb[q], za[0], za[1], za[2], za[3], qa[0], qa[1]);
+#pragma unroll
+              for (int mt = 0; mt < 2; ++mt) {
+                const int pbase = (mt * S + s) * 4;
+                const uint32_t a0 = code_pair<KB>(kc, kr[q][(pbase + 0) / KPPW], (pbase + 0) % KPPW);
+                const uint32_t a1 = code_pair<KB>(kc, kr[q][(pbase + 1) / KPPW], (pbase + 1) % KPPW);
+                const uint32_t a2 = code_pair<KB>(kc, kr[q][(pbase + 2) / KPPW], (pbase + 2) % KPPW);
+                const uint32_t a3 = code_pair<KB>(kc, kr[q][(pbase + 3) / KPPW], (pbase + 3) % KPPW);
+                mma_f16(sa[q][mt], a0, a1, a2, a3, bq[0], bq[1]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sc[q][0][e] = fmaf(sa[q][0][e], CodeConsts<KB>::kCodeInv, zb[q][e]);
+            sc[q][1][e] = fmaf(sa[q][1][e], CodeConsts<KB>::kCodeInv, zb[q][e]);
+          }
+      };
       for (int k = 0; k < n_my && !failed; ++k, ++n_t) {
         const int st = n_t % NST, pb = n_t & 1;
         const int64_t f = my0 + static_cast<int64_t>(k) * GPB * NP;  // first item of the run
@@ -520,6 +582,12 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           failed = true;
           break;
         }
+        float scr[GPB][2][4];
+        if constexpr (GPB == 2) {  // a short run scores its one group twice (the copy is discarded)
+          qk_scores_pair(stages + st * STAGE, stages + st * STAGE + (cnt > 1 ? CHUNK : 0), scr);
+        } else {
+          qk_scores(stages + st * STAGE, scr[0]);
+        }
         float pr[GPB][2][2];
 #pragma unroll
         for (int q = 0; q < GPB; ++q) {
@@ -527,8 +595,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
             pr[q][0][0] = pr[q][0][1] = pr[q][1][0] = pr[q][1][1] = -INFINITY;
             continue;
           }
-          float sc[2][4];
-          qk_scores(stages + st * STAGE + q * CHUNK, sc);
+          const float (&sc)[2][4] = scr[q];
           // valid tokens: inside [qlo, F) and not a KVSink sink of this group
           // (only the unit's first and last groups can be partial)
           const int64_t it = f + q;
