@@ -399,7 +399,7 @@ def run_ours(args, rank, world, local):
             "config": {"workload": WORKLOAD_NAME, "global_batch": w["batch"] * world, "seq_len": L,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (about 543 MB of cache read per step)",
-                       "arith": "codes exact in f16 MMA operands, scales folded as f16 hi+lo, f32 accumulate"},
+                       "arith": "codes exact in f16 MMA operands; K scales folded into q as f16 value + residual, V scales into the f16 weights; f32 accumulate"},
             "us_per_step": round(ms_step * 1e3, 2),
             "us_per_model_step_x32": round(ms_step * 1e3 * w["layers_reported"], 1),
             "pct_of_peak": round(100 * achieved / peak, 2),

@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           m_run = mn;
         }
         const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
-        uint32_t ph[GPB][4];  // weights as (f16 value, f16 residual) per token
+        uint32_t ph[GPB][4];  // weights as (f16 value, 0) per token: the odd B columns stay zero
 #pragma unroll
         for (int q = 0; q < GPB; ++q)
 #pragma unroll
@@ -653,8 +653,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
                                                                 T::VMETA)[16 * mt + g + 8 * r];
                 w = p > 0.0f ? p * nv : 0.0f;
               }
-              const __half hp = __float2half_rn(w);
-              ph[q][mt * 2 + r] = as_u32(__halves2half2(hp, __float2half_rn(w - __half2float(hp))));
+              ph[q][mt * 2 + r] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(w)));
             }
         // hand the weights to the PV warp
         if (!warp_wait(&pempty[pb], static_cast<uint32_t>(((n_t >> 1) & 1) ^ 1), abort_flag)) {
@@ -684,7 +683,6 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
       float zacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int m = 0; m < MV; ++m) oacc[m][0] = oacc[m][1] = oacc[m][2] = oacc[m][3] = 0.0f;
-      const __half2 keep_lo = __halves2half2(__float2half_rn(0.0f), __float2half_rn(1.0f));
       CodeConsts<VB> vc;
       vc.load(a);
       // values of one group with its weights ph into oacc, zacc
@@ -735,28 +733,26 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
             }
           __syncwarp();  // the tile is read before the next group overwrites it
         } else {
-        // V scales of this thread's four tokens (NVG f16 per token)
-        uint32_t vsw[4][NVG / 2];
+        // the weights as the B operand (column g, token pairs 2t + 8 kk,
+        // + 1; the odd columns are zero), shared by the zero-point MMA and
+        // every channel group
+        uint32_t bT[4];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const int tok = 16 * (kk >> 1) + g + 8 * (kk & 1);
-          const uint32_t* row = reinterpret_cast<const uint32_t*>(tile + T::VMETA) + tok * (NVG / 2);
-#pragma unroll
-          for (int i = 0; i < NVG / 2; ++i) vsw[kk][i] = row[i];
-        }
+        for (int kk = 0; kk < 4; ++kk) bT[kk] = movmatrix_t(ph[kk]);
         // zero points: zsum[v][j] += sum_t zV[t][v] p_j[t] as one MMA per
         // 16 tokens with the groups as rows (the zeros are stored group-major)
         {
           const uint32_t* zw = reinterpret_cast<const uint32_t*>(tile + T::VMETA + 64 * NVG);
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
-            const uint32_t bz0 = movmatrix_t(ph[2 * kb]);
-            const uint32_t bz1 = movmatrix_t(ph[2 * kb + 1]);
             const uint32_t z0 = g < NVG ? zw[g * 16 + 8 * kb + t] : 0u;
             const uint32_t z2 = g < NVG ? zw[g * 16 + 8 * kb + t + 4] : 0u;
-            mma_f16(zacc, z0, 0u, z2, 0u, bz0, bz1);
+            mma_f16(zacc, z0, 0u, z2, 0u, bT[2 * kb], bT[2 * kb + 1]);
           }
         }
+        // V scales in B order: 16 bytes per lane and group hold the scales
+        // of the lane's token pairs 2t + 8 kk, + 1 (kk = 0..3)
+        const uint4* vsc = reinterpret_cast<const uint4*>(tile + T::VMETA);
         const uint4* vcode = reinterpret_cast<const uint4*>(tile + T::VC);
 #pragma unroll
         for (int v = 0; v < NVG; ++v) {
@@ -773,20 +769,13 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
               if (wi >= 0 && wi < VB) vr[wi] = ww[k2];
             }
           }
-          uint32_t R[4];
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const __half2 s2 = (v & 1) ? __high2half2(as_h2(vsw[kk][v >> 1])) : __low2half2(as_h2(vsw[kk][v >> 1]));
-            // (p_hi s, p_lo s), the exact residual of p_hi s, and their sum
-            const __half2 pk = as_h2(ph[kk]);
-            const __half2 x = __hmul2(pk, s2);
-            const __half2 e = __hfma2(__low2half2(pk), s2, __hneg2(__low2half2(x)));
-            R[kk] = as_u32(__hfma2(e, keep_lo, x));
-          }
+          const uint4 s4 = vsc[v * 4 + t];
+          const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
-            const uint32_t b0 = movmatrix_t(R[2 * kb]);
-            const uint32_t b1 = movmatrix_t(R[2 * kb + 1]);
+            // p s of each token: one f16 product per weight
+            const uint32_t b0 = as_u32(__hmul2(as_h2(bT[2 * kb]), as_h2(sw[2 * kb])));
+            const uint32_t b1 = as_u32(__hmul2(as_h2(bT[2 * kb + 1]), as_h2(sw[2 * kb + 1])));
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
               const int m = 2 * v + hh;

@@ -5,7 +5,7 @@
 // A "chunk" holds one 32-token group of one (layer, b, kv-head):
 //   KIVI:       [K codes 32*D*kb/8][K scales D f16][K zeros D f16]
 //               [V codes 32*D*vb/8][V scales 32 x D/32 f16][V zeros D/32 x 32 f16]
-//               (V scales token-major, V zeros group-major: vscale_pos, vzero_pos)
+//               (both group-major, scales in lane order: vscale_pos, vzero_pos)
 //   TurboQuant: [K codes 32 x D*kb/8 row-major][K norms 32 f32]
 //               [V codes 32 x D*vb/8 row-major][V norms 32 f32]
 // Chunk sizes are multiples of 16 bytes so one 1-D bulk copy moves a chunk.
@@ -108,10 +108,16 @@ KVQ_HD int kzero_pos(int D, int c) {
 }
 
 // f16 positions inside the V meta of token r, channel group vg (NV groups):
-// the scales token by token, then the zeros group by group (so that one
-// 32-bit word holds the zeros of two consecutive tokens of a group, the A
-// operand of the decode kernel's zero-point MMA).
-KVQ_HD int vscale_pos(int NV, int r, int vg) { return r * NV + vg; }
+// the scales group by group, each group's 32 in the order the decode
+// kernel's B operand wants them (token 8 kk + 2t + e at 8t + 2kk + e, so
+// the lanes t of a group read 16 contiguous bytes holding the token pairs
+// (2t, 2t + 1), (2t + 8, 2t + 9), ... in 32-bit words), then the zeros group
+// by group in token order (one 32-bit word holds the zeros of two
+// consecutive tokens of a group, the A operand of the zero-point MMA).
+KVQ_HD int vscale_pos(int NV, int r, int vg) {
+  (void)NV;
+  return vg * 32 + 8 * ((r & 7) >> 1) + 2 * (r >> 3) + (r & 1);
+}
 KVQ_HD int vzero_pos(int NV, int r, int vg) { return 32 * NV + vg * 32 + r; }
 
 // Word index and bit position of element f inside a lane block. Pair

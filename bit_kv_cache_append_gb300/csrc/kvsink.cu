@@ -123,7 +123,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(SinkSelectArgs
 // place), stored in ascending position order as the sink set.
 __global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(SinkSelectArgs a) {
   const int b = blockIdx.x;
-  __shared__ float fm[kMaxSinks];
   __shared__ int64_t fp[kMaxSinks];
   __shared__ float wm[kTopkThreads / 32];
   __shared__ int64_t wp[kTopkThreads / 32];
@@ -157,7 +156,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(SinkSelectArgs
       int xc = wc[0];
       for (int w = 1; w < kTopkThreads / 32; ++w)
         if (better(wm[w], wp[w], xm, xp)) { xm = wm[w]; xp = wp[w]; xc = wc[w]; }
-      fm[round] = xm;
       fp[round] = xp;
       if (xc >= 0) { cm_base[xc] = -INFINITY; cp_base[xc] = INT64_MAX; }
     }

@@ -28,3 +28,23 @@ def read_golden(name):
 @pytest.fixture
 def golden():
     return read_golden
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Worst attention errors seen against the oracle (the margins under the
+    tolerances) and the tests that produced them, when any comparison ran."""
+    parity = sys.modules.get("tests.parity")
+    errs = getattr(parity, "ERRORS", None)
+    if errs:
+        rel = max(e[0] for e in errs)
+        mx = max(e[1] for e in errs)
+        terminalreporter.write_line(
+            f"attention parity: {len(errs)} comparisons, worst rel-L2 {rel:.3e} (limit {parity.REL_L2:g}), "
+            f"worst max-abs {mx:.3e} (limit {parity.MAX_ABS:g})")
+        worst = {}
+        for e in errs:
+            name = e[2].split("[")[0]
+            if name not in worst or e[0] > worst[name][0]:
+                worst[name] = e
+        for e in sorted(worst.values(), key=lambda e: -e[0]):
+            terminalreporter.write_line(f"  rel-L2 {e[0]:.3e}  max-abs {e[1]:.3e}  {e[2]}")

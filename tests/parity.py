@@ -13,6 +13,10 @@ import numpy as np
 REL_L2 = 1e-3
 MAX_ABS = 5e-3
 
+# (rel_l2, max_abs, test) of every attention comparison of the session, for
+# the summary the test session prints at its end
+ERRORS: list = []
+
 KIVI_ARRAYS = ("k_codes", "k_scale", "k_zero", "v_codes", "v_scale", "v_zero")
 TQ_ARRAYS = ("k_codes", "k_norm", "v_codes", "v_norm")
 
@@ -84,5 +88,7 @@ def compare_attention(out_gpu: np.ndarray, out_ref: np.ndarray, heads=None) -> d
     rel = float(np.linalg.norm(d) / max(np.linalg.norm(out_ref.astype(np.float64)), 1e-30))
     mx = float(np.max(np.abs(d))) if d.size else 0.0
     assert np.all(np.isfinite(out_gpu)), "non-finite output"
+    import os
+    ERRORS.append((rel, mx, os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]))
     assert rel <= REL_L2 and mx <= MAX_ABS, dict(rel_l2=rel, max_abs=mx)
     return dict(rel_l2=rel, max_abs=mx)

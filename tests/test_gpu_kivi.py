@@ -114,9 +114,13 @@ def test_split_count_invariance():
         gc.prefill_quantize(0, torch_act(k, "bf16"), torch_act(v, "bf16"))
         outs.append(gc.decode_attn(0, q).cpu().numpy())
     torch.cuda.synchronize()
+    # the weights enter the value products as f16 (11 significant bits) taken
+    # relative to each partition's own running max, so partitionings agree
+    # to a few 1e-4 (relative rounding of at most 2^-11 twice per term); a
+    # wrong log-sum-exp merge shows as an O(1) difference
     for o in outs[1:]:
         d = np.linalg.norm(o - outs[0]) / np.linalg.norm(outs[0])
-        assert d < 1e-5
+        assert d < 5e-4
 
 
 def test_constant_and_extreme_groups():
