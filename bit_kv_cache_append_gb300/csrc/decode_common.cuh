@@ -195,11 +195,11 @@ __device__ __forceinline__ float query_value(const DecodeArgs& a, int b, int hq,
   return x * a.qscale;
 }
 
-// query_value of the channel pair (c0, c0 + 1), c0 even: one 32-bit load of
-// the pair (q must be 4-byte aligned) and, with RoPE, of its rotation
-// partner and one 16-byte load of the two table entries; the same
-// arithmetic element by element.
-__device__ __forceinline__ float2 query_pair(const DecodeArgs& a, int b, int hq, int c0) {
+// The channel pair (c0, c0 + 1), c0 even, of a query row times `scale`
+// (query_value's arithmetic element by element when scale is a.qscale): one
+// 32-bit load of the pair (q must be 4-byte aligned) and, with RoPE, of its
+// rotation partner and one 16-byte load of the two table entries.
+__device__ __forceinline__ float2 query_pair(const DecodeArgs& a, int b, int hq, int c0, float scale) {
   const Geometry& G = a.geo;
   const int D = G.D, half = D / 2;
   const uint16_t* qrow = a.q + (static_cast<size_t>(b) * G.Hq + hq) * D;
@@ -222,7 +222,7 @@ __device__ __forceinline__ float2 query_pair(const DecodeArgs& a, int b, int hq,
       rope_pair(y1, x1, tr.z, tr.w, &ra, &rb), x1 = rb;
     }
   }
-  return make_float2(x0 * a.qscale, x1 * a.qscale);
+  return make_float2(x0 * scale, x1 * scale);
 }
 
 // Per-warp online-softmax states of one CTA merged through shared memory and
@@ -439,7 +439,7 @@ __device__ bool exact_states_tc(const DecodeArgs& a, int b, int h, float* red, u
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
       const int c0 = 16 * s + 2 * t + 8 * p;
-      const float2 x = jc < gq ? query_pair(a, b, h * gq + jc, c0) : make_float2(0.0f, 0.0f);
+      const float2 x = jc < gq ? query_pair(a, b, h * gq + jc, c0, a.qscale) : make_float2(0.0f, 0.0f);
       qb[s][p] = split_act2<BF>(x.x, x.y, col_lo);
     }
   float m_run = -INFINITY, l_run = 0.0f;  // of query head t (this lane's C columns)

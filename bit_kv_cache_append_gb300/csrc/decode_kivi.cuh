@@ -260,7 +260,12 @@ struct RunCursor {
   }
 };
 
-template <int D, int KB, int VB, bool TQ>
+// QX (KIVI only): the query enters unscaled and unrotated, so each value is
+// exact in f16 (an f16 or bf16 activation) and q sK splits into an f16
+// product and its exact residual in two operations; the score scale is
+// applied in the softmax. Otherwise (RoPE applied here, or TurboQuant) the
+// query is an fp32 value carried as f16 value + residual with the scale in.
+template <int D, int KB, int VB, bool TQ, bool QX>
 __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(DecodeArgs a) {
   using T = KiviTile<D, KB, VB, TQ>;
   constexpr int NP = T::NP, NST = T::NST, CHUNK = T::CHUNK;
@@ -353,9 +358,10 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
     if (!is_pv) {
       // ------------------------------------------------------------ QK warp
       // the query operand of the unit, shared by the CTA's QK warps: per
-      // k-step s and lane, {qx, qa} of the lane's two k-pairs, where qa is
-      // the column's operand (value, or residual on "lo" columns) and qx the
-      // value on "lo" columns, zero on the others, so that
+      // k-step s and lane, {qx, qa} of the lane's two k-pairs (fold_q turns
+      // it into the B operand). QX: qa is the value and qx the value on "lo"
+      // columns, zero on the others. Otherwise qa is the column's operand
+      // (value, or residual on "lo" columns) and qx as before, so that
       // qa s + (qx s - f16(qx s)) is the column's folded operand
       uint4* qsm = reinterpret_cast<uint4*>(smem + T::OFF_Q);
       if constexpr (TQ) {
@@ -401,21 +407,44 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             const int c0 = t * (D / 4) + 4 * s + 2 * p;
-            const float2 x = jc < gq ? query_pair(a, b, h * gq + jc, c0) : make_float2(0.0f, 0.0f);
+            const float2 x = jc < gq ? query_pair(a, b, h * gq + jc, c0, QX ? 1.0f : a.qscale)
+                                     : make_float2(0.0f, 0.0f);
             const float x0 = x.x, x1 = x.y;
             const uint32_t hi = f2_to_h2(x0, x1);
-            const float2 hf = h2_to_f2(hi);
-            v[2 * p] = col_lo ? hi : 0u;
-            v[2 * p + 1] = col_lo ? f2_to_h2(x0 - hf.x, x1 - hf.y) : hi;
+            if constexpr (QX) {  // {qm, qv}: q on "lo" columns (else 0), q
+              v[2 * p] = col_lo ? hi : 0u;
+              v[2 * p + 1] = hi;
+            } else {
+              const float2 hf = h2_to_f2(hi);
+              v[2 * p] = col_lo ? hi : 0u;
+              v[2 * p + 1] = col_lo ? f2_to_h2(x0 - hf.x, x1 - hf.y) : hi;
+            }
           }
           qsm[s * 32 + lane] = make_uint4(v[0], v[1], v[2], v[3]);
         }
         named_barrier_sync(1, NP * 32);  // the QK warps only
       }
+      // the running max m_run is in score units; ks turns them into log2
+      // units (the score scale when the scores arrive unscaled, else 1)
       float m_run = -INFINITY, l_run = 0.0f;
+      const float ks = QX ? a.qscale : 1.0f;
+      const float lazy = QX ? kLazyRescale / a.qscale : kLazyRescale;
       const bool n_dyn = G.n_dyn != 0;
       CodeConsts<KB> kc;
       kc.load(a);
+      // the B operand of one k-step: the query operand {qx, qa} times the K
+      // scales sK of its channels, as an f16 product on "value" columns and
+      // the rest of the product on "lo" columns
+      auto fold_q = [&](uint32_t qx, uint32_t qa, uint32_t sk) -> uint32_t {
+        const __half2 sv = as_h2(sk);
+        const __half2 x = __hmul2(as_h2(qx), sv);
+        if constexpr (QX) {  // qv sK - (qm sK on lo columns): the product, or its exact residual
+          return as_u32(__hfma2(as_h2(qa), sv, __hneg2(x)));
+        } else {  // qa sK + the exact residual of qx sK
+          const __half2 y = __hfma2(as_h2(qx), sv, __hneg2(x));
+          return as_u32(__hfma2(as_h2(qa), sv, y));
+        }
+      };
       // scores of one group into the lane's C fragment
       auto qk_scores = [&](const uint8_t* tile, float (&sc)[2][4]) {
         if constexpr (TQ) {
@@ -484,15 +513,10 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
               const uint32_t qx[2] = {q4.x, q4.z}, qa[2] = {q4.y, q4.w};
               uint32_t bq[2];
 #pragma unroll
-              for (int p = 0; p < 2; ++p) {
-                const __half2 sv = as_h2(sp[2 * hlf + p]);
-                const __half2 x = __hmul2(as_h2(qx[p]), sv);
-                const __half2 y = __hfma2(as_h2(qx[p]), sv, __hneg2(x));  // exact residual of x
-                bq[p] = as_u32(__hfma2(as_h2(qa[p]), sv, y));
-              }
+              for (int p = 0; p < 2; ++p) bq[p] = fold_q(qx[p], qa[p], sp[2 * hlf + p]);
               uint32_t za[4];
               ldmatrix_x4(za, zrow + s * 32);
-              mma_f16(zb[hlf], za[0], za[1], za[2], za[3], qa[0], qa[1]);
+              mma_f16(zb[hlf], za[0], za[1], za[2], za[3], QX ? qx[0] : qa[0], QX ? qx[1] : qa[1]);
 #pragma unroll
               for (int mt = 0; mt < 2; ++mt) {
                 const int pbase = (mt * S + s) * 4;
@@ -545,15 +569,10 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
             for (int q = 0; q < 2; ++q) {
               uint32_t bq[2];
 #pragma unroll
-              for (int p = 0; p < 2; ++p) {
-                const __half2 sv = as_h2(sp[q][2 * hlf + p]);
-                const __half2 x = __hmul2(as_h2(qx[p]), sv);
-                const __half2 y = __hfma2(as_h2(qx[p]), sv, __hneg2(x));  // exact residual of x
-                bq[p] = as_u32(__hfma2(as_h2(qa[p]), sv, y));
-              }
+              for (int p = 0; p < 2; ++p) bq[p] = fold_q(qx[p], qa[p], sp[q][2 * hlf + p]);
               uint32_t za[4];
               ldmatrix_x4(za, tl[q] + T::KMETA + 2 * D + ((lane >> 4) & 1) * 16 + s * 32);
-              mma_f16(zb[q], za[0], za[1], za[2], za[3], qa[0], qa[1]);
+              mma_f16(zb[q], za[0], za[1], za[2], za[3], QX ? qx[0] : qa[0], QX ? qx[1] : qa[1]);
 #pragma unroll
               for (int mt = 0; mt < 2; ++mt) {
                 const int pbase = (mt * S + s) * 4;
@@ -628,16 +647,16 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
         float mx = -INFINITY;
 #pragma unroll
         for (int q = 0; q < GPB; ++q) mx = fmaxf(mx, fmaxf(fmaxf(pr[q][0][0], pr[q][0][1]), fmaxf(pr[q][1][0], pr[q][1][1])));
-        if (__any_sync(full, mx > m_run + kLazyRescale)) {
+        if (__any_sync(full, mx > m_run + lazy)) {
           mx = fmaxf(mx, __shfl_xor_sync(full, mx, 4));
           mx = fmaxf(mx, __shfl_xor_sync(full, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(full, mx, 16));
-          const float mn = mx > m_run + kLazyRescale ? mx : m_run;
-          al = (m_run == -INFINITY) ? 0.0f : fast_exp2(m_run - mn);
+          const float mn = mx > m_run + lazy ? mx : m_run;
+          al = (m_run == -INFINITY) ? 0.0f : fast_exp2((m_run - mn) * ks);
           l_run *= al;
           m_run = mn;
         }
-        const float mref = (m_run == -INFINITY) ? 0.0f : m_run;
+        const float nref = (m_run == -INFINITY) ? 0.0f : -m_run * ks;  // exponent offset
         uint32_t ph[GPB][4];  // weights as (f16 value, 0) per token: the odd B columns stay zero
 #pragma unroll
         for (int q = 0; q < GPB; ++q)
@@ -645,7 +664,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-              const float p = fast_exp2(pr[q][mt][r] - mref);
+              const float p = fast_exp2(fmaf(pr[q][mt][r], ks, nref));
               l_run += p;
               float w = p;
               if constexpr (TQ) {  // the V norm of the token folded in (rows past F hold no data: weight 0)
@@ -673,7 +692,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
       __syncthreads();  // (1) the previous unit's partial has been written
       if (t < gq && g == 0) {
         float* rj = red + (pair * kMaxGqa + t) * (D + 2);
-        rj[D] = m_run;
+        rj[D] = m_run * ks;  // log2 units
         rj[D + 1] = l_run;
       }
     } else {
@@ -855,7 +874,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
   }
 }
 
-template <int D, int KB, int VB, bool TQ>
+template <int D, int KB, int VB, bool TQ, bool QX>
 cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
   using T = KiviTile<D, KB, VB, TQ>;
   const size_t smem = T::smem_bytes();
@@ -866,10 +885,10 @@ cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   int& occupancy = occ_of[dev];
   if (!occupancy) {
-    e = cudaFuncSetAttribute(decode_kivi_kernel<D, KB, VB, TQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kivi_kernel<D, KB, VB, TQ, QX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, decode_kivi_kernel<D, KB, VB, TQ>, 64 * T::NP, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, decode_kivi_kernel<D, KB, VB, TQ, QX>, 64 * T::NP, smem);
     if (e != cudaSuccess) return e;
     if (occupancy < 1) occupancy = 1;
   }
@@ -882,7 +901,7 @@ cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
   if (n < 1) n = 1;
   a.n_ctas = static_cast<int>(n);
   if (a.work <= 0) return cudaSuccess;  // nothing quantised to read: the merge does it all
-  decode_kivi_kernel<D, KB, VB, TQ><<<a.n_ctas, 64 * T::NP, smem, s>>>(a);
+  decode_kivi_kernel<D, KB, VB, TQ, QX><<<a.n_ctas, 64 * T::NP, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -891,13 +910,17 @@ cudaError_t launch_kivi_d(DecodeArgs& a, cudaStream_t s, int sm_count) {
   const int kb = a.geo.kb, vb = a.geo.vb;
   if (a.geo.mode_tq) {
 #define KVQ_CASE(K, V) \
-  if (kb == K && vb == V) return launch_kivi_instance<D, K, V, true>(a, s, sm_count);
+  if (kb == K && vb == V) return launch_kivi_instance<D, K, V, true, false>(a, s, sm_count);
     KVQ_CASE(2, 2) KVQ_CASE(2, 4) KVQ_CASE(4, 2) KVQ_CASE(4, 4)
 #undef KVQ_CASE
     return cudaErrorInvalidValue;
   }
-#define KVQ_CASE(K, V) \
-  if (kb == K && vb == V) return launch_kivi_instance<D, K, V, false>(a, s, sm_count);
+  // an exact query operand unless RoPE is applied to the query here
+  const bool qx = a.tab.rope == nullptr;
+#define KVQ_CASE(K, V)                                                                                    \
+  if (kb == K && vb == V)                                                                                 \
+    return qx ? launch_kivi_instance<D, K, V, false, true>(a, s, sm_count)                               \
+              : launch_kivi_instance<D, K, V, false, false>(a, s, sm_count);
   KVQ_CASE(2, 2) KVQ_CASE(2, 4) KVQ_CASE(2, 8)
   KVQ_CASE(4, 2) KVQ_CASE(4, 4) KVQ_CASE(4, 8)
   KVQ_CASE(8, 2) KVQ_CASE(8, 4) KVQ_CASE(8, 8)
