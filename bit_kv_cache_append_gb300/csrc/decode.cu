@@ -59,22 +59,42 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(DecodeArgs a, i
   const int ns = slots_of_unit(a, u);
   const float* ml = a.part_ml + static_cast<size_t>(row) * a.ns * 2;
   const float* rj = red + j * (D + 2);  // warp w's state at rj + w * kMaxGqa * (D + 2)
-  float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, ml[2 * s]);
-  if (lane < NW) M = fmaxf(M, rj[lane * kMaxGqa * (D + 2) + D]);
+  // the exact states' max first (shared memory), then the split partials in
+  // chunks of four slots whose loads are all issued before any is used: the
+  // running max only grows, the sums so far are rescaled when it does
+  float M = lane < NW ? rj[lane * kMaxGqa * (D + 2) + D] : -INFINITY;
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float L = 0.0f, oq[NS], oe[NS];
 #pragma unroll
   for (int i = 0; i < NS; ++i) oq[i] = oe[i] = 0.0f;
-#pragma unroll 4
-  for (int s = 0; s < ns; ++s) {  // a slot with m = -inf has o = 0 and l = 0
-    const float ms = ml[2 * s];
-    const float w = ms == -INFINITY ? 0.0f : exp2f(ms - M);
-    L = fmaf(ml[2 * s + 1], w, L);
-    const float* po = a.part_o + (static_cast<size_t>(row) * a.ns + s) * D;
+  for (int s0 = 0; s0 < ns; s0 += 4) {  // a slot with m = -inf has o = 0 and l = 0
+    float ms[4], ls[4], po[4][NS];
 #pragma unroll
-    for (int i = 0; i < NS; ++i) oq[i] = fmaf(po[i * 32 + lane], w, oq[i]);
+    for (int c = 0; c < 4; ++c) {
+      const int s = s0 + c;
+      const bool in = s < ns;
+      ms[c] = in ? ml[2 * s] : -INFINITY;
+      ls[c] = in ? ml[2 * s + 1] : 0.0f;
+      const float* p = a.part_o + (static_cast<size_t>(row) * a.ns + (in ? s : 0)) * D;
+#pragma unroll
+      for (int i = 0; i < NS; ++i) po[c][i] = in ? p[i * 32 + lane] : 0.0f;
+    }
+    const float Mn = fmaxf(fmaxf(M, fmaxf(ms[0], ms[1])), fmaxf(ms[2], ms[3]));
+    if (Mn > M) {  // warp-uniform (every lane holds the same values)
+      const float r = M == -INFINITY ? 0.0f : exp2f(M - Mn);
+      L *= r;
+#pragma unroll
+      for (int i = 0; i < NS; ++i) oq[i] *= r;
+      M = Mn;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float w = ms[c] == -INFINITY ? 0.0f : exp2f(ms[c] - M);
+      L = fmaf(ls[c], w, L);
+#pragma unroll
+      for (int i = 0; i < NS; ++i) oq[i] = fmaf(po[c][i], w, oq[i]);
+    }
   }
   for (int w = 0; w < NW; ++w) {
     const float* r = rj + w * kMaxGqa * (D + 2);
