@@ -120,7 +120,8 @@ class _Layer:
         ns = max(cfg.n_sink, cfg.n_dyn_sinks)
         self.sink_k = np.zeros((B, H, ns, D), np.float32)
         self.sink_v = np.zeros((B, H, ns, D), np.float32)
-        self.sink_pos = None  # KVSink: int64 [B, k]
+        self.sink_pos = None  # KVSink: int64 [B, n] by position (n = min(k, L))
+        self.sink_m = None    # KVSink: float32 [B, n] their key norms
 
 
 class OracleCache:
@@ -177,27 +178,44 @@ class OracleCache:
             raise OverflowError("capacity")
         if self.cfg.rope_base:
             k = rope.rotate_keys(k, st.L, self.cfg.rope_base, self.cfg.act_dtype)
+        self._fold_sinks(layer, k, v)
         self._append_rotated(layer, k, v)
 
     def prefill_quantize(self, layer: int, k, v) -> None:
-        """kv_prefill_quantize: an append that, in KVSink mode, first selects
-        the top-k sinks over the call's tokens (the cache must be empty)."""
-        k, v = self._check_input(k, v)
+        """kv_prefill_quantize: the same state change as kv_append of the
+        same tokens (the library runs it with a bulk quantiser)."""
+        self.append(layer, k, v)
+
+    def _fold_sinks(self, layer: int, k, v) -> None:
+        """KVSink: fold the call's tokens (keys rotated like every stored key)
+        into each sequence's running top-k before any of its groups is
+        quantised (kvsink.admit); new members' K/V rows go to the sink rows."""
         st, cfg = self.layers[layer], self.cfg
-        if not self._capacity_ok(st, k.shape[2]):
-            raise OverflowError("capacity")
-        if cfg.rope_base:
-            k = rope.rotate_keys(k, st.L, cfg.rope_base, cfg.act_dtype)
-        if cfg.n_dyn_sinks:
-            if st.L != 0:
-                raise RuntimeError("KVSink selection runs once, on an empty cache")
-            m = kvsink.key_norms(k)
-            pos = kvsink.top_k(m, cfg.n_dyn_sinks)
-            st.sink_pos = pos
-            for b in range(cfg.batch):
-                st.sink_k[b, :, :pos.shape[1]] = k[b][:, pos[b]]
-                st.sink_v[b, :, :pos.shape[1]] = v[b][:, pos[b]]
-        self._append_rotated(layer, k, v)
+        if not cfg.n_dyn_sinks:
+            return
+        L0 = st.L
+        q0 = self.q_end(layer)
+        m = kvsink.key_norms(k)
+        old_pos = st.sink_pos if st.sink_pos is not None else np.zeros((cfg.batch, 0), np.int64)
+        old_m = st.sink_m if st.sink_m is not None else np.zeros((cfg.batch, 0), np.float32)
+        new = [kvsink.admit(list(zip(old_pos[b].tolist(), old_m[b].tolist())), m[b], L0, q0,
+                            cfg.n_dyn_sinks) for b in range(cfg.batch)]
+        n = len(new[0])
+        pos = np.array([[p for p, _ in nb] for nb in new], np.int64).reshape(cfg.batch, n)
+        sk = np.zeros_like(st.sink_k)
+        sv = np.zeros_like(st.sink_v)
+        for b in range(cfg.batch):
+            for j, p in enumerate(pos[b]):
+                if p >= L0:   # a token of this call
+                    sk[b, :, j] = k[b, :, p - L0]
+                    sv[b, :, j] = v[b, :, p - L0]
+                else:         # a member kept from before
+                    i = int(np.nonzero(old_pos[b] == p)[0][0])
+                    sk[b, :, j] = st.sink_k[b, :, i]
+                    sv[b, :, j] = st.sink_v[b, :, i]
+        st.sink_k, st.sink_v = sk, sv
+        st.sink_pos = pos
+        st.sink_m = np.array([[mm for _, mm in nb] for nb in new], np.float32).reshape(cfg.batch, n)
 
     def _append_rotated(self, layer: int, k, v) -> None:
         st, cfg = self.layers[layer], self.cfg

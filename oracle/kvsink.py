@@ -16,8 +16,15 @@ Readings where the page is silent:
     the Hkv head norms in head order, divided by Hkv (float32 division).
   * The top-k is per batch element (per sequence), ordered by norm
     descending, ties to the lower position.
-  * Selection runs once, over the tokens of the prefill call, when the cache
-    is empty; the set then stays fixed for the rest of the sequence.
+  * The running top-k is folded call by call (every append and prefill, the
+    page's "on every update_and_fetch"): the candidates are the call's tokens
+    and the sinks whose group was not yet quantised when the call began; a
+    sink whose group is already quantised is locked (its codes hold a
+    substitute's values, its fp16 row is its only faithful copy, and the
+    page never restores a quantised token), so it neither leaves the set nor
+    yields its place. The set is the locked sinks plus the best
+    min(k, L) - locked candidates. On an empty cache one call is the plain
+    top-k over its tokens.
   * Sink K AND V rows are kept exact and replaced, in their group, by the
     nearest non-sink row of the SAME group (nearest by position, ties to the
     earlier row). A group with no non-sink row is left as it is.
@@ -50,6 +57,25 @@ def top_k(m: np.ndarray, k: int, first_pos: int = 0) -> np.ndarray:
         order = np.lexsort((np.arange(T), -m[b].astype(np.float32)))
         out[b] = np.sort(order[:kk].astype(np.int64)) + first_pos
     return out
+
+
+def admit(members: list, m_call: np.ndarray, first_pos: int, q0: int, k: int) -> list:
+    """One call's fold of one sequence into the running top-k.
+
+    members: [(pos, m)] of the set before the call; m_call: float32 [n] norms
+    of the call's tokens at positions first_pos .. first_pos + n - 1; q0: the
+    end of the quantised groups when the call began (members below it are
+    locked). Returns the new set [(pos, m)] sorted by position, of size
+    min(k, first_pos + n).
+    """
+    n = len(m_call)
+    locked = [(p, m) for p, m in members if p < q0]
+    cand = [(p, m) for p, m in members if p >= q0]
+    cand += [(first_pos + i, np.float32(m_call[i])) for i in range(n)]
+    budget = min(k, first_pos + n) - len(locked)
+    # norm descending, ties to the lower position
+    cand.sort(key=lambda pm: (-float(pm[1]), pm[0]))
+    return sorted(locked + cand[:max(budget, 0)])
 
 
 def substitutes(sink_rows: set, n: int = 32) -> dict:

@@ -149,9 +149,105 @@ def test_key_norm_is_mean_over_heads():
     assert np.array_equal(kvsink.key_norms(k)[0], np.array([0.0, 3.0, 0.0], np.float32))
 
 
-def test_selection_only_on_empty_cache():
-    k, v, _ = _setup(6, T=64)
-    c = _cache(5)
-    c.prefill_quantize(0, k, v)
-    with pytest.raises(RuntimeError):
-        c.prefill_quantize(0, k, v)
+def _normed_rows(norms, B=1, H=2, D=128, seed=0):
+    """K rows whose key norm (every head) is exactly the given value (one
+    nonzero channel), and N(0,1) V rows: float32 [B, H, T, D]."""
+    T = len(norms)
+    k = np.zeros((B, H, T, D), np.float32)
+    k[:, :, :, 0] = np.asarray(norms, np.float32)[None, None, :]
+    v = np.random.default_rng(seed).standard_normal((B, H, T, D)).astype(np.float16).astype(np.float32)
+    return k, v
+
+
+def _masks(c):
+    ex = c.export(0)
+    return [int(x) for x in ex["sink_mask"][0]] if "sink_mask" in ex else []
+
+
+def test_running_admission_one_token_per_call():
+    """k = 2, one token per call. While group 0 is open every member can be
+    displaced: 3 (norm 5) displaces 1, 10 (9) displaces 0, 20 (7) displaces
+    3; a later token of equal norm never displaces (ties to the lower
+    position). Group 0 is quantised when token 31 arrives: from then on 10 and
+    20 are locked and 33 (norm 8) is not admitted."""
+    norms = [1.0] * 40
+    norms[3], norms[10], norms[20], norms[33] = 5.0, 9.0, 7.0, 8.0
+    k, v = _normed_rows(norms)
+    c = _cache(2, B=1, H=2)
+    want = {0: [0], 1: [0, 1], 2: [0, 1], 3: [0, 3], 9: [0, 3], 10: [3, 10], 19: [3, 10],
+            20: [10, 20], 31: [10, 20], 32: [10, 20], 33: [10, 20], 39: [10, 20]}
+    for t in range(40):
+        c.append(0, k[:, :, t:t + 1], v[:, :, t:t + 1])
+        if t in want:
+            assert c.sink_positions(0)[0].tolist() == want[t], t
+    ex = c.export(0)
+    assert _masks(c) == [(1 << 10) | (1 << 20)]
+    assert np.array_equal(ex["sink_k"][0], k[0][:, [10, 20]])
+    assert np.array_equal(ex["sink_v"][0], v[0][:, [10, 20]])
+
+
+def test_running_admission_calls_across_groups():
+    """k = 2 with calls of several tokens. The prefill of 40 tokens takes 35
+    (norm 7) and 5 (6); group 0 is quantised in that call, locking 5. Token
+    40 (9) displaces 35, which is still in the residual and is later
+    quantised as an ordinary row. The call of 41..64 holds 60 (9), which ties
+    40 and loses to the lower position; its group 1 is quantised with 40 as
+    its sink. Token 65 (20) finds both members locked."""
+    norms = [1.0] * 66
+    norms[5], norms[35], norms[40], norms[50], norms[60], norms[65] = 6.0, 7.0, 9.0, 8.0, 9.0, 20.0
+    k, v = _normed_rows(norms, seed=1)
+    c = _cache(2, B=1, H=2)
+    c.prefill_quantize(0, k[:, :, :40], v[:, :, :40])
+    assert c.sink_positions(0)[0].tolist() == [5, 35]
+    assert _masks(c) == [1 << 5]
+    c.append(0, k[:, :, 40:41], v[:, :, 40:41])
+    assert c.sink_positions(0)[0].tolist() == [5, 40]
+    c.append(0, k[:, :, 41:65], v[:, :, 41:65])
+    assert c.sink_positions(0)[0].tolist() == [5, 40]
+    assert _masks(c) == [1 << 5, 1 << 8]
+    c.append(0, k[:, :, 65:66], v[:, :, 65:66])
+    assert c.sink_positions(0)[0].tolist() == [5, 40]
+    # the displaced 35 reads back from its quantised group like any other row
+    pos, K, V, pool = c.read_set(0, 0, 0)
+    i35 = int(np.nonzero(pos == 35)[0][0])
+    assert pool[i35] == 1
+
+
+def test_running_admission_is_plain_top_k_while_nothing_is_locked():
+    """Brute force: calls of random sizes inside the first group (no group is
+    quantised, so nothing is locked) leave exactly the top-k of every token so
+    far."""
+    rng = np.random.default_rng(7)
+    for trial in range(20):
+        kk = int(rng.integers(1, 6))
+        norms = rng.integers(1, 9, 31).astype(np.float32)   # many ties
+        k, v = _normed_rows(norms, seed=trial)
+        c = _cache(kk, B=1, H=2)
+        t = 0
+        while t < 31:
+            n = int(rng.integers(1, 6))
+            c.append(0, k[:, :, t:t + n], v[:, :, t:t + n])
+            t = min(31, t + n)
+            want = kvsink.top_k(kvsink.key_norms(k[:, :, :t]), kk)[0].tolist()
+            assert c.sink_positions(0)[0].tolist() == want, (trial, t)
+
+
+def test_running_admission_invariants():
+    """Over many groups with random calls: the set holds min(k, L) members,
+    a member below the quantised end never leaves, and every member's rows
+    are its own."""
+    rng = np.random.default_rng(3)
+    norms = rng.integers(1, 50, 300).astype(np.float32)
+    k, v = _normed_rows(norms, seed=3)
+    c = _cache(4, B=1, H=2)
+    t, prev_locked = 0, set()
+    while t < 300:
+        n = int(rng.integers(1, 40))
+        c.append(0, k[:, :, t:t + n], v[:, :, t:t + n])
+        t = min(300, t + n)
+        sp = c.sink_positions(0)[0].tolist()
+        assert len(sp) == min(4, t)
+        assert prev_locked <= set(sp)
+        prev_locked = {p for p in sp if p < c.q_end(0)}
+        ex = c.export(0)
+        assert np.array_equal(ex["sink_k"][0], k[0][:, sp])
