@@ -168,6 +168,8 @@ Geometry make_geometry(const kv_cache_config* c) {
   lo = align256(lo + B * H * g.n_sink_slots * D * 2);
   g.l_sink_pos = lo;
   lo = align256(lo + B * kMaxSinks * 8);
+  g.l_sink_m = lo;
+  lo = align256(lo + B * kMaxSinks * 4);
   g.l_sink_mask = lo;
   lo = align256(lo + B * static_cast<size_t>(g.n_slots) * 4);
   g.layer_bytes = lo;
@@ -185,6 +187,7 @@ kvq::LayerDev layer_dev(const kv_cache* c, int layer) {
   d.sink_k = reinterpret_cast<uint16_t*>(base + g.l_sink_k);
   d.sink_v = reinterpret_cast<uint16_t*>(base + g.l_sink_v);
   d.sink_pos = reinterpret_cast<int64_t*>(base + g.l_sink_pos);
+  d.sink_m = reinterpret_cast<float*>(base + g.l_sink_m);
   d.sink_mask = reinterpret_cast<uint32_t*>(base + g.l_sink_mask);
   return d;
 }
@@ -229,9 +232,10 @@ kv_status do_append(kv_cache* c, int layer, const void* k, const void* v, int n,
   if (L1 - first > g.max_tokens)
     return fail(KV_ERR_CAPACITY, "append exceeds max_tokens (evict first or raise max_tokens)");
   if (g.rope_max_pos && L1 > g.rope_max_pos) return fail(KV_ERR_CAPACITY, "position beyond rope_max_pos");
-  const bool select = prefill && g.n_dyn > 0;
-  if (select && (L0 != 0 || ls.dyn_selected))
-    return fail(KV_ERR_STATE, "KVSink selection runs once, on an empty layer");
+  // KVSink: every call (append or prefill) folds its tokens into the
+  // running top-k before its groups are quantised
+  const bool select = g.n_dyn > 0;
+  (void)prefill;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   kvq::AppendArgs a{};
@@ -250,7 +254,7 @@ kv_status do_append(kv_cache* c, int layer, const void* k, const void* v, int n,
   cudaError_t e = cudaSuccess;
   int n_sel = ls.n_dyn_sel;
   if (select) {
-    n_sel = std::min(g.n_dyn, n);
+    n_sel = static_cast<int>(std::min<int64_t>(g.n_dyn, L1));
     kvq::SinkSelectArgs sa{};
     sa.geo = g;
     sa.lay = a.lay;
@@ -261,7 +265,11 @@ kv_status do_append(kv_cache* c, int layer, const void* k, const void* v, int n,
     sa.cand_m = reinterpret_cast<float*>(c->arena + g.off_cand_m);
     sa.cand_p = reinterpret_cast<int64_t*>(c->arena + g.off_cand_p);
     sa.n_chunks = (n + 1023) / 1024;
-    sa.k_sel = n_sel;
+    sa.k_sel = std::min(g.n_dyn, n);
+    sa.L0 = L0;
+    sa.q0 = q0;
+    sa.n_old = ls.n_dyn_sel;
+    sa.k_total = n_sel;
     e = kvq::launch_sink_select(sa, s, &launches);
     if (e == cudaSuccess) {
       a.n_dyn_sel = n_sel;
@@ -632,25 +640,42 @@ kv_status kv_cache_export(kv_cache* cache, int layer, int what, void* host_dst, 
   uint8_t* dst = static_cast<uint8_t*>(host_dst);
   auto d2h = [&](void* h, const void* dv, size_t n) { return cudaMemcpy(h, dv, n, cudaMemcpyDeviceToHost); };
 
+  // the sink slots of each sequence in position order (KVSink slots are
+  // filled in admission order; overlay sink j sits in slot j)
+  std::vector<int64_t> pos(static_cast<size_t>(B) * kMaxSinks);
+  std::vector<int> order(static_cast<size_t>(B) * kMaxSinks);
+  if (what == KV_EXPORT_SINK_POS || what == KV_EXPORT_SINK_K || what == KV_EXPORT_SINK_V) {
+    if (g.n_dyn) {
+      e = d2h(pos.data(), d.sink_pos, pos.size() * 8);
+    } else {
+      for (int64_t b = 0; b < B; ++b)
+        for (int64_t j = 0; j < p.S; ++j) pos[b * kMaxSinks + j] = j;
+    }
+    for (int64_t b = 0; b < B; ++b) {
+      int* ob = order.data() + b * kMaxSinks;
+      for (int j = 0; j < p.S; ++j) ob[j] = j;
+      const int64_t* pb = pos.data() + b * kMaxSinks;
+      std::sort(ob, ob + p.S, [pb](int x, int y) { return pb[x] < pb[y]; });
+    }
+  }
+
   switch (what) {
     case KV_EXPORT_SINK_POS: {
-      std::vector<int64_t> pos(static_cast<size_t>(B) * kMaxSinks);
-      if (g.n_dyn) {
-        e = d2h(pos.data(), d.sink_pos, pos.size() * 8);
-      } else {
-        for (int64_t b = 0; b < B; ++b)
-          for (int64_t j = 0; j < p.S; ++j) pos[b * kMaxSinks + j] = j;
-      }
       int64_t* o = reinterpret_cast<int64_t*>(dst);
       for (int64_t b = 0; b < B; ++b)
-        for (int64_t j = 0; j < p.S; ++j) o[b * p.S + j] = pos[b * kMaxSinks + j];
+        for (int64_t j = 0; j < p.S; ++j) o[b * p.S + j] = pos[b * kMaxSinks + order[b * kMaxSinks + j]];
       break;
     }
     case KV_EXPORT_SINK_K:
     case KV_EXPORT_SINK_V: {
       const uint16_t* src = what == KV_EXPORT_SINK_K ? d.sink_k : d.sink_v;
-      for (int64_t bh = 0; bh < B * H && e == cudaSuccess; ++bh)
-        e = d2h(dst + bh * p.S * D * 2, src + bh * g.n_sink_slots * D, p.S * D * 2);
+      std::vector<uint16_t> rows(static_cast<size_t>(g.n_sink_slots) * D);
+      for (int64_t bh = 0; bh < B * H && e == cudaSuccess; ++bh) {
+        e = d2h(rows.data(), src + bh * g.n_sink_slots * D, rows.size() * 2);
+        const int* ob = order.data() + (bh / H) * kMaxSinks;
+        for (int64_t j = 0; j < p.S; ++j)
+          std::memcpy(dst + (bh * p.S + j) * D * 2, rows.data() + static_cast<size_t>(ob[j]) * D, D * 2);
+      }
       break;
     }
     case KV_EXPORT_TAIL_K:

@@ -17,7 +17,8 @@ struct LayerDev {
   uint16_t* tail_v;
   uint16_t* sink_k;     // [B][H][n_sink_slots][D]
   uint16_t* sink_v;
-  int64_t* sink_pos;    // [B][kMaxSinks]
+  int64_t* sink_pos;    // [B][kMaxSinks] absolute positions of the sink set (slot order)
+  float* sink_m;        // [B][kMaxSinks] their key norms
   uint32_t* sink_mask;  // [B][n_slots]
 };
 
@@ -87,7 +88,11 @@ struct SinkSelectArgs {
   float* cand_m;        // [B][n_chunks][kMaxSinks]
   int64_t* cand_p;
   int n_chunks;
-  int k_sel;            // sinks to select
+  int k_sel;            // candidates kept per chunk: min(k, n)
+  int64_t L0;           // position of the call's first token
+  int64_t q0;           // end of the quantised groups when the call began
+  int n_old;            // members before the call (slots 0 .. n_old - 1)
+  int k_total;          // members after the call: min(k, L0 + n)
 };
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int64_t* launches);

@@ -153,7 +153,7 @@ struct Geometry {
   size_t off_err, off_rope, off_signs, off_cbk, off_cbv, off_part_o, off_part_ml;
   size_t off_norms, off_cand_m, off_cand_p, n_cand_chunks;
   size_t off_layers, layer_bytes;
-  size_t l_chunks, l_tail_k, l_tail_v, l_sink_k, l_sink_v, l_sink_pos, l_sink_mask;
+  size_t l_chunks, l_tail_k, l_tail_v, l_sink_k, l_sink_v, l_sink_pos, l_sink_m, l_sink_mask;
   size_t total;
 };
 

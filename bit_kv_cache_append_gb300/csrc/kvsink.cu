@@ -1,7 +1,9 @@
 // KVSink-style sink selection (VeloxQuant-MLX "KVSink-Adapted Sink
 // Protection", "How it works" 1): the per-token key L2 norm averaged over the
-// KV heads, and the top-k positions per sequence (norm descending, ties to the
-// lower position).
+// KV heads, folded call by call into a running top-k of positions per
+// sequence (norm descending, ties to the lower position). A sink whose group
+// is already quantised stays (the page never restores a quantised token, and
+// its codes hold a substitute's values).
 #include "kvq_device.cuh"
 
 namespace kvq {
@@ -118,27 +120,66 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(SinkSelectArgs
   block_topk(m, p, a.k_sel, a.cand_m + o, a.cand_p + o);
 }
 
-// Pass 2: the top k over the chunk winners of one sequence, by k rounds of a
-// block-wide arg-best over the candidate array (each winner is struck out in
-// place), stored in ascending position order as the sink set.
-__global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(SinkSelectArgs a) {
+// Pass 2, one CTA per sequence: the running top-k after the call. Members
+// whose position lies below q0 (their group was quantised before the call)
+// are locked and keep their slots. The other members and the chunk winners
+// of the call compete for the remaining k_total - locked places by rounds of
+// a block-wide arg-best (each winner struck out in place): a member that
+// wins keeps its slot, the call's winners take the freed slots and then the
+// new ones, in rank order. Slots are not kept in position order; only the
+// set matters to the readers.
+__global__ void __launch_bounds__(kTopkThreads) sink_update_kernel(SinkSelectArgs a) {
   const int b = blockIdx.x;
-  __shared__ int64_t fp[kMaxSinks];
+  __shared__ int64_t win_p[kMaxSinks];
+  __shared__ float win_m[kMaxSinks];
+  __shared__ int64_t un_p[kMaxSinks];   // unlocked members: candidates (struck out in place)
+  __shared__ float un_m[kMaxSinks];
+  __shared__ int un_slot[kMaxSinks];
+  __shared__ int keep[kMaxSinks];
+  __shared__ int n_un, n_lock;
   __shared__ float wm[kTopkThreads / 32];
   __shared__ int64_t wp[kTopkThreads / 32];
   __shared__ int wc[kTopkThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t* spos = a.lay.sink_pos + static_cast<size_t>(b) * kMaxSinks;
+  float* sm = a.lay.sink_m + static_cast<size_t>(b) * kMaxSinks;
+  if (threadIdx.x == 0) {
+    int nu = 0, nl = 0;
+    for (int j = 0; j < a.n_old; ++j) {
+      const bool locked = spos[j] < a.q0;
+      keep[j] = locked ? 1 : 0;
+      if (locked) {
+        ++nl;
+      } else {
+        un_p[nu] = spos[j];
+        un_m[nu] = sm[j];
+        un_slot[nu] = j;
+        ++nu;
+      }
+    }
+    n_un = nu;
+    n_lock = nl;
+  }
+  __syncthreads();
+  const int budget = a.k_total - n_lock;
   const int n_cand = a.n_chunks * kMaxSinks;
   float* cm_base = a.cand_m + static_cast<size_t>(b) * n_cand;
-  int64_t* cp_base = a.cand_p + static_cast<size_t>(b) * n_cand;
-  for (int round = 0; round < a.k_sel; ++round) {
+  int64_t* cp_base = a.cand_p + static_cast<size_t>(b) * n_cand;  // call-relative positions
+  for (int round = 0; round < budget; ++round) {
     float bm = -INFINITY;
     int64_t bp = INT64_MAX;
     int bc = -1;
-    for (int c = threadIdx.x; c < n_cand; c += kTopkThreads) {
-      if (c % kMaxSinks >= a.k_sel) continue;
-      const float m = cm_base[c];
-      const int64_t p = cp_base[c];
+    for (int c = threadIdx.x; c < n_cand + n_un; c += kTopkThreads) {
+      float m;
+      int64_t p;
+      if (c < n_cand) {
+        if (c % kMaxSinks >= a.k_sel) continue;
+        m = cm_base[c];
+        p = cp_base[c] == INT64_MAX ? INT64_MAX : cp_base[c] + a.L0;
+      } else {
+        m = un_m[c - n_cand];
+        p = un_p[c - n_cand];
+      }
       if (better(m, p, bm, bp)) { bm = m; bp = p; bc = c; }
     }
 #pragma unroll
@@ -156,19 +197,36 @@ __global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(SinkSelectArgs
       int xc = wc[0];
       for (int w = 1; w < kTopkThreads / 32; ++w)
         if (better(wm[w], wp[w], xm, xp)) { xm = wm[w]; xp = wp[w]; xc = wc[w]; }
-      fp[round] = xp;
-      if (xc >= 0) { cm_base[xc] = -INFINITY; cp_base[xc] = INT64_MAX; }
+      win_m[round] = xm;
+      win_p[round] = xp;
+      if (xc >= 0 && xc < n_cand) { cm_base[xc] = -INFINITY; cp_base[xc] = INT64_MAX; }
+      else if (xc >= n_cand) { un_m[xc - n_cand] = -INFINITY; un_p[xc - n_cand] = INT64_MAX; }
     }
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    for (int i = 1; i < a.k_sel; ++i) {  // ascending by position
-      const int64_t x = fp[i];
-      int j = i - 1;
-      while (j >= 0 && fp[j] > x) { fp[j + 1] = fp[j]; --j; }
-      fp[j + 1] = x;
+    // winning members keep their slots
+    for (int i = 0; i < n_un; ++i) {
+      const int j = un_slot[i];
+      const int64_t p = spos[j];
+      for (int r = 0; r < budget; ++r)
+        if (win_p[r] == p) {
+          keep[j] = 1;
+          win_p[r] = -1;
+          break;
+        }
     }
-    for (int i = 0; i < a.k_sel; ++i) a.lay.sink_pos[b * kMaxSinks + i] = fp[i];
+    // the call's winners fill the freed slots, then the new ones
+    int r = 0;
+    for (int j = 0; j < a.k_total; ++j) {
+      if (j < a.n_old && keep[j]) continue;
+      while (r < budget && win_p[r] < 0) ++r;
+      if (r < budget) {
+        spos[j] = win_p[r];
+        sm[j] = win_m[r];
+        ++r;
+      }
+    }
   }
 }
 
@@ -180,7 +238,7 @@ cudaError_t launch_sink_select(const SinkSelectArgs& a, cudaStream_t s, int64_t*
   else keynorm_kernel<64><<<g1, 128, 0, s>>>(a);
   dim3 g2(a.n_chunks, a.geo.B);
   topk_chunk_kernel<<<g2, kTopkThreads, 0, s>>>(a);
-  topk_final_kernel<<<a.geo.B, kTopkThreads, 0, s>>>(a);
+  sink_update_kernel<<<a.geo.B, kTopkThreads, 0, s>>>(a);
   *launches += 3;
   return cudaGetLastError();
 }

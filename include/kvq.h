@@ -138,21 +138,27 @@ kv_status kv_cache_reset(kv_cache* cache);
  * (KIVI: K per channel over the group, V per token over 32-channel groups,
  * min/max affine codes, P1 "Affine quantisation formula"; TurboQuant: every
  * token at once, P2 "Algorithm Detail"); the rest waits in the exact tail.
- * Positions below n_sink are also copied to the sink buffer. Errors:
- * KV_ERR_CAPACITY when the retained span would exceed max_tokens (or the RoPE
- * table), nothing enqueued.
+ * Positions below n_sink are also copied to the sink buffer. When
+ * n_dyn_sinks > 0 (KVSink, P4 "How it works" 1-3), the call first folds its
+ * tokens into each sequence's running top-k of key norms (the L2 norm of
+ * each head's key averaged over the KV heads; norm descending, ties to the
+ * lower position): the candidates are the call's tokens and the sinks whose
+ * group was still unquantised when the call began; sinks in quantised
+ * groups are locked (P4 "Known v1 limitation": a token quantised in an
+ * earlier call is never restored), and the set holds min(n_dyn_sinks, L)
+ * positions. Sink K/V rows are stored exact, and in every group quantised
+ * afterwards each sink row is replaced by its nearest non-sink row of the
+ * group before min/max calibration. Errors: KV_ERR_CAPACITY when the
+ * retained span would exceed max_tokens (or the RoPE table), nothing
+ * enqueued.
  */
 kv_status kv_append(kv_cache* cache, int layer, const void* k, const void* v, int n_new,
                     void* cuda_stream);
 
 /*
- * Prefill: the same as kv_append for n_tokens tokens, plus, when
- * n_dyn_sinks > 0, KVSink sink selection first (P4 "How it works" 1-3): the
- * per-token key L2 norm averaged over KV heads, the top n_dyn_sinks
- * positions per sequence (ties to the lower position) stored exact, and in
- * every group each sink row replaced by its nearest non-sink row before
- * min/max calibration. Selection runs once, on an empty layer
- * (KV_ERR_STATE otherwise; P4 "Known v1 limitation").
+ * Prefill: the same state change as kv_append of the same n_tokens tokens
+ * (KVSink selection included: on an empty layer it is the top n_dyn_sinks
+ * positions of the call), run by a bulk quantiser sized for long inputs.
  */
 kv_status kv_prefill_quantize(kv_cache* cache, int layer, const void* k, const void* v,
                               int n_tokens, void* cuda_stream);

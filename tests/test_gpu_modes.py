@@ -168,3 +168,72 @@ def test_kvsink_ties_and_residual_sinks():
     assert list(gc.export(0, "sink_pos")[0]) == [7, 40, 70]
     compare_exports(gc, oc, 0)
     _decode_both(gc, oc, 0, W.queries(w, 1), "f16")
+
+
+def _sink_rows_with_norms(norms, B, H, D=128, seed=0):
+    """N(0,1) K/V rows (fp16 values) whose listed positions get their K row
+    scaled so that its norm dominates: {pos: factor}."""
+    rng = np.random.default_rng(seed)
+    T = max(norms) + 1 if isinstance(norms, dict) else len(norms)
+    k = rng.standard_normal((B, H, T, D)).astype(np.float16).astype(np.float32)
+    v = rng.standard_normal((B, H, T, D)).astype(np.float16).astype(np.float32)
+    for p, f in norms.items():
+        k[:, :, p] = (k[:, :, p] * f).astype(np.float16).astype(np.float32)
+    return k, v
+
+
+def test_kvsink_running_admission_one_token_per_call():
+    """A prefill of 50 tokens leaves two of its three sinks in the open group
+    (35, 45) and locks 5. Single-token calls then displace the weakest open
+    sink when they beat it (55 displaces 45; 60 loses to 35); once group 1 is
+    quantised every sink is locked and 70, the largest key of all, stays out.
+    The set, rows, masks and codes equal the oracle's after every call, and
+    attention along the way."""
+    import torch
+    w = W.scaled(W.WORKLOADS["kvsink"], batch=2, n_kv_heads=2, n_q_heads=8, context=160)
+    kw = cache_kwargs(w, 512, n_dyn_sinks=3)
+    gc, oc = _pair(kw)
+    k, v = _sink_rows_with_norms({5: 25.0, 35: 20.0, 45: 15.0, 55: 30.0, 60: 18.0, 70: 40.0, 159: 1.0},
+                                 2, 2, seed=4)
+    gc.prefill_quantize(0, torch_act(k[:, :, :50], "f16"), torch_act(v[:, :, :50], "f16"))
+    oc.prefill_quantize(0, k[:, :, :50], v[:, :, :50])
+    assert gc.export(0, "sink_pos").tolist() == [[5, 35, 45]] * 2
+    compare_exports(gc, oc, 0)
+    for t in range(50, 160):
+        gc.append(0, torch_act(k[:, :, t:t + 1], "f16"), torch_act(v[:, :, t:t + 1], "f16"))
+        oc.append(0, k[:, :, t:t + 1], v[:, :, t:t + 1])
+        assert np.array_equal(gc.export(0, "sink_pos"), oc.export(0)["sink_pos"]), t
+        if t % 23 == 0 or t in (55, 63, 64, 159):
+            compare_exports(gc, oc, 0)
+            _decode_both(gc, oc, 0, W.queries(w, t), "f16")
+    assert gc.export(0, "sink_pos").tolist() == [[5, 35, 55]] * 2
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("k_dyn", [1, 5])
+def test_kvsink_running_admission_calls_across_groups(k_dyn):
+    """Calls of random sizes (many spanning a group boundary, prefills among
+    them) over planted high-norm rows whose norm grows with the position, so
+    that later calls keep displacing the sinks still in an open group: sink
+    sets, rows, masks and codes equal the oracle's after every call;
+    attention at the end."""
+    w = W.scaled(W.WORKLOADS["kvsink"], batch=2, n_kv_heads=2, n_q_heads=8, context=1200)
+    kw = cache_kwargs(w, 2048, n_dyn_sinks=k_dyn)
+    gc, oc = _pair(kw)
+    rng = np.random.default_rng(11 + k_dyn)
+    planted = {int(p): 3.0 + 27.0 * p / 1200 for p in rng.choice(1200, 60, replace=False)}
+    planted[1199] = 1.0
+    k, v = _sink_rows_with_norms(planted, 2, 2, seed=k_dyn)
+    t = 0
+    while t < 1200:
+        n = int(rng.choice([1, 2, 7, 33, 45, 70, 300]))
+        n = min(n, 1200 - t)
+        if n >= 300:
+            gc.prefill_quantize(0, torch_act(k[:, :, t:t + n], "f16"), torch_act(v[:, :, t:t + n], "f16"))
+            oc.prefill_quantize(0, k[:, :, t:t + n], v[:, :, t:t + n])
+        else:
+            gc.append(0, torch_act(k[:, :, t:t + n], "f16"), torch_act(v[:, :, t:t + n], "f16"))
+            oc.append(0, k[:, :, t:t + n], v[:, :, t:t + n])
+        t += n
+        compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 5), "f16")
