@@ -85,12 +85,12 @@ def validate(cfg: CacheConfig) -> None:
         raise ValueError("head_dim must be 64 or 128")
     if cfg.mode == "kivi":
         for b in (cfg.k_bits, cfg.v_bits):
-            if b not in (2, 4, 8):
-                raise ValueError("KIVI bits must be 2, 4 or 8")
+            if b not in (2, 3, 4, 8):
+                raise ValueError("KIVI bits must be 2, 3, 4 or 8")
     elif cfg.mode == "turboquant":
         for b in (cfg.k_bits, cfg.v_bits):
-            if b not in (2, 4):
-                raise ValueError("TurboQuant bits must be 2 or 4")
+            if b not in (2, 3, 4):
+                raise ValueError("TurboQuant bits must be 2, 3 or 4")
         if cfg.n_dyn_sinks:
             raise ValueError("KVSink sinks are defined on KIVI groups only")
     else:
@@ -414,7 +414,8 @@ class OracleCache:
         n_tail = B * (L - F)
         n_evicted = B * (E - cfg.n_sink)
         row16 = 2 * D * 2                     # K + V row of a 16-bit dtype
-        code = D * (cfg.k_bits + cfg.v_bits) // 8
+        # stored bytes: 8 // bits codes per byte (3-bit codes two to a byte)
+        code = D // (8 // cfg.k_bits) + D // (8 // cfg.v_bits)
         if cfg.mode == "kivi":
             g_lo, g_hi = lo // GROUP, (F + GROUP - 1) // GROUP
             n_kgroups = max(0, g_hi - g_lo) if F > lo else 0

@@ -38,8 +38,8 @@ FP16_MAX = 65504.0
 
 def levels(bits: int) -> int:
     """Largest unsigned code, 2^b - 1 (qMax - qMin of the signed form)."""
-    if bits not in (2, 4, 8):
-        raise ValueError(f"KIVI bit width must be 2, 4 or 8, got {bits}")
+    if bits not in (2, 3, 4, 8):
+        raise ValueError(f"KIVI bit width must be 2, 3, 4 or 8, got {bits}")
     return (1 << bits) - 1
 
 
@@ -110,9 +110,12 @@ def dequantize_v_rows(codes, s_h, z_h) -> np.ndarray:
 
 
 def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
-    """Pack codes along the last axis, v0 in the least-significant bits.
+    """Pack codes along the last axis, v0 in the least-significant bits,
+    8 // bits codes per byte (Foundry spec, "Step 3: Packing": 2-bit
+    [v0:2][v1:2][v2:2][v3:2], 3-bit [v0:3][v1:3][__:2] with two bits unused,
+    4-bit [v0:4][v1:4]; 8-bit one code per byte).
 
-    codes: uint8 [..., D] with values < 2^bits. Returns uint8 [..., D*bits/8].
+    codes: uint8 [..., D] with values < 2^bits. Returns uint8 [..., D / (8 // bits)].
     """
     per = 8 // bits
     D = codes.shape[-1]

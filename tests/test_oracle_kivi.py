@@ -7,7 +7,7 @@ import pytest
 
 from oracle import kivi
 
-BITS = (2, 4, 8)
+BITS = (2, 3, 4, 8)
 
 
 def _fp16_values(rng, shape, scale=1.0):
@@ -136,13 +136,16 @@ def test_pack_unpack_every_level(bits):
     codes = np.array([(i * 7 + 3) % (lb + 1) for i in range(4 * 256)], np.uint8).reshape(4, 256)
     codes[0, : lb + 1] = np.arange(lb + 1)
     packed = kivi.pack_codes(codes, bits)
-    assert packed.shape == (4, codes.shape[1] * bits // 8)
+    assert packed.shape == (4, codes.shape[1] // per)
     assert np.array_equal(kivi.unpack_codes(packed, bits), codes)
 
 
 def test_pack_layout_v0_in_low_bits():
-    """Foundry spec, "Step 3: Packing": [v0:2][v1:2][v2:2][v3:2] and
-    [v0:4][v1:4], read with v0 in the least-significant bits."""
+    """Foundry spec, "Step 3: Packing": [v0:2][v1:2][v2:2][v3:2],
+    [v0:3][v1:3][__:2] (two bits unused) and [v0:4][v1:4], read with v0 in
+    the least-significant bits."""
     assert kivi.pack_codes(np.array([[1, 2, 3, 0]], np.uint8), 2)[0, 0] == 0b00111001
+    assert kivi.pack_codes(np.array([[5, 6]], np.uint8), 3)[0, 0] == 0b00110101
+    assert kivi.pack_codes(np.array([[7, 7, 0, 1]], np.uint8), 3).tolist() == [[0b00111111, 0b00001000]]
     assert kivi.pack_codes(np.array([[0xA, 0x5]], np.uint8), 4)[0, 0] == 0x5A
     assert list(kivi.pack_codes(np.array([[7, 200]], np.uint8), 8)[0]) == [7, 200]

@@ -86,7 +86,7 @@ def test_codebook_one_bit_closed_form(a):
     assert np.allclose(c, [0.5 - off, 0.5 + off], atol=1e-13)
 
 
-@pytest.mark.parametrize("d,bits", [(64, 2), (128, 2), (128, 4), (64, 4)])
+@pytest.mark.parametrize("d,bits", [(64, 2), (128, 2), (128, 3), (64, 3), (128, 4), (64, 4)])
 def test_codebook_lloyd_conditions_by_quadrature(d, bits):
     """Centroid condition (checked with adaptive quadrature of the density, a
     different routine than the oracle's incomplete beta) and midpoint
@@ -106,7 +106,7 @@ def test_codebook_lloyd_conditions_by_quadrature(d, bits):
     assert np.allclose(b, 1.0 - b[::-1], atol=1e-12)
 
 
-@pytest.mark.parametrize("levels_row", [1, 2])
+@pytest.mark.parametrize("levels_row", [1, 2, 3])
 def test_codebook_near_gaussian_lloyd_max(levels_row):
     """For d = 128 the Beta(64, 64) code sits at the Gaussian Lloyd-Max levels
     scaled by its sigma (tests/golden/gaussian_lloyd_max.txt)."""
@@ -122,7 +122,7 @@ def test_codebook_near_gaussian_lloyd_max(levels_row):
 
 def test_codebook_float32_middle_boundary_is_half():
     for d in (64, 128):
-        for bits in (2, 4):
+        for bits in (2, 3, 4):
             b, _ = tq.codebook(d, bits)
             assert b.dtype == np.float32 and b[len(b) // 2] == np.float32(0.5)
 
@@ -138,7 +138,7 @@ def test_zero_vector():
     assert np.all(tq.dequantize(codes, n, sgn, cen) == 0)
 
 
-@pytest.mark.parametrize("bits,row", [(2, 1), (4, 2)])
+@pytest.mark.parametrize("bits,row", [(2, 1), (3, 2), (4, 3)])
 def test_roundtrip_mse_matches_lloyd_max_distortion(bits, row):
     """Relative round-trip MSE of random Gaussian vectors equals the Gaussian
     Lloyd-Max distortion per coordinate (Foundry unit test 1: roundtrip MSE
