@@ -79,11 +79,11 @@ kv_status check_config(const kv_cache_config* c) {
   if (c->group_size != kGroup) return fail(KV_ERR_INVALID_ARG, "group_size must be 32");
   if (c->mode == KV_MODE_KIVI) {
     for (int b : {c->k_bits, c->v_bits})
-      if (b != 2 && b != 4 && b != 8) return fail(KV_ERR_INVALID_ARG, "KIVI bits must be 2, 4 or 8");
+      if (b != 2 && b != 3 && b != 4 && b != 8) return fail(KV_ERR_INVALID_ARG, "KIVI bits must be 2, 3, 4 or 8");
     if (c->residual != kGroup) return fail(KV_ERR_INVALID_ARG, "KIVI residual must be 32 (one group)");
   } else if (c->mode == KV_MODE_TURBOQUANT) {
     for (int b : {c->k_bits, c->v_bits})
-      if (b != 2 && b != 4) return fail(KV_ERR_INVALID_ARG, "TurboQuant bits must be 2 or 4");
+      if (b != 2 && b != 3 && b != 4) return fail(KV_ERR_INVALID_ARG, "TurboQuant bits must be 2, 3 or 4");
     if (c->residual != 0) return fail(KV_ERR_INVALID_ARG, "TurboQuant residual must be 0");
     if (c->n_dyn_sinks) return fail(KV_ERR_INVALID_ARG, "KVSink sinks are defined on KIVI groups only");
   } else {
@@ -127,7 +127,7 @@ Geometry make_geometry(const kv_cache_config* c) {
   g.tail_cap = next_pow2(std::max(c->window, kGroup - 1) + 1);
   g.n_sink_slots = std::max(1, std::max(c->n_sink, c->n_dyn_sinks));
   g.max_splits = c->max_splits ? c->max_splits : 64;
-  g.chunk = kvq::chunk_layout(g.mode_tq, g.D, g.kb, g.vb);
+  g.chunk = kvq::chunk_layout(g.mode_tq, g.D, kvq::storage_bits(g.kb), kvq::storage_bits(g.vb));
   g.rope_max_pos = c->rope_base > 0.0 ? c->rope_max_pos : 0;
 
   const size_t B = g.B, H = g.H, D = g.D;
@@ -530,7 +530,7 @@ kv_status kv_cache_stats(kv_cache* cache, int layer, kv_cache_stats_t* out) {
   out->n_tail = B * (L - F);
   out->n_evicted = B * (E - g.n_sink);
   const int64_t row16 = 2 * D * 2;
-  out->code_bytes = out->n_quant * H * (D * (g.kb + g.vb) / 8);
+  out->code_bytes = out->n_quant * H * (D * (kvq::storage_bits(g.kb) + kvq::storage_bits(g.vb)) / 8);
   if (!g.mode_tq) {
     const int64_t groups = F > lo ? (F + kGroup - 1) / kGroup - lo / kGroup : 0;
     out->kmeta_bytes = groups * B * H * 4 * D;
@@ -570,8 +570,8 @@ kv_status export_size(const kv_cache* c, int layer, int what, size_t* bytes) {
   const size_t B = g.B, H = g.H, D = g.D;
   const bool tq = g.mode_tq;
   switch (what) {
-    case KV_EXPORT_K_CODES: *bytes = B * H * p.n * D * g.kb / 8; return KV_OK;
-    case KV_EXPORT_V_CODES: *bytes = B * H * p.n * D * g.vb / 8; return KV_OK;
+    case KV_EXPORT_K_CODES: *bytes = B * H * p.n * D * kvq::storage_bits(g.kb) / 8; return KV_OK;
+    case KV_EXPORT_V_CODES: *bytes = B * H * p.n * D * kvq::storage_bits(g.vb) / 8; return KV_OK;
     case KV_EXPORT_K_SCALE:
     case KV_EXPORT_K_ZERO:
       if (tq) break;
@@ -724,24 +724,30 @@ kv_status kv_cache_export(kv_cache* cache, int layer, int what, void* host_dst, 
           const int ntok = static_cast<int>(std::min<int64_t>(kGroup, p.T1 - grp * kGroup));
           if (what == KV_EXPORT_K_CODES || what == KV_EXPORT_V_CODES) {
             const bool isk = what == KV_EXPORT_K_CODES;
-            const int bits = isk ? g.kb : g.vb;
-            const int rowb = static_cast<int>(D) * bits / 8;
+            // canonical rows: 8 / bits codes per byte, code c at bit
+            // (c mod per) * bits of byte c / per; storage puts 3-bit codes
+            // in the 4-bit layout
+            const int bits = isk ? g.kb : g.vb, sbits = kvq::storage_bits(bits), per = 8 / bits;
+            const int rowb = static_cast<int>(D) / per;
             uint8_t* o = dst + (bh * p.n + gi * kGroup) * rowb;
             const uint8_t* reg = chunk.data() + (isk ? g.chunk.kc_off : g.chunk.vc_off);
-            if (g.mode_tq) {
+            if (g.mode_tq && sbits == bits) {
               std::memcpy(o, reg, static_cast<size_t>(ntok) * rowb);
+            } else if (g.mode_tq) {  // two 3-bit codes per stored byte, at bits 0 and 4
+              for (int i = 0; i < ntok * rowb; ++i)
+                o[i] = static_cast<uint8_t>((reg[i] & 0x7) | ((reg[i] >> 4) & 0x7) << 3);
             } else {
-              const uint32_t mask = (1u << bits) - 1;
+              const uint32_t mask = (1u << sbits) - 1;
               for (int lane = 0; lane < 32; ++lane)
                 for (int f = 0; f < D; ++f) {
                   int tok, ch, w, bit;
                   if (isk) kvq::k_frag_pos(static_cast<int>(D), lane, f, &tok, &ch);
                   else kvq::v_frag_pos(static_cast<int>(D), lane, f, &tok, &ch);
-                  kvq::frag_bits(bits, f, &w, &bit);
+                  kvq::frag_bits(sbits, f, &w, &bit);
                   uint32_t word;
                   std::memcpy(&word, reg + kvq::code_word_offset(lane, w), 4);
                   const uint32_t code = (word >> bit) & mask;
-                  o[tok * rowb + ch * bits / 8] |= static_cast<uint8_t>(code << ((ch % (8 / bits)) * bits));
+                  o[tok * rowb + ch / per] |= static_cast<uint8_t>(code << ((ch % per) * bits));
                 }
             }
           } else if (what == KV_EXPORT_K_SCALE || what == KV_EXPORT_K_ZERO) {

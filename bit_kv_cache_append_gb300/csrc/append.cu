@@ -114,10 +114,13 @@ __device__ __forceinline__ int word_bit(int i) {
   return 8 * j + 16 * e;
 }
 
+// KB, VB: code widths (levels 2^bits - 1); the codes are packed with their
+// storage widths (a 3-bit code in the 4-bit layout).
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
   constexpr int HALF = D / 2, NV = D / 32, CPR = HALF / 8;
   constexpr int LK = (1 << KB) - 1, LV = (1 << VB) - 1;
+  constexpr int SK = storage_bits(KB), SV = storage_bits(VB);
   // the group's rows as activation-dtype bits (rows padded by 16 bytes so
   // that 16-byte row stores stay aligned and column reads spread over banks)
   __shared__ __align__(16) uint16_t xk[32][D + 8];
@@ -227,8 +230,8 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
   __syncthreads();
 
   // pack in the decode kernel's fragment order (kvq_layout.h)
-  constexpr int KPER = 32 / KB, VPER = 32 / VB;
-  constexpr int KWPL = D * KB / 32, VWPL = D * VB / 32;  // words per lane block
+  constexpr int KPER = 32 / SK, VPER = 32 / SV;
+  constexpr int KWPL = D * SK / 32, VWPL = D * SV / 32;  // words per lane block
   for (int wi = tid; wi < 32 * KWPL; wi += D) {
     const int lane = wi / KWPL, w = wi % KWPL;
     uint32_t word = 0;
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
     for (int i = 0; i < KPER; ++i) {
       int tok, ch;
       k_frag_pos(D, lane, w * KPER + i, &tok, &ch);
-      word |= static_cast<uint32_t>(ck[tok][ch]) << word_bit<KB>(i);
+      word |= static_cast<uint32_t>(ck[tok][ch]) << word_bit<SK>(i);
     }
     *reinterpret_cast<uint32_t*>(chunk + G.chunk.kc_off + code_word_offset(lane, w)) = word;
   }
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
     for (int i = 0; i < VPER; ++i) {
       int tok, ch;
       v_frag_pos(D, lane, w * VPER + i, &tok, &ch);
-      word |= static_cast<uint32_t>(cv[tok][ch]) << word_bit<VB>(i);
+      word |= static_cast<uint32_t>(cv[tok][ch]) << word_bit<SV>(i);
     }
     *reinterpret_cast<uint32_t*>(chunk + G.chunk.vc_off + code_word_offset(lane, w)) = word;
   }
@@ -259,9 +262,10 @@ void launch_flush(const AppendArgs& a, dim3 grid, cudaStream_t s) {
   const int kb = a.geo.kb, vb = a.geo.vb;
 #define KVQ_FLUSH(K, V) \
   if (kb == K && vb == V) { kivi_flush_kernel<D, K, V><<<grid, D, 0, s>>>(a); return; }
-  KVQ_FLUSH(2, 2) KVQ_FLUSH(2, 4) KVQ_FLUSH(2, 8)
-  KVQ_FLUSH(4, 2) KVQ_FLUSH(4, 4) KVQ_FLUSH(4, 8)
-  KVQ_FLUSH(8, 2) KVQ_FLUSH(8, 4) KVQ_FLUSH(8, 8)
+  KVQ_FLUSH(2, 2) KVQ_FLUSH(2, 3) KVQ_FLUSH(2, 4) KVQ_FLUSH(2, 8)
+  KVQ_FLUSH(3, 2) KVQ_FLUSH(3, 3) KVQ_FLUSH(3, 4) KVQ_FLUSH(3, 8)
+  KVQ_FLUSH(4, 2) KVQ_FLUSH(4, 3) KVQ_FLUSH(4, 4) KVQ_FLUSH(4, 8)
+  KVQ_FLUSH(8, 2) KVQ_FLUSH(8, 3) KVQ_FLUSH(8, 4) KVQ_FLUSH(8, 8)
 #undef KVQ_FLUSH
 }
 
@@ -374,12 +378,13 @@ __global__ void __launch_bounds__(128) tq_quantize_kernel(AppendArgs a, int row_
     const float n = which ? tq_code_row<D>(xv, s_signs, s_bv, bits, rsq, codes[warp])
                           : tq_code_row<D>(xk, s_signs, s_bk, bits, rsq, codes[warp]);
     __syncwarp();
-    const int row_words = D * bits / 32, per = 32 / bits;
+    const int sbits = storage_bits(bits);  // 3-bit codes are stored as nibbles
+    const int row_words = D * sbits / 32, per = 32 / sbits;
     uint32_t* dst = reinterpret_cast<uint32_t*>(chunk + (which ? G.chunk.vc_off : G.chunk.kc_off) +
-                                                r * (D * bits / 8));
+                                                r * (D * sbits / 8));
     if (lane < row_words) {
       uint32_t word = 0;
-      for (int i = 0; i < per; ++i) word |= static_cast<uint32_t>(codes[warp][lane * per + i]) << (bits * i);
+      for (int i = 0; i < per; ++i) word |= static_cast<uint32_t>(codes[warp][lane * per + i]) << (sbits * i);
       dst[lane] = word;
     }
     if (lane == 0)

@@ -305,18 +305,17 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
   uint32_t* lut_k = reinterpret_cast<uint32_t*>(smem + T::OFF_LUT);
   uint32_t* lut_v = reinterpret_cast<uint32_t*>(smem + T::OFF_LUT + T::LUTK);
   if constexpr (TQ) {  // value of code c: 2 c[c] - 1 (Foundry TurboQuant spec, "Algorithm Detail")
-    const int nk = 1 << KB, nv = 1 << VB;
+    // KB, VB are the stored field widths; the codebooks have 2^bits levels
+    // (a 3-bit code sits in a 4-bit field, whose upper values never occur)
+    const int nk = 1 << KB, nv = 1 << VB, lk = 1 << G.kb, lv = 1 << G.vb;
+    auto level = [](const float* cb, int l, int c) { return c < l ? 2.0f * cb[l - 1 + c] - 1.0f : 0.0f; };
     for (int i = threadIdx.x; i < (1 << (2 * KB)) * T::NLUT; i += blockDim.x) {
       const int e = i / T::NLUT;
-      const float lo = 2.0f * a.tab.cb_k[nk - 1 + (e & (nk - 1))] - 1.0f;
-      const float hi = 2.0f * a.tab.cb_k[nk - 1 + (e >> KB)] - 1.0f;
-      lut_k[i] = f2_to_h2(lo, hi);
+      lut_k[i] = f2_to_h2(level(a.tab.cb_k, lk, e & (nk - 1)), level(a.tab.cb_k, lk, e >> KB));
     }
     for (int i = threadIdx.x; i < (1 << (2 * VB)) * T::NLUT; i += blockDim.x) {
       const int e = i / T::NLUT;
-      const float lo = 2.0f * a.tab.cb_v[nv - 1 + (e & (nv - 1))] - 1.0f;
-      const float hi = 2.0f * a.tab.cb_v[nv - 1 + (e >> VB)] - 1.0f;
-      lut_v[i] = f2_to_h2(lo, hi);
+      lut_v[i] = f2_to_h2(level(a.tab.cb_v, lv, e & (nv - 1)), level(a.tab.cb_v, lv, e >> VB));
     }
   }
   __syncthreads();
@@ -907,7 +906,8 @@ cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
 
 template <int D>
 cudaError_t launch_kivi_d(DecodeArgs& a, cudaStream_t s, int sm_count) {
-  const int kb = a.geo.kb, vb = a.geo.vb;
+  // stored field widths: 3-bit codes run in the 4-bit kernels
+  const int kb = storage_bits(a.geo.kb), vb = storage_bits(a.geo.vb);
   if (a.geo.mode_tq) {
 #define KVQ_CASE(K, V) \
   if (kb == K && vb == V) return launch_kivi_instance<D, K, V, true, false>(a, s, sm_count);

@@ -54,6 +54,11 @@ struct Chunk {
   int kc_off, kmeta_off, vc_off, vmeta_off, bytes;
 };
 
+// Bits a code occupies in storage: 3-bit codes are kept two to a byte, in
+// the 4-bit layout (Foundry spec, "Step 3: Packing": [v0:3][v1:3][__:2]).
+KVQ_HD constexpr int storage_bits(int bits) { return bits == 3 ? 4 : bits; }
+
+// kb, vb: storage bits (storage_bits of the code widths).
 KVQ_HD Chunk chunk_layout(int mode_tq, int D, int kb, int vb) {
   Chunk c;
   c.kc_off = 0;
