@@ -72,6 +72,7 @@ class CacheConfig:
     act_dtype: str = "f16"      # "f16" | "bf16"
     seed: int = 0
     rope_base: float = 0.0
+    rope_reposition: bool = False   # StreamingLLM position re-encoding at read
 
 
 def validate(cfg: CacheConfig) -> None:
@@ -97,6 +98,8 @@ def validate(cfg: CacheConfig) -> None:
         raise ValueError(f"unknown mode {cfg.mode!r}")
     if min(cfg.n_sink, cfg.window, cfg.evict_window, cfg.n_dyn_sinks) < 0:
         raise ValueError("negative size")
+    if cfg.rope_reposition and not cfg.rope_base:
+        raise ValueError("re-positioning needs the cache to apply RoPE")
     if cfg.n_dyn_sinks and (cfg.n_sink or cfg.window or cfg.evict_window):
         raise ValueError("KVSink sinks exclude the StreamingLLM overlay and eviction")
     if cfg.n_dyn_sinks > 32:
@@ -360,13 +363,23 @@ class OracleCache:
                 np.concatenate(V_list), np.concatenate(pool))
 
     # ------------------------------------------------------------ attention
+    def cache_position(self, layer: int, p):
+        """Slot index of absolute position p inside the cache (StreamingLLM
+        "RoPE caveat": the sinks keep 0 .. N_s - 1, the kept tokens follow
+        without the evicted gap). Equal to p until something is evicted."""
+        n_s, E = self.cfg.n_sink, self.layers[layer].E
+        p = np.asarray(p, np.int64)
+        return np.where(p < n_s, p, n_s + (p - E))
+
     def query_rotated(self, layer: int, q: np.ndarray) -> np.ndarray:
         """The query as attention uses it: RoPE'd at position L - 1 when the
-        cache applies RoPE (float32, not rounded to the activation dtype)."""
+        cache applies RoPE, at its cache slot when it re-positions (float32,
+        not rounded to the activation dtype)."""
         q = np.asarray(q, np.float32)
         if self.cfg.rope_base:
             L = self.layers[layer].L
-            q = rope.rotate(q[..., None, :], [L - 1], self.cfg.rope_base)[..., 0, :]
+            pos = int(self.cache_position(layer, L - 1)) if self.cfg.rope_reposition else L - 1
+            q = rope.rotate(q[..., None, :], [pos], self.cfg.rope_base)[..., 0, :]
         return q
 
     def decode_attn(self, layer: int, q: np.ndarray, heads=None):
@@ -387,8 +400,13 @@ class OracleCache:
         for b, j in todo:
             by_kv.setdefault((b, j // self.g), []).append(j)
         for (b, h), js in by_kv.items():
-            _, K, V, _ = self.read_set(layer, b, h)
+            pos, K, V, _ = self.read_set(layer, b, h)
             K64 = K.astype(np.float64)
+            if cfg.rope_reposition:
+                # StreamingLLM re-positioning: un-rotate each stored key at
+                # its absolute position, rotate it at its cache slot
+                K64 = rope.rotate64(rope.rotate64(K64, -pos, cfg.rope_base),
+                                    self.cache_position(layer, pos), cfg.rope_base)
             V64 = V.astype(np.float64)
             for j in js:
                 s = (K64 @ qr[b, j]) / math.sqrt(D)

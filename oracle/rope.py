@@ -42,6 +42,24 @@ def cos_sin(positions, head_dim: int, base: float) -> np.ndarray:
     return tab
 
 
+def rotate64(x: np.ndarray, positions, base: float) -> np.ndarray:
+    """Rotate float64 rows x [..., T, D] at positions [T] (any integers,
+    negative ones un-rotate), angles, cos and sin all in double."""
+    x = np.asarray(x, np.float64)
+    D = x.shape[-1]
+    half = D // 2
+    pos = np.asarray(positions, np.float64)[:, None]
+    inv = np.array([base ** (-(2.0 * i) / D) for i in range(half)], np.float64)[None, :]
+    c = np.cos(pos * inv)
+    s = np.sin(pos * inv)
+    a = x[..., :half]
+    b = x[..., half:]
+    out = np.empty_like(x)
+    out[..., :half] = a * c - b * s
+    out[..., half:] = a * s + b * c
+    return out
+
+
 def rotate(x: np.ndarray, positions, base: float) -> np.ndarray:
     """Rotate float32 rows x [..., T, D] at absolute positions [T] (float32)."""
     x = np.asarray(x, np.float32)

@@ -310,3 +310,66 @@ def test_turboquant_cache_attention_quality():
         ref = _sdpa64(q[0, j], k[0, j // 4], v[0, j // 4])
         cos.append(np.dot(out[0, j], ref) / (np.linalg.norm(out[0, j]) * np.linalg.norm(ref)))
     assert np.mean(cos) > 0.97
+
+
+# ------------------------------------------------------------------ RoPE re-positioning
+
+def _ring_stream(reposition, n_sink, T=300, keep=96, D=128, seed=0, zero_rows=False):
+    """One sequence streamed token by token with eviction after each append
+    (StreamingLLM ring), RoPE base 10000, K8/V8."""
+    c = OracleCache(_cfg(batch=1, n_kv_heads=1, n_q_heads=1, head_dim=D, k_bits=8, v_bits=8,
+                         n_sink=n_sink, evict_window=keep, rope_base=10000.0, rope_reposition=reposition,
+                         max_tokens=keep + 64))
+    rng = np.random.default_rng(seed)
+    for t in range(T):
+        if zero_rows:
+            k = np.zeros((1, 1, 1, D), np.float32)
+            v = np.zeros((1, 1, 1, D), np.float32)
+            if t == 0:
+                k[0, 0, 0, 0] = 1.0      # the one sink: e_0 (unchanged by RoPE at position 0)
+                v[0, 0, 0, 1] = 1.0
+        else:
+            k, v = _f16(rng, (1, 1, 1, D)), _f16(rng, (1, 1, 1, D))
+        c.append(0, k, v)
+        c.evict(0)
+    return c
+
+
+def test_reposition_closed_form_single_sink():
+    """StreamingLLM "RoPE caveat": with re-positioning the query sits at its
+    cache slot N_s + (L - 1 - E) = keep instead of L - 1. One sink key e_0,
+    every other key and value zero, q = 8 e_0: the sink score is
+    8 cos(pos * theta_0) / sqrt(D) with theta_0 = 1, the others 0, so
+    out[1] = e^s / (e^s + n - 1) and every other channel is 0."""
+    import math
+    T, keep, D = 300, 96, 128
+    q = np.zeros((1, 1, D), np.float32)
+    q[0, 0, 0] = 8.0
+    for reposition, qpos in ((False, T - 1), (True, keep)):
+        c = _ring_stream(reposition, 1, T, keep, D, zero_rows=True)
+        assert c.layers[0].E == T - keep
+        n = 1 + keep                       # the sink and the kept window
+        s = 8.0 * math.cos(qpos) / math.sqrt(D)
+        out, _ = c.decode_attn(0, q)
+        assert abs(float(out[0, 0, 1]) - math.exp(s) / (math.exp(s) + n - 1)) < 1e-6
+        assert np.all(np.delete(out[0, 0], 1) == 0.0)
+
+
+def test_reposition_is_vanilla_without_eviction_or_sinks():
+    """Until something is evicted every cache slot is the absolute position,
+    and with no sinks every kept key and the query move by the same offset:
+    both give the vanilla output (relative rotations are all that attention
+    sees)."""
+    rng = np.random.default_rng(5)
+    q = _f16(rng, (1, 1, 128))
+    for n_sink, T in ((4, 80), (0, 300)):
+        a = _ring_stream(False, n_sink, T, seed=7)
+        b = _ring_stream(True, n_sink, T, seed=7)
+        assert (a.layers[0].E > n_sink) == (T > 96)
+        oa, _ = a.decode_attn(0, q)
+        ob, _ = b.decode_attn(0, q)
+        assert np.allclose(oa, ob, rtol=1e-5, atol=1e-6)
+    # with sinks and eviction the sinks' distance changes, and so does the output
+    a = _ring_stream(False, 4, 300, seed=7)
+    b = _ring_stream(True, 4, 300, seed=7)
+    assert not np.allclose(a.decode_attn(0, q)[0], b.decode_attn(0, q)[0], rtol=1e-3)
