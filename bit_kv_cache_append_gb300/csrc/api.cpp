@@ -103,6 +103,8 @@ kv_status check_config(const kv_cache_config* c) {
   if (c->max_tokens > (static_cast<int64_t>(1) << 40)) return fail(KV_ERR_INVALID_ARG, "max_tokens too large");
   if (!(c->rope_base >= 0.0)) return fail(KV_ERR_INVALID_ARG, "rope_base must be >= 0");
   if (c->rope_base > 0.0 && c->rope_max_pos < 1) return fail(KV_ERR_INVALID_ARG, "rope_max_pos must be >= 1");
+  if (c->rope_reposition && !(c->rope_base > 0.0))
+    return fail(KV_ERR_INVALID_ARG, "rope_reposition needs the cache to apply RoPE (rope_base > 0)");
   if (c->max_splits < 0 || c->max_splits > 4096) return fail(KV_ERR_INVALID_ARG, "max_splits out of range");
   return KV_OK;
 }
@@ -129,6 +131,7 @@ Geometry make_geometry(const kv_cache_config* c) {
   g.max_splits = c->max_splits ? c->max_splits : 64;
   g.chunk = kvq::chunk_layout(g.mode_tq, g.D, kvq::storage_bits(g.kb), kvq::storage_bits(g.vb));
   g.rope_max_pos = c->rope_base > 0.0 ? c->rope_max_pos : 0;
+  g.rope_repos = c->rope_reposition ? 1 : 0;
 
   const size_t B = g.B, H = g.H, D = g.D;
   size_t off = 0;
@@ -443,6 +446,8 @@ kv_status decode_attn_impl(kv_cache* cache, int layer, const void* q, float* out
   a.qlo = std::max<int64_t>(g.n_sink, ls.E);
   a.n_sink_read = static_cast<int>(std::min<int64_t>(std::min<int64_t>(g.n_sink, ls.L), a.F));
   a.n_dyn_sel = ls.n_dyn_sel;
+  // re-positioning moves the query against the sinks by the evicted span
+  a.sink_qpos = ls.L - 1 - (g.rope_repos ? ls.E - g.n_sink : 0);
   a.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(g.D)));
   const int64_t units = static_cast<int64_t>(g.B) * g.H;
   if (a.F > a.qlo) {

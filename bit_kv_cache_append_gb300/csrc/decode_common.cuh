@@ -195,11 +195,13 @@ __device__ __forceinline__ float query_value(const DecodeArgs& a, int b, int hq,
   return x * a.qscale;
 }
 
-// The channel pair (c0, c0 + 1), c0 even, of a query row times `scale`
-// (query_value's arithmetic element by element when scale is a.qscale): one
-// 32-bit load of the pair (q must be 4-byte aligned) and, with RoPE, of its
-// rotation partner and one 16-byte load of the two table entries.
-__device__ __forceinline__ float2 query_pair(const DecodeArgs& a, int b, int hq, int c0, float scale) {
+// The channel pair (c0, c0 + 1), c0 even, of a query row times `scale`,
+// RoPE'd at position qpos (query_value's arithmetic element by element when
+// scale is a.qscale and qpos is L - 1): one 32-bit load of the pair (q must
+// be 4-byte aligned) and, with RoPE, of its rotation partner and one 16-byte
+// load of the two table entries.
+__device__ __forceinline__ float2 query_pair(const DecodeArgs& a, int b, int hq, int c0, float scale,
+                                             int64_t qpos) {
   const Geometry& G = a.geo;
   const int D = G.D, half = D / 2;
   const uint16_t* qrow = a.q + (static_cast<size_t>(b) * G.Hq + hq) * D;
@@ -212,7 +214,7 @@ __device__ __forceinline__ float2 query_pair(const DecodeArgs& a, int b, int hq,
     const uint32_t yw = *reinterpret_cast<const uint32_t*>(qrow + (lo ? c0 + half : c0 - half));
     const float y0 = act_to_float(static_cast<uint16_t>(yw & 0xffffu), G.act_bf16);
     const float y1 = act_to_float(static_cast<uint16_t>(yw >> 16), G.act_bf16);
-    const float4 tr = *reinterpret_cast<const float4*>(a.tab.rope + static_cast<size_t>(a.L - 1) * D + 2 * i);
+    const float4 tr = *reinterpret_cast<const float4*>(a.tab.rope + static_cast<size_t>(qpos) * D + 2 * i);
     float ra, rb;
     if (lo) {
       rope_pair(x0, y0, tr.x, tr.y, &ra, &rb), x0 = ra;
@@ -439,7 +441,7 @@ __device__ bool exact_states_tc(const DecodeArgs& a, int b, int h, float* red, u
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
       const int c0 = 16 * s + 2 * t + 8 * p;
-      const float2 x = jc < gq ? query_pair(a, b, h * gq + jc, c0, a.qscale) : make_float2(0.0f, 0.0f);
+      const float2 x = jc < gq ? query_pair(a, b, h * gq + jc, c0, a.qscale, a.L - 1) : make_float2(0.0f, 0.0f);
       qb[s][p] = split_act2<BF>(x.x, x.y, col_lo);
     }
   float m_run = -INFINITY, l_run = 0.0f;  // of query head t (this lane's C columns)
@@ -473,6 +475,34 @@ __device__ bool exact_states_tc(const DecodeArgs& a, int b, int h, float* red, u
                                16 * s + 8 * (lane >> 4));
             mma_act<BF>(sc[mt], A[0], A[1], A[2], A[3], qb[s][0], qb[s][1]);
           }
+        if (i0 + rb < n_sink_items && a.sink_qpos != a.L - 1) {
+          // re-positioning: the sink rows of this tile meet the query
+          // rotated at sink_qpos; their scores again with that operand
+          float ss[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+#pragma unroll
+          for (int s = 0; s < S; ++s) {
+            uint32_t qs[2];
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+              const int c0 = 16 * s + 2 * t + 8 * p;
+              const float2 x = jc < gq ? query_pair(a, b, h * gq + jc, c0, a.qscale, a.sink_qpos)
+                                       : make_float2(0.0f, 0.0f);
+              qs[p] = split_act2<BF>(x.x, x.y, col_lo);
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              uint32_t A[4];
+              ldmatrix_x4(A, sk + static_cast<size_t>(rb + 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1)) * D +
+                                 16 * s + 8 * (lane >> 4));
+              mma_act<BF>(ss[mt], A[0], A[1], A[2], A[3], qs[0], qs[1]);
+            }
+          }
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (i0 + rb + 16 * mt + g + 8 * (e >> 1) < n_sink_items) sc[mt][e] = ss[mt][e];
+        }
         float pr[2][2];
         float mx = -INFINITY;
 #pragma unroll

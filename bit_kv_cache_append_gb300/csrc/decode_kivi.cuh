@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             const int c0 = t * (D / 4) + 4 * s + 2 * p;
-            const float2 x = jc < gq ? query_pair(a, b, h * gq + jc, c0, QX ? 1.0f : a.qscale)
+            const float2 x = jc < gq ? query_pair(a, b, h * gq + jc, c0, QX ? 1.0f : a.qscale, a.L - 1)
                                      : make_float2(0.0f, 0.0f);
             const float x0 = x.x, x1 = x.y;
             const uint32_t hi = f2_to_h2(x0, x1);

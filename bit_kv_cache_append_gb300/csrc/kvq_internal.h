@@ -68,6 +68,8 @@ struct DecodeArgs {
   int ns;               // partial slot stride per (sequence, query head)
   int n_sink_read;      // overlay: sink slots [0, n) read from the sink buffer
   int n_dyn_sel;        // KVSink: selected sinks (read when pos < F)
+  int64_t sink_qpos;    // RoPE position of the query against the sink rows
+                        // (L - 1, or L - 1 - (E - n_sink) when re-positioning)
   float qscale;         // log2(e) / sqrt(D)
   // f16x2 constants of the code-to-f16 conversion, read from the parameter
   // bank so that one instruction needs at most one immediate: the magic

@@ -146,6 +146,7 @@ struct Geometry {
   int B, H, Hq, D, gqa;
   int mode_tq, kb, vb;
   int n_sink, window, evict_window, n_dyn;
+  int rope_repos;     // StreamingLLM position re-encoding at read
   int act_bf16;
   int64_t max_tokens;
   int n_slots;        // group chunks per (layer, b, h)

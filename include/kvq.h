@@ -92,6 +92,16 @@ typedef struct {
   int64_t rope_max_pos; /* positions the RoPE table covers (rope_base > 0) */
   int max_splits;     /* upper bound on split-KV partitions per (b, h);
                          0 = library default (64)                           */
+  int rope_reposition; /* 1 (with rope_base > 0): StreamingLLM position
+                         re-encoding at read ([P1] "RoPE caveat"): every kept
+                         key is read as if rotated at its slot in the cache
+                         (sinks at 0 .. n_sink-1, the kept tokens after them
+                         without the evicted gap) and the query at its own
+                         slot. Relative rotations change only between the
+                         query and the sinks, so the library reads the sink
+                         rows against the query rotated at
+                         L - 1 - (E - n_sink) and everything else as in the
+                         vanilla scheme. 0: vanilla (absolute positions)    */
 } kv_cache_config;
 
 typedef struct kv_cache kv_cache; /* opaque host-side handle */

@@ -45,7 +45,8 @@ def oracle_config(kw):
                        max_tokens=kw["max_tokens"], mode=kw["mode"], k_bits=kw["k_bits"],
                        v_bits=kw["v_bits"], n_sink=kw["n_sink"], window=kw["window"],
                        evict_window=kw["evict_window"], n_dyn_sinks=kw["n_dyn_sinks"],
-                       act_dtype=kw["act_dtype"], seed=kw["seed"], rope_base=kw["rope_base"])
+                       act_dtype=kw["act_dtype"], seed=kw["seed"], rope_base=kw["rope_base"],
+                       rope_reposition=bool(kw.get("rope_reposition", False)))
 
 
 def compare_exports(gpu_cache, oc, layer: int) -> None:

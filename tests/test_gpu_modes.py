@@ -26,13 +26,15 @@ def _decode_both(gc, oc, layer, q, act, heads=None):
 
 # ------------------------------------------------------------------ ring
 
+@pytest.mark.parametrize("reposition", [False, True])
 @pytest.mark.parametrize("name", ["ring_int8", "ring_int4"])
-def test_ring_stream_with_rope_and_eviction(name):
+def test_ring_stream_with_rope_and_eviction(name, reposition):
     """Shortened StreamingLLM stream: 2 layers, per step append 1 -> evict ->
-    decode; identical eviction ranges, codes and attention."""
+    decode; identical eviction ranges, codes and attention, with keys read
+    at their absolute positions or re-positioned at their cache slots."""
     w = W.scaled(W.WORKLOADS[name], batch=4, n_kv_heads=4, n_q_heads=4, evict_window=96, n_layers=2)
     steps = 400
-    kw = cache_kwargs(w, 96 + 64, rope_max_pos=steps)
+    kw = cache_kwargs(w, 96 + 64, rope_max_pos=steps, rope_reposition=reposition)
     gc, oc = _pair(kw)
     ranges_g, ranges_o = [], []
     for t in range(steps):
