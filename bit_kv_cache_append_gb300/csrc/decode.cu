@@ -39,7 +39,7 @@ size_t merge_smem_bytes(int stage_bytes) {
 // (x = D FWHT(y) / sqrt(d)) before the exact part, which is in the original
 // domain, is added (Foundry "TurboQuant KV Cache Compression - Spec",
 // "Optimization: Fused dequant-dot": rotate the accumulated output once).
-template <int D>
+template <int D, bool REPOS>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(DecodeArgs a, int stage_bytes) {
   constexpr int NS = D / 32, NW = kMergeWarps;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -48,8 +48,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(DecodeArgs a, i
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 1);
   const Geometry& G = a.geo;
   const int u = blockIdx.x, b = u / G.H, h = u % G.H;
-  const bool ok = G.act_bf16 ? exact_states_tc<D, NW, true>(a, b, h, red, smem, stage_bytes, bar, abort_flag)
-                             : exact_states_tc<D, NW, false>(a, b, h, red, smem, stage_bytes, bar, abort_flag);
+  const bool ok = G.act_bf16 ? exact_states_tc<D, NW, true, REPOS>(a, b, h, red, smem, stage_bytes, bar, abort_flag)
+                             : exact_states_tc<D, NW, false, REPOS>(a, b, h, red, smem, stage_bytes, bar, abort_flag);
   if (!ok && threadIdx.x == 0) set_error(a.tab.err_flag, kErrTimeout);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= G.gqa) return;
@@ -131,17 +131,18 @@ int merge_stage_bytes(const Geometry& G) {
 // scheduled before it ends (programmatic dependent launch); otherwise it is
 // an ordinary launch, since its exact pools read rows the appends before it
 // wrote.
-template <int D>
-cudaError_t launch_merge(DecodeArgs& a, cudaStream_t s, bool after_split) {
+template <int D, bool REPOS>
+cudaError_t launch_merge_instance(DecodeArgs& a, cudaStream_t s, bool after_split) {
   const int stage = merge_stage_bytes(a.geo);
   const size_t smem = merge_smem_bytes<D>(stage);
-  static size_t configured[kMaxDevices] = {};  // per device: the attribute is per device
+  static size_t configured[kMaxDevices] = {};  // per device and instance: the attribute is per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (smem > configured[dev]) {
-    e = cudaFuncSetAttribute(merge_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = cudaFuncSetAttribute(merge_kernel<D, REPOS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     configured[dev] = smem;
   }
@@ -155,7 +156,13 @@ cudaError_t launch_merge(DecodeArgs& a, cudaStream_t s, bool after_split) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = after_split ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, merge_kernel<D>, a, stage);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<D, REPOS>, a, stage);
+}
+
+template <int D>
+cudaError_t launch_merge(DecodeArgs& a, cudaStream_t s, bool after_split) {
+  return a.sink_qpos != a.L - 1 ? launch_merge_instance<D, true>(a, s, after_split)
+                                : launch_merge_instance<D, false>(a, s, after_split);
 }
 
 }  // namespace

@@ -387,7 +387,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // [w][j][0..D-1] = o, [w][j][D] = m in log2 units, [w][j][D+1] = l). `bar`
 // is an mbarrier this function initialises; `abort_flag` is the CTA's shared
 // give-up flag. Returns false (for every thread) when a wait gave up.
-template <int D, int NW, bool BF>
+// REPOS: the cache re-positions RoPE (the sink rows are scored against the
+// query rotated at sink_qpos); a separate instance so that the common one
+// carries none of its registers.
+template <int D, int NW, bool BF, bool REPOS>
 __device__ bool exact_states_tc(const DecodeArgs& a, int b, int h, float* red, uint8_t* stage, int stage_bytes,
                                 uint64_t* bar, volatile int* abort_flag) {
   constexpr int S = D / 16, MV = D / 16;
@@ -475,7 +478,7 @@ __device__ bool exact_states_tc(const DecodeArgs& a, int b, int h, float* red, u
                                16 * s + 8 * (lane >> 4));
             mma_act<BF>(sc[mt], A[0], A[1], A[2], A[3], qb[s][0], qb[s][1]);
           }
-        if (i0 + rb < n_sink_items && a.sink_qpos != a.L - 1) {
+        if (REPOS && i0 + rb < n_sink_items && a.sink_qpos != a.L - 1) {
           // re-positioning: the sink rows of this tile meet the query
           // rotated at sink_qpos; their scores again with that operand
           float ss[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
