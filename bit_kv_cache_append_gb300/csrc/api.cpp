@@ -263,6 +263,7 @@ kv_status do_append(kv_cache* c, int layer, const void* k, const void* v, int n,
     sa.lay = a.lay;
     sa.tab = a.tab;
     sa.k = a.k;
+    sa.v = a.v;
     sa.n = n;
     sa.norms = reinterpret_cast<float*>(c->arena + g.off_norms);
     sa.cand_m = reinterpret_cast<float*>(c->arena + g.off_cand_m);
@@ -273,10 +274,14 @@ kv_status do_append(kv_cache* c, int layer, const void* k, const void* v, int n,
     sa.q0 = q0;
     sa.n_old = ls.n_dyn_sel;
     sa.k_total = n_sel;
-    e = kvq::launch_sink_select(sa, s, &launches);
-    if (e == cudaSuccess) {
-      a.n_dyn_sel = n_sel;
-      e = kvq::launch_sink_gather(a, s, &launches);
+    if (n <= kvq::kSinkSmallCallTokens) {  // decode-time appends: one launch
+      e = kvq::launch_sink_admit_small(sa, s, &launches);
+    } else {
+      e = kvq::launch_sink_select(sa, s, &launches);
+      if (e == cudaSuccess) {
+        a.n_dyn_sel = n_sel;
+        e = kvq::launch_sink_gather(a, s, &launches);
+      }
     }
   }
   a.dyn_active = (select || ls.dyn_selected) ? 1 : 0;

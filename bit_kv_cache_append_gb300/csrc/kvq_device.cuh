@@ -28,6 +28,24 @@ __device__ __forceinline__ void rope_pair(float a, float b, float c, float s, fl
   *rb = __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c));
 }
 
+// Rotate 8 RoPE pairs (channels c0..c0+7 with c0+D/2..) held as act-dtype
+// bits, at table row `tab_row` ([D/2][2] cos, sin); results rounded back to
+// the activation dtype (posttrainllm "StreamingLLM + KIVI", "RoPE caveat":
+// keys keep the rotation of their absolute position).
+__device__ __forceinline__ void rotate8(uint4& lo, uint4& hi, const float* tab_row, int c0, int bf16) {
+  uint16_t* pl = reinterpret_cast<uint16_t*>(&lo);
+  uint16_t* ph = reinterpret_cast<uint16_t*>(&hi);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float x = act_to_float(pl[i], bf16), y = act_to_float(ph[i], bf16);
+    const float c = tab_row[2 * (c0 + i)], s = tab_row[2 * (c0 + i) + 1];
+    float rx, ry;
+    rope_pair(x, y, c, s, &rx, &ry);
+    pl[i] = float_to_act(rx, bf16);
+    ph[i] = float_to_act(ry, bf16);
+  }
+}
+
 __device__ __forceinline__ void set_error(int* flag, int code) {
   if (flag) atomicExch(flag, code);
 }

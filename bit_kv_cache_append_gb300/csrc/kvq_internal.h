@@ -85,6 +85,7 @@ struct SinkSelectArgs {
   LayerDev lay;
   TablesDev tab;
   const uint16_t* k;    // [B][H][n][D]
+  const uint16_t* v;    // [B][H][n][D] (the single-kernel path copies new sink rows)
   int n;
   float* norms;         // [B][n]
   float* cand_m;        // [B][n_chunks][kMaxSinks]
@@ -99,6 +100,10 @@ struct SinkSelectArgs {
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int64_t* launches);
 cudaError_t launch_sink_select(const SinkSelectArgs& a, cudaStream_t s, int64_t* launches);
+// KVSink calls of at most this many tokens take the single-launch path
+// (norms, set update and new sink rows in one kernel per sequence).
+constexpr int kSinkSmallCallTokens = 256;
+cudaError_t launch_sink_admit_small(const SinkSelectArgs& a, cudaStream_t s, int64_t* launches);
 cudaError_t launch_sink_gather(const AppendArgs& a, cudaStream_t s, int64_t* launches);
 cudaError_t launch_decode(DecodeArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, int sm_count,
                           int64_t* launches);

@@ -9,15 +9,14 @@
 namespace kvq {
 namespace {
 
-// One warp per (token, b): head norms by the fixed pairwise tree over k^2
-// (stride D/2, D/4, ..., 1), summed over heads in head order, divided by Hkv.
+// Key norm of token t (of the call) of sequence b, valid in lane 0: head
+// norms by the fixed pairwise tree over k^2 (stride D/2, D/4, ..., 1), summed
+// over heads in head order, divided by Hkv. Keys are rotated (and rounded to
+// the activation dtype) first when the cache applies RoPE.
 template <int D>
-__global__ void __launch_bounds__(128) keynorm_kernel(SinkSelectArgs a) {
+__device__ float token_key_norm(const SinkSelectArgs& a, int b, int t, int lane) {
   constexpr int NS = D / 32;
   const Geometry& G = a.geo;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 4 + warp, b = blockIdx.y;
-  if (t >= a.n) return;
   const int bf16 = G.act_bf16;
   float acc = 0.0f;
   for (int h = 0; h < G.H; ++h) {
@@ -26,7 +25,7 @@ __global__ void __launch_bounds__(128) keynorm_kernel(SinkSelectArgs a) {
 #pragma unroll
     for (int i = 0; i < NS; ++i) x[i] = act_to_float(a.k[row + i * 32 + lane], bf16);
     if (a.tab.rope) {
-      const float* tr = a.tab.rope + static_cast<size_t>(t) * D;
+      const float* tr = a.tab.rope + static_cast<size_t>(a.L0 + t) * D;
 #pragma unroll
       for (int i = 0; i < NS / 2; ++i) {
         const int c = i * 32 + lane;
@@ -53,7 +52,17 @@ __global__ void __launch_bounds__(128) keynorm_kernel(SinkSelectArgs a) {
     const float nrm = __fsqrt_rn(s);
     acc = (h == 0) ? nrm : __fadd_rn(acc, nrm);
   }
-  if (lane == 0) a.norms[static_cast<size_t>(b) * a.n + t] = __fdiv_rn(acc, static_cast<float>(G.H));
+  return __fdiv_rn(acc, static_cast<float>(G.H));
+}
+
+// One warp per (token, b).
+template <int D>
+__global__ void __launch_bounds__(128) keynorm_kernel(SinkSelectArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 4 + warp, b = blockIdx.y;
+  if (t >= a.n) return;
+  const float m = token_key_norm<D>(a, b, t, lane);
+  if (lane == 0) a.norms[static_cast<size_t>(b) * a.n + t] = m;
 }
 
 __device__ __forceinline__ bool better(float m1, int64_t p1, float m2, int64_t p2) {
@@ -61,6 +70,7 @@ __device__ __forceinline__ bool better(float m1, int64_t p1, float m2, int64_t p
 }
 
 constexpr int kTopkThreads = 256;
+constexpr int kSinkSmallCall = kSinkSmallCallTokens;  // longest call of the single-launch path
 constexpr int kTopkPer = 4;
 constexpr int kChunk = kTopkThreads * kTopkPer;
 
@@ -120,16 +130,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(SinkSelectArgs
   block_topk(m, p, a.k_sel, a.cand_m + o, a.cand_p + o);
 }
 
-// Pass 2, one CTA per sequence: the running top-k after the call. Members
-// whose position lies below q0 (their group was quantised before the call)
-// are locked and keep their slots. The other members and the chunk winners
-// of the call compete for the remaining k_total - locked places by rounds of
-// a block-wide arg-best (each winner struck out in place): a member that
+// The running top-k of sequence b after the call, by one CTA. Members whose
+// position lies below q0 (their group was quantised before the call) are
+// locked and keep their slots. The other members and the call's candidates
+// (cand(c, &m, &p) for c < n_call, absolute positions, false for an empty
+// entry; strike(c) takes a winner out) compete for the remaining
+// k_total - locked places by rounds of a block-wide arg-best: a member that
 // wins keeps its slot, the call's winners take the freed slots and then the
 // new ones, in rank order. Slots are not kept in position order; only the
-// set matters to the readers.
-__global__ void __launch_bounds__(kTopkThreads) sink_update_kernel(SinkSelectArgs a) {
-  const int b = blockIdx.x;
+// set matters to the readers. Ends with the block synchronised.
+template <typename Cand, typename Strike>
+__device__ void update_sinks(const SinkSelectArgs& a, int b, int n_call, Cand cand, Strike strike) {
   __shared__ int64_t win_p[kMaxSinks];
   __shared__ float win_m[kMaxSinks];
   __shared__ int64_t un_p[kMaxSinks];   // unlocked members: candidates (struck out in place)
@@ -162,23 +173,18 @@ __global__ void __launch_bounds__(kTopkThreads) sink_update_kernel(SinkSelectArg
   }
   __syncthreads();
   const int budget = a.k_total - n_lock;
-  const int n_cand = a.n_chunks * kMaxSinks;
-  float* cm_base = a.cand_m + static_cast<size_t>(b) * n_cand;
-  int64_t* cp_base = a.cand_p + static_cast<size_t>(b) * n_cand;  // call-relative positions
   for (int round = 0; round < budget; ++round) {
     float bm = -INFINITY;
     int64_t bp = INT64_MAX;
     int bc = -1;
-    for (int c = threadIdx.x; c < n_cand + n_un; c += kTopkThreads) {
+    for (int c = threadIdx.x; c < n_call + n_un; c += blockDim.x) {
       float m;
       int64_t p;
-      if (c < n_cand) {
-        if (c % kMaxSinks >= a.k_sel) continue;
-        m = cm_base[c];
-        p = cp_base[c] == INT64_MAX ? INT64_MAX : cp_base[c] + a.L0;
+      if (c < n_call) {
+        if (!cand(c, &m, &p)) continue;
       } else {
-        m = un_m[c - n_cand];
-        p = un_p[c - n_cand];
+        m = un_m[c - n_call];
+        p = un_p[c - n_call];
       }
       if (better(m, p, bm, bp)) { bm = m; bp = p; bc = c; }
     }
@@ -195,12 +201,12 @@ __global__ void __launch_bounds__(kTopkThreads) sink_update_kernel(SinkSelectArg
       float xm = wm[0];
       int64_t xp = wp[0];
       int xc = wc[0];
-      for (int w = 1; w < kTopkThreads / 32; ++w)
+      for (int w = 1; w < static_cast<int>(blockDim.x) / 32; ++w)
         if (better(wm[w], wp[w], xm, xp)) { xm = wm[w]; xp = wp[w]; xc = wc[w]; }
       win_m[round] = xm;
       win_p[round] = xp;
-      if (xc >= 0 && xc < n_cand) { cm_base[xc] = -INFINITY; cp_base[xc] = INT64_MAX; }
-      else if (xc >= n_cand) { un_m[xc - n_cand] = -INFINITY; un_p[xc - n_cand] = INT64_MAX; }
+      if (xc >= 0 && xc < n_call) strike(xc);
+      else if (xc >= n_call) { un_m[xc - n_call] = -INFINITY; un_p[xc - n_call] = INT64_MAX; }
     }
     __syncthreads();
   }
@@ -228,9 +234,85 @@ __global__ void __launch_bounds__(kTopkThreads) sink_update_kernel(SinkSelectArg
       }
     }
   }
+  __syncthreads();
+}
+
+// Pass 2 of a long call, one CTA per sequence: the set update over the chunk
+// winners (call-relative positions).
+__global__ void __launch_bounds__(kTopkThreads) sink_update_kernel(SinkSelectArgs a) {
+  const int b = blockIdx.x;
+  const int n_cand = a.n_chunks * kMaxSinks;
+  float* cm_base = a.cand_m + static_cast<size_t>(b) * n_cand;
+  int64_t* cp_base = a.cand_p + static_cast<size_t>(b) * n_cand;
+  update_sinks(
+      a, b, n_cand,
+      [&](int c, float* m, int64_t* p) {
+        if (c % kMaxSinks >= a.k_sel || cp_base[c] == INT64_MAX) return false;
+        *m = cm_base[c];
+        *p = cp_base[c] + a.L0;
+        return true;
+      },
+      [&](int c) { cm_base[c] = -INFINITY; cp_base[c] = INT64_MAX; });
+}
+
+// A short call (n <= kSinkSmallCall) in one launch per sequence: the call's
+// key norms into shared memory, the set update over them, and the K/V rows
+// of the call's new members into their sink slots (keys rotated like every
+// stored key). The same arithmetic and order as the three-pass path.
+template <int D>
+__global__ void __launch_bounds__(kTopkThreads) sink_admit_small_kernel(SinkSelectArgs a) {
+  const int b = blockIdx.x;
+  const Geometry& G = a.geo;
+  __shared__ float cm[kSinkSmallCall];
+  __shared__ int64_t cp[kSinkSmallCall];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = warp; t < a.n; t += kTopkThreads / 32) {
+    const float m = token_key_norm<D>(a, b, t, lane);
+    if (lane == 0) {
+      cm[t] = m;
+      cp[t] = a.L0 + t;
+    }
+  }
+  __syncthreads();
+  update_sinks(
+      a, b, a.n,
+      [&](int c, float* m, int64_t* p) {
+        if (cp[c] == INT64_MAX) return false;
+        *m = cm[c];
+        *p = cp[c];
+        return true;
+      },
+      [&](int c) { cm[c] = -INFINITY; cp[c] = INT64_MAX; });
+  // rows of the members this call brought in
+  constexpr int HALF = D / 2, CPR = HALF / 8;
+  const int64_t* spos = a.lay.sink_pos + static_cast<size_t>(b) * kMaxSinks;
+  for (int idx = threadIdx.x; idx < a.k_total * G.H * CPR; idx += blockDim.x) {
+    const int j = idx / (G.H * CPR), h = (idx / CPR) % G.H, c0 = (idx % CPR) * 8;
+    const int64_t row = spos[j] - a.L0;
+    if (row < 0 || row >= a.n) continue;
+    const size_t bh = static_cast<size_t>(b) * G.H + h;
+    const size_t in_row = (bh * a.n + row) * D;
+    uint4 klo = *reinterpret_cast<const uint4*>(a.k + in_row + c0);
+    uint4 khi = *reinterpret_cast<const uint4*>(a.k + in_row + HALF + c0);
+    const uint4 vlo = *reinterpret_cast<const uint4*>(a.v + in_row + c0);
+    const uint4 vhi = *reinterpret_cast<const uint4*>(a.v + in_row + HALF + c0);
+    if (a.tab.rope) rotate8(klo, khi, a.tab.rope + static_cast<size_t>(spos[j]) * D, c0, G.act_bf16);
+    const size_t o = (bh * G.n_sink_slots + j) * D;
+    *reinterpret_cast<uint4*>(a.lay.sink_k + o + c0) = klo;
+    *reinterpret_cast<uint4*>(a.lay.sink_k + o + HALF + c0) = khi;
+    *reinterpret_cast<uint4*>(a.lay.sink_v + o + c0) = vlo;
+    *reinterpret_cast<uint4*>(a.lay.sink_v + o + HALF + c0) = vhi;
+  }
 }
 
 }  // namespace
+
+cudaError_t launch_sink_admit_small(const SinkSelectArgs& a, cudaStream_t s, int64_t* launches) {
+  if (a.geo.D == 128) sink_admit_small_kernel<128><<<a.geo.B, kTopkThreads, 0, s>>>(a);
+  else sink_admit_small_kernel<64><<<a.geo.B, kTopkThreads, 0, s>>>(a);
+  *launches += 1;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_sink_select(const SinkSelectArgs& a, cudaStream_t s, int64_t* launches) {
   dim3 g1((a.n + 3) / 4, a.geo.B);

@@ -184,15 +184,17 @@ def _sink_rows_with_norms(norms, B, H, D=128, seed=0):
     return k, v
 
 
-def test_kvsink_running_admission_one_token_per_call():
+@pytest.mark.parametrize("rope", [0.0, 10000.0])
+def test_kvsink_running_admission_one_token_per_call(rope):
     """A prefill of 50 tokens leaves two of its three sinks in the open group
     (35, 45) and locks 5. Single-token calls then displace the weakest open
     sink when they beat it (55 displaces 45; 60 loses to 35); once group 1 is
     quantised every sink is locked and 70, the largest key of all, stays out.
     The set, rows, masks and codes equal the oracle's after every call, and
-    attention along the way."""
+    attention along the way. With RoPE the key norms are taken on the keys
+    rotated at their absolute positions (those of each call's tokens)."""
     import torch
-    w = W.scaled(W.WORKLOADS["kvsink"], batch=2, n_kv_heads=2, n_q_heads=8, context=160)
+    w = W.scaled(W.WORKLOADS["kvsink"], batch=2, n_kv_heads=2, n_q_heads=8, context=160, rope_base=rope)
     kw = cache_kwargs(w, 512, n_dyn_sinks=3)
     gc, oc = _pair(kw)
     k, v = _sink_rows_with_norms({5: 25.0, 35: 20.0, 45: 15.0, 55: 30.0, 60: 18.0, 70: 40.0, 159: 1.0},
