@@ -158,22 +158,31 @@ struct KiviTile {
   // up to 6 KB); one for TurboQuant, whose tables and tiles leave less
   // shared memory, and for larger chunks
   static constexpr int GPB = (TQ || CHUNK > 6144) ? 1 : 2;
-#ifndef KVQ_DECODE_STAGES
-  // bulk-copy stages per pair: 2 runs of 2 groups; else 3 groups, or 2
-  // where the TurboQuant K4/V4 tables and tiles would not leave room for two
-  // CTAs per SM
-  static constexpr int NST = GPB == 2 ? 2 : ((TQ && KB == 4 && VB == 4) ? 2 : 3);
-#else
-  static constexpr int NST = KVQ_DECODE_STAGES;
-#endif
   static constexpr int STAGE = GPB * CHUNK;
-  static constexpr int PBUF = GPB * 32 * 16 + 16;        // weights (16 B per lane per group) + 4 rescale factors
+  static constexpr int PBUF = GPB * 32 * 8 + 16;         // weights (4 f16, 8 B per lane per group) + 4 rescale factors
   // TurboQuant codebook tables: code pair -> f16x2 of the two values
   // 2 c[code] - 1, NLUT interleaved copies (lane & 7 picks one) against
   // bank conflicts
   static constexpr int NLUT = 8;
   static constexpr int LUTK = TQ ? (1 << (2 * KB)) * NLUT * 4 : 0;
   static constexpr int LUTV = TQ ? (1 << (2 * VB)) * NLUT * 4 : 0;
+  static constexpr int VT_ROW = D + 8;
+  static constexpr int RED_FLOATS = NP * kMaxGqa * (D + 2);  // one merged state per pair
+  // shared memory of the CTA with nst stages per pair (the layout below)
+  static constexpr int smem_for(int nst) {
+    return NP * nst * STAGE + NP * 2 * PBUF + (D / 16) * 32 * 16 + (TQ ? kMaxGqa * D * 4 : 0) + LUTK + LUTV +
+           (TQ ? NP * 32 * VT_ROW * 2 : 0) + RED_FLOATS * 4 + NP * (nst + 4) * 8 + 16;
+  }
+  // what one of two CTAs may take of an SM's 228 KB (1 KB of each CTA's
+  // share is reserved by the hardware)
+  static constexpr int kTwoCtaSmem = 228 * 1024 / 2 - 1024;
+#ifndef KVQ_DECODE_STAGES
+  // bulk-copy stages per pair: three where they leave room for two CTAs per
+  // SM (runs of two groups up to 4 KB each; single groups), else two
+  static constexpr int NST = smem_for(3) <= kTwoCtaSmem ? 3 : 2;
+#else
+  static constexpr int NST = KVQ_DECODE_STAGES;
+#endif
   // shared memory: stages | weight buffers | query operand | query scratch |
   // tables | red | barriers | abort flag
   static constexpr int OFF_PBUF = NP * NST * STAGE;
@@ -182,14 +191,14 @@ struct KiviTile {
   static constexpr int OFF_LUT = OFF_QF + (TQ ? kMaxGqa * D * 4 : 0);
   // TurboQuant: each PV warp's dequantised V tile, 32 token rows of D f16
   // padded by 8 halves (conflict-free row stores and transposed ldmatrix)
-  static constexpr int VT_ROW = D + 8;
   static constexpr int OFF_VT = OFF_LUT + LUTK + LUTV;
   static constexpr int OFF_RED = OFF_VT + (TQ ? NP * 32 * VT_ROW * 2 : 0);
-  static constexpr int RED_FLOATS = NP * kMaxGqa * (D + 2);  // one merged state per pair
   static constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
   static constexpr int NBAR = NP * (NST + 4);             // full[NST], pfull[2], pempty[2]
   static constexpr int OFF_ABORT = OFF_BAR + NBAR * 8;
   static constexpr size_t smem_bytes() { return OFF_ABORT + 16; }
+  static_assert(smem_bytes() == static_cast<size_t>(smem_for(NST)), "layout and its size agree");
+  static_assert(OFF_BAR % 8 == 0, "mbarriers are 8-byte aligned");
 };
 
 // TurboQuant: the codebook table entry of a code pair (index = low code |
@@ -681,8 +690,9 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
         uint8_t* pw = pbuf + pb * T::PBUF;
 #pragma unroll
         for (int q = 0; q < GPB; ++q)
-          *reinterpret_cast<uint4*>(pw + (q * 32 + lane) * 16) = make_uint4(ph[q][0], ph[q][1], ph[q][2], ph[q][3]);
-        reinterpret_cast<float*>(pw + GPB * 32 * 16)[t] = al;  // the 8 lanes of query head t store the same value
+          *reinterpret_cast<uint2*>(pw + (q * 32 + lane) * 8) =
+              make_uint2(ph[q][0] | (ph[q][1] << 16), ph[q][2] | (ph[q][3] << 16));
+        reinterpret_cast<float*>(pw + GPB * 32 * 8)[t] = al;  // the 8 lanes of query head t store the same value
         mbar_arrive(&pfull[pb]);
       }
       l_run += __shfl_xor_sync(full, l_run, 4);
@@ -821,13 +831,14 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
         uint32_t ph[GPB][4];
 #pragma unroll
         for (int q = 0; q < GPB; ++q) {
-          const uint4 pv4 = *reinterpret_cast<const uint4*>(pw + (q * 32 + lane) * 16);
-          ph[q][0] = pv4.x;
-          ph[q][1] = pv4.y;
-          ph[q][2] = pv4.z;
-          ph[q][3] = pv4.w;
+          // the four f16 weights, each back to (value, 0) for the transposes
+          const uint2 pv2 = *reinterpret_cast<const uint2*>(pw + (q * 32 + lane) * 8);
+          ph[q][0] = pv2.x & 0xffffu;
+          ph[q][1] = pv2.x >> 16;
+          ph[q][2] = pv2.y & 0xffffu;
+          ph[q][3] = pv2.y >> 16;
         }
-        const float al = reinterpret_cast<const float*>(pw + GPB * 32 * 16)[t];
+        const float al = reinterpret_cast<const float*>(pw + GPB * 32 * 8)[t];
         mbar_arrive(&pempty[pb]);
         if (__any_sync(full, al != 1.0f)) {
 #pragma unroll
