@@ -251,9 +251,10 @@ enum {
   KV_EXPORT_V_ZERO = 5,   /* f16 [B][Hkv][n][D/32]  (KIVI)                   */
   KV_EXPORT_K_NORM = 6,   /* f32 [B][Hkv][n]        (TurboQuant)             */
   KV_EXPORT_V_NORM = 7,   /* f32 [B][Hkv][n]        (TurboQuant)             */
-  KV_EXPORT_SINK_POS = 8, /* i64 [B][S] ascending                            */
-  KV_EXPORT_SINK_K = 9,   /* act [B][Hkv][S][D]                              */
-  KV_EXPORT_SINK_V = 10,  /* act [B][Hkv][S][D]                              */
+  KV_EXPORT_SINK_POS = 8, /* i64 [B][S] ascending (the library keeps KVSink
+                             slots in admission order; the export sorts)    */
+  KV_EXPORT_SINK_K = 9,   /* act [B][Hkv][S][D], rows in SINK_POS order       */
+  KV_EXPORT_SINK_V = 10,  /* act [B][Hkv][S][D], rows in SINK_POS order       */
   KV_EXPORT_TAIL_K = 11,  /* act [B][Hkv][R][D]                              */
   KV_EXPORT_TAIL_V = 12,  /* act [B][Hkv][R][D]                              */
   KV_EXPORT_SINK_MASK = 13, /* u32 [B][G] bit r: token 32g+r is a sink (KIVI) */
