@@ -241,3 +241,28 @@ def test_kvsink_running_admission_calls_across_groups(k_dyn):
         t += n
         compare_exports(gc, oc, 0)
     _decode_both(gc, oc, 0, W.queries(w, 5), "f16")
+
+
+def test_kvsink_group_of_only_sinks():
+    """k = 32 with the 32 largest keys exactly filling group 0: the group is
+    left as is (no non-sink row to substitute), its mask is full and every
+    row of it is read exact from the sinks; then appends with larger keys
+    find every sink locked."""
+    import torch
+    w = W.scaled(W.WORKLOADS["kvsink"], batch=2, n_kv_heads=2, n_q_heads=8, context=120)
+    kw = cache_kwargs(w, 512, n_dyn_sinks=32)
+    gc, oc = _pair(kw)
+    k, v = _sink_rows_with_norms({p: 10.0 + p for p in range(32)} | {100: 80.0, 119: 1.0}, 2, 2, seed=6)
+    gc.prefill_quantize(0, torch_act(k[:, :, :70], "f16"), torch_act(v[:, :, :70], "f16"))
+    oc.prefill_quantize(0, k[:, :, :70], v[:, :, :70])
+    assert gc.export(0, "sink_pos").tolist() == [list(range(32))] * 2
+    assert gc.export(0, "sink_mask")[:, 0].tolist() == [0xFFFFFFFF] * 2
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 2), "f16")
+    for t in range(70, 120):
+        gc.append(0, torch_act(k[:, :, t:t + 1], "f16"), torch_act(v[:, :, t:t + 1], "f16"))
+        oc.append(0, k[:, :, t:t + 1], v[:, :, t:t + 1])
+    assert gc.export(0, "sink_pos").tolist() == [list(range(32))] * 2
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 3), "f16")
+    torch.cuda.synchronize()

@@ -251,3 +251,26 @@ def test_running_admission_invariants():
         prev_locked = {p for p in sp if p < c.q_end(0)}
         ex = c.export(0)
         assert np.array_equal(ex["sink_k"][0], k[0][:, sp])
+
+
+def test_group_of_only_sinks_is_left_as_is():
+    """k = 32 with the 32 largest keys exactly filling group 0: no row of the
+    group is left to substitute, so the group is quantised as plain KIVI
+    would ("How it works" 3 needs a non-sink row), its mask is full, and
+    attention reads all 32 rows exact from the sinks."""
+    norms = [1.0] * 70
+    for p in range(32):
+        norms[p] = 10.0 + p
+    k, v = _normed_rows(norms, seed=9)
+    c = _cache(32, B=1, H=2)
+    c.prefill_quantize(0, k, v)
+    assert c.sink_positions(0)[0].tolist() == list(range(32))
+    plain = _cache(0, B=1, H=2)
+    plain.prefill_quantize(0, k, v)
+    a, b = c.export(0), plain.export(0)
+    for name in ("k_codes", "k_scale", "k_zero", "v_codes", "v_scale", "v_zero"):
+        n = 1 if name in ("k_scale", "k_zero") else 32     # group 0: per group, or its 32 token rows
+        assert np.array_equal(a[name][:, :, :n], b[name][:, :, :n]), name
+    assert int(a["sink_mask"][0, 0]) == 0xFFFFFFFF
+    pos, K, V, pool = c.read_set(0, 0, 0)
+    assert np.array_equal(pool[pos < 32], np.zeros(32, np.int64))
