@@ -222,7 +222,9 @@ kv_status check_layer(const kv_cache* c, int layer) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-kv_status do_append(kv_cache* c, int layer, const void* k, const void* v, int n, void* stream, bool prefill) {
+// kv_append and kv_prefill_quantize: one state change; the group flush
+// quantises every group the call completes in one launch, however many.
+kv_status do_append(kv_cache* c, int layer, const void* k, const void* v, int n, void* stream) {
   kv_status st = check_layer(c, layer);
   if (st != KV_OK) return st;
   if (!k || !v) return fail(KV_ERR_INVALID_ARG, "k/v is NULL");
@@ -238,7 +240,6 @@ kv_status do_append(kv_cache* c, int layer, const void* k, const void* v, int n,
   // KVSink: every call (append or prefill) folds its tokens into the
   // running top-k before its groups are quantised
   const bool select = g.n_dyn > 0;
-  (void)prefill;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   kvq::AppendArgs a{};
@@ -384,12 +385,12 @@ kv_status kv_cache_reset(kv_cache* cache) {
 }
 
 kv_status kv_append(kv_cache* cache, int layer, const void* k, const void* v, int n_new, void* cuda_stream) {
-  return do_append(cache, layer, k, v, n_new, cuda_stream, false);
+  return do_append(cache, layer, k, v, n_new, cuda_stream);
 }
 
 kv_status kv_prefill_quantize(kv_cache* cache, int layer, const void* k, const void* v, int n_tokens,
                               void* cuda_stream) {
-  return do_append(cache, layer, k, v, n_tokens, cuda_stream, true);
+  return do_append(cache, layer, k, v, n_tokens, cuda_stream);
 }
 
 kv_status kv_evict(kv_cache* cache, int layer, int64_t* evicted_begin, int64_t* evicted_end) {
