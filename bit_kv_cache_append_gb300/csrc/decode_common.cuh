@@ -482,7 +482,7 @@ __device__ bool exact_states_tc(const DecodeArgs& a, int b, int h, float* red, u
           // re-positioning: the sink rows of this tile meet the query
           // rotated at sink_qpos; their scores again with that operand
           float ss[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
-#pragma unroll
+#pragma unroll 1  // one tile per decode: kept rolled, it costs the instance no registers
           for (int s = 0; s < S; ++s) {
             uint32_t qs[2];
 #pragma unroll
