@@ -5,10 +5,11 @@
 // KV head) unit is a run of 32-token groups; all units' groups form one flat
 // list cut into n_ctas equal contiguous ranges, one per persistent CTA
 // (n_ctas = SM count x resident CTAs). A CTA walks its range unit by unit;
-// for each unit it touches, its 4 warp pairs take the unit's groups in turn
-// (p, p+4, ...) and the CTA merges the pairs into one partial (max, sum,
-// unnormalised output) per query head. The exact pools (sinks and tail) are
-// left to the merge kernel, which combines them with every partial of a
+// for each unit it touches, its 4 warp pairs take the unit's groups in runs
+// of two consecutive groups (runs p, p+4, ...; one group per run where a
+// chunk exceeds 6 KB) and the CTA merges the pairs into one partial (max,
+// sum, unnormalised output) per query head. The exact pools (sinks and tail)
+// are left to the merge kernel, which combines them with every partial of a
 // (sequence, query head).
 //
 // Warp specialisation: a pair is a QK warp and a PV warp working on the same
@@ -16,9 +17,11 @@
 // weights and hands the weights (and the rescale factor of the running max)
 // to the PV warp through a double-buffered shared-memory slot; the PV warp
 // turns the V codes into the weighted sum and, being the last reader of each
-// staged chunk, refills the stage with the next 1-D bulk copy. Each role
-// keeps only its own operands in registers, so more warps fit per SM and the
-// two halves of a group's dependency chain overlap across groups.
+// staged run, refills the stage with the next run (one 1-D bulk copy when
+// its chunks are adjacent in the ring); three stages per pair where they
+// leave room for two CTAs per SM, else two. Each role keeps only its own
+// operands in registers, so more warps fit per SM and the two halves of a
+// group's dependency chain overlap across groups.
 //
 // Per group, on the tensor cores (mma.sync m16n8k16, f16 in, f32 out):
 //   scores^T [32 tokens x 8 cols] = zeros-row . q + codes_K [32 x D] . qt
@@ -30,12 +33,14 @@
 // and the zero points: the K zeros enter as a row of the MMA (sum_c zK[c]
 // q_j[c]), the V zeros as fp32 sums sum_t p_j[t] zV[t][c/32].
 // The codes enter the MMA exactly, as code * unit in f16 with a power-of-two
-// unit undone on the fp32 sums (code_pair). The 8 MMA columns
-// hold, for query head j, column 2j = the f16 value of the folded operand
-// and column 2j+1 its f16 residual, so each product is carried at about 22
-// bits and thread (g, t) of a C fragment owns query head t. The residuals of
-// q * sK and p * sV are formed exactly in f16 (an FMA returns
-// x_hi * s - f16(x_hi * s) without rounding).
+// unit undone on the fp32 sums (code_pair). In the score MMA the 8 columns
+// hold, for query head j, column 2j = the f16 value of q * sK and column
+// 2j+1 its f16 residual, formed exactly by an FMA (x * s - f16(x * s) has no
+// rounding), so the product is carried at about 22 bits: a score error is
+// amplified by the exponential. In the value MMA the weight p of a token is
+// one f16 value in the even columns (the odd ones are zero) and p * sV one f16
+// product, made on the transposed weights: the errors of the weights average
+// over tokens. Thread (g, t) of a C fragment owns query head t.
 //
 // Every wait is bounded; a wait that gives up raises the CTA's abort flag so
 // that every other wait of the CTA gives up at once.
