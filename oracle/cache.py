@@ -73,6 +73,7 @@ class CacheConfig:
     seed: int = 0
     rope_base: float = 0.0
     rope_reposition: bool = False   # StreamingLLM position re-encoding at read
+    v_q4_0: bool = False            # V in the symmetric q4_0 form (KIVI, 4-bit V)
 
 
 def validate(cfg: CacheConfig) -> None:
@@ -98,6 +99,8 @@ def validate(cfg: CacheConfig) -> None:
         raise ValueError(f"unknown mode {cfg.mode!r}")
     if min(cfg.n_sink, cfg.window, cfg.evict_window, cfg.n_dyn_sinks) < 0:
         raise ValueError("negative size")
+    if cfg.v_q4_0 and (cfg.mode != "kivi" or cfg.v_bits != 4):
+        raise ValueError("the q4_0 V form is a 4-bit KIVI V format")
     if cfg.rope_reposition and not cfg.rope_base:
         raise ValueError("re-positioning needs the cache to apply RoPE")
     if cfg.n_dyn_sinks and (cfg.n_sink or cfg.window or cfg.evict_window):
@@ -282,7 +285,10 @@ class OracleCache:
                         kr[b, :, i] = kvsink.exclude(kr[b, :, i], sink_rows)
                         vr[b, :, i] = kvsink.exclude(vr[b, :, i], sink_rows)
         kq, ks, kz = kivi.quantize_k_group(kr, cfg.k_bits)      # [B,H,ng,32,D], [B,H,ng,D]
-        vq, vs, vz = kivi.quantize_v_rows(vr, cfg.v_bits)       # [B,H,ng,32,D], [B,H,ng,32,D/32]
+        if cfg.v_q4_0:
+            vq, vs, vz = kivi.quantize_v_rows_q4_0(vr)
+        else:
+            vq, vs, vz = kivi.quantize_v_rows(vr, cfg.v_bits)   # [B,H,ng,32,D], [B,H,ng,32,D/32]
         for i in range(ng):
             st.groups[g0 + i] = dict(kq=kq[:, :, i], ks=ks[:, :, i], kz=kz[:, :, i],
                                      vq=vq[:, :, i], vs=vs[:, :, i], vz=vz[:, :, i],

@@ -103,6 +103,38 @@ def quantize_v_rows(v_rows: np.ndarray, bits: int):
     return q.reshape(*lead, T, D), s, z
 
 
+def quantize_slices_q4_0(x: np.ndarray):
+    """The symmetric 4-bit block format P3 names for V ("`--kv q2k`": "V at 4
+    bits per token (q4_0)"), as its public definition has it: per slice of 32,
+    m = the value of largest magnitude (the first on ties), d = m / -8, code
+    q = min(15, floor(x / d + 8.5)) and value (q - 8) d. Written in the affine
+    form of this cache: scale d, zero -8 d (exact in fp16). Readings: d is
+    stored in fp16 and the codes use the stored value, like KIVI's; a slice
+    of zeros has d = 0 and every code 8.
+
+    x: float32 [..., n]. Returns (codes uint8 [..., n], scale fp16 [...],
+    zero fp16 [...]).
+    """
+    x = np.asarray(x, np.float32)
+    _check_finite(x)
+    idx = np.argmax(np.abs(x), axis=-1)                      # first index of the largest |x|
+    m = np.take_along_axis(x, idx[..., None], axis=-1)[..., 0]
+    d_h = (m / np.float32(-8.0)).astype(np.float16)           # fp32 division, stored fp16
+    z_h = (d_h.astype(np.float32) * np.float32(-8.0)).astype(np.float16)
+    d = d_h.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = np.floor((x / d) + np.float32(8.5))               # fp32 divide, fp32 add
+    q = np.where(d == 0, np.float32(8.0), np.clip(t, np.float32(0.0), np.float32(15.0)))
+    return q.astype(np.uint8), d_h, z_h
+
+
+def quantize_v_rows_q4_0(v_rows: np.ndarray):
+    """V per token over 32-channel groups in the symmetric q4_0 form."""
+    *lead, T, D = v_rows.shape
+    q, s, z = quantize_slices_q4_0(v_rows.reshape(*lead, T, D // GROUP, GROUP))
+    return q.reshape(*lead, T, D), s, z
+
+
 def dequantize_v_rows(codes, s_h, z_h) -> np.ndarray:
     *lead, T, D = codes.shape
     x = dequantize_slices(codes.reshape(*lead, T, D // GROUP, GROUP), s_h, z_h)

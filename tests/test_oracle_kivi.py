@@ -149,3 +149,48 @@ def test_pack_layout_v0_in_low_bits():
     assert kivi.pack_codes(np.array([[7, 7, 0, 1]], np.uint8), 3).tolist() == [[0b00111111, 0b00001000]]
     assert kivi.pack_codes(np.array([[0xA, 0x5]], np.uint8), 4)[0, 0] == 0x5A
     assert list(kivi.pack_codes(np.array([[7, 200]], np.uint8), 8)[0]) == [7, 200]
+
+
+# ------------------------------------------------------------------ q4_0 V form
+
+def _slice(vals):
+    x = np.zeros(32, np.float32)
+    x[:len(vals)] = vals
+    return x
+
+
+def test_q4_0_worked_slices():
+    """d = m / -8 with m the first value of largest magnitude; code
+    floor(x / d + 8.5) clamped to [0, 15]; value (code - 8) d."""
+    q, s, z = kivi.quantize_slices_q4_0(_slice([1.0, -2.0, 0.5, 0.75]))
+    assert float(s) == 0.25 and float(z) == -2.0
+    assert q[:5].tolist() == [12, 0, 10, 11, 8]
+    # a positive extreme gives a negative d; -1 lands between levels
+    q, s, z = kivi.quantize_slices_q4_0(_slice([3.0, -1.0]))
+    assert float(s) == -0.375 and float(z) == 3.0
+    assert q[:3].tolist() == [0, 11, 8]
+    # equal magnitudes: the first decides the sign; the other one clamps at 15
+    q, s, z = kivi.quantize_slices_q4_0(_slice([-4.0, 4.0]))
+    assert float(s) == 0.5 and q[:2].tolist() == [0, 15]
+    # all zeros: d = 0 and every code 8
+    q, s, z = kivi.quantize_slices_q4_0(np.zeros(32, np.float32))
+    assert float(s) == 0.0 and float(z) == 0.0 and np.all(q == 8)
+
+
+def test_q4_0_nearest_level_brute_force_and_affine_readback():
+    """Away from the clamp each code is the nearest level (code - 8) d, ties
+    upwards, within |d| / 2; the affine read-back code * s + z equals
+    (code - 8) d exactly."""
+    rng = np.random.default_rng(11)
+    x = _fp16_values(rng, (400, 32), 3.0)
+    q, s, z = kivi.quantize_slices_q4_0(x)
+    d = s.astype(np.float64)[:, None]
+    lv = (np.arange(16)[None, None, :] - 8) * d[..., None]          # [400, 1, 16]
+    deq = kivi.dequantize_slices(q, s, z).astype(np.float64)
+    assert np.array_equal(deq, (q.astype(np.float64) - 8) * d)
+    x64 = x.astype(np.float64)
+    free = (x64 / d) < 7.5 - 1e-6                                   # not clamped at 15
+    err = np.abs(x64[..., None] - lv)                               # [400, 32, 16]
+    best = err.min(axis=-1)
+    assert np.all(np.abs(x64 - deq)[free] <= np.abs(d).repeat(32, 1)[free] / 2 + 1e-6)
+    assert np.all(np.abs(np.abs(x64 - deq) - best)[free] <= 1e-6)
