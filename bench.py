@@ -451,6 +451,8 @@ OTHER_WORKLOADS = {
                             mode="turboquant", k_bits=4, v_bits=4),
     "turboquant_k3v2": dict(batch=32, n_kv_heads=8, n_q_heads=32, head_dim=128, context=16384, act_dtype="f16",
                             mode="turboquant", k_bits=3, v_bits=2),
+    "llama8b_q4_0v": dict(batch=16, n_kv_heads=8, n_q_heads=32, head_dim=128, context=32768, act_dtype="bf16",
+                          mode="kivi", k_bits=2, v_bits=4, v_q4_0=True),
     "kvsink": dict(batch=4, n_kv_heads=8, n_q_heads=32, head_dim=128, context=131072, act_dtype="f16",
                    mode="kivi", k_bits=2, v_bits=2, n_dyn_sinks=5),
     "ring_int8": dict(batch=64, n_kv_heads=8, n_q_heads=8, head_dim=64, context=4100, act_dtype="f16",
@@ -481,7 +483,7 @@ def run_workload(args):
                k_bits=w["k_bits"], v_bits=w["v_bits"], n_sink=w.get("n_sink", 0), window=0,
                evict_window=w.get("evict_window", 0), n_dyn_sinks=w.get("n_dyn_sinks", 0), act_dtype=w["act_dtype"],
                rope_base=w.get("rope_base", 0.0), rope_max_pos=(L + n_total + 64 if w.get("rope_base") else 0),
-               rope_reposition=w.get("rope_reposition", False))
+               rope_reposition=w.get("rope_reposition", False), v_q4_0=w.get("v_q4_0", False))
     warm_prefill(torch, binding, dev, cfg, dt)
     cache = binding.KVCache(device=dev, **cfg)
     g = torch.Generator(device=dev)

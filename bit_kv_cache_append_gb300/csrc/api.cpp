@@ -103,6 +103,8 @@ kv_status check_config(const kv_cache_config* c) {
   if (c->max_tokens > (static_cast<int64_t>(1) << 40)) return fail(KV_ERR_INVALID_ARG, "max_tokens too large");
   if (!(c->rope_base >= 0.0)) return fail(KV_ERR_INVALID_ARG, "rope_base must be >= 0");
   if (c->rope_base > 0.0 && c->rope_max_pos < 1) return fail(KV_ERR_INVALID_ARG, "rope_max_pos must be >= 1");
+  if (c->v_q4_0 && (c->mode != KV_MODE_KIVI || c->v_bits != 4))
+    return fail(KV_ERR_INVALID_ARG, "v_q4_0 is a 4-bit KIVI V format");
   if (c->rope_reposition && !(c->rope_base > 0.0))
     return fail(KV_ERR_INVALID_ARG, "rope_reposition needs the cache to apply RoPE (rope_base > 0)");
   if (c->max_splits < 0 || c->max_splits > 4096) return fail(KV_ERR_INVALID_ARG, "max_splits out of range");
@@ -132,6 +134,7 @@ Geometry make_geometry(const kv_cache_config* c) {
   g.chunk = kvq::chunk_layout(g.mode_tq, g.D, kvq::storage_bits(g.kb), kvq::storage_bits(g.vb));
   g.rope_max_pos = c->rope_base > 0.0 ? c->rope_max_pos : 0;
   g.rope_repos = c->rope_reposition ? 1 : 0;
+  g.v_q4_0 = c->v_q4_0 ? 1 : 0;
 
   const size_t B = g.B, H = g.H, D = g.D;
   size_t off = 0;

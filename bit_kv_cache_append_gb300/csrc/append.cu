@@ -197,13 +197,42 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
       mx = fmaxf(mx, x);
     }
     __half sh, zh;
-    float s, z;
-    quantize_slice_params(mn, mx, VB, &sh, &zh, &s, &z);
-    const float rs = __frcp_rn(s);
+    if (VB == 4 && G.v_q4_0) {
+      // the symmetric q4_0 form ([P3] "Summary"): d = m / -8 with m the value
+      // of largest magnitude (the first in channel order on ties), code
+      // min(15, floor(x / d + 8.5)) from the stored d, zero -8 d
+      float m = 0.0f, am = -1.0f;
+      int mi = 32;
 #pragma unroll 8
-    for (int i = 0; i < 32; ++i) {
-      const int c = base + ((i + 8 * vg) & 31);
-      cv[r][c] = static_cast<uint8_t>(quantize_code<LV>(act_to_float(xv[r][c], bf16), s, z, rs));
+      for (int i = 0; i < 32; ++i) {
+        const int j = (i + 8 * vg) & 31;
+        const float x = act_to_float(xv[r][base + j], bf16);
+        const float ax = fabsf(x);
+        if (ax > am || (ax == am && j < mi)) {
+          am = ax;
+          m = x;
+          mi = j;
+        }
+      }
+      sh = __float2half_rn(__fdiv_rn(m, -8.0f));
+      const float d = __half2float(sh);
+      zh = __float2half_rn(__fmul_rn(d, -8.0f));  // exact: a power-of-two multiple
+#pragma unroll 8
+      for (int i = 0; i < 32; ++i) {
+        const int c = base + ((i + 8 * vg) & 31);
+        float q = 8.0f;
+        if (d != 0.0f) q = fminf(fmaxf(floorf(__fadd_rn(__fdiv_rn(act_to_float(xv[r][c], bf16), d), 8.5f)), 0.0f), 15.0f);
+        cv[r][c] = static_cast<uint8_t>(q);
+      }
+    } else {
+      float s, z;
+      quantize_slice_params(mn, mx, VB, &sh, &zh, &s, &z);
+      const float rs = __frcp_rn(s);
+#pragma unroll 8
+      for (int i = 0; i < 32; ++i) {
+        const int c = base + ((i + 8 * vg) & 31);
+        cv[r][c] = static_cast<uint8_t>(quantize_code<LV>(act_to_float(xv[r][c], bf16), s, z, rs));
+      }
     }
     __half* vm = reinterpret_cast<__half*>(chunk + G.chunk.vmeta_off);
     vm[vscale_pos(NV, r, vg)] = sh;

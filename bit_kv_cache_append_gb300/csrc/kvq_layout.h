@@ -147,6 +147,7 @@ struct Geometry {
   int mode_tq, kb, vb;
   int n_sink, window, evict_window, n_dyn;
   int rope_repos;     // StreamingLLM position re-encoding at read
+  int v_q4_0;         // V in the symmetric q4_0 form (scale d, zero -8 d)
   int act_bf16;
   int64_t max_tokens;
   int n_slots;        // group chunks per (layer, b, h)

@@ -102,6 +102,13 @@ typedef struct {
                          rows against the query rotated at
                          L - 1 - (E - n_sink) and everything else as in the
                          vanilla scheme. 0: vanilla (absolute positions)    */
+  int v_q4_0;         /* 1 (KIVI, v_bits = 4): V in the symmetric q4_0 form
+                         ([P3] "Summary": V at 4 bits per token, q4_0): per
+                         32 values d = m / -8 with m the value of largest
+                         magnitude (the first on ties), code
+                         min(15, floor(x / d + 8.5)), value (code - 8) d;
+                         stored as scale d and zero -8 d (fp16), codes from
+                         the stored d. 0: the KIVI min/max affine form      */
 } kv_cache_config;
 
 typedef struct kv_cache kv_cache; /* opaque host-side handle */

@@ -46,7 +46,8 @@ def oracle_config(kw):
                        v_bits=kw["v_bits"], n_sink=kw["n_sink"], window=kw["window"],
                        evict_window=kw["evict_window"], n_dyn_sinks=kw["n_dyn_sinks"],
                        act_dtype=kw["act_dtype"], seed=kw["seed"], rope_base=kw["rope_base"],
-                       rope_reposition=bool(kw.get("rope_reposition", False)))
+                       rope_reposition=bool(kw.get("rope_reposition", False)),
+                       v_q4_0=bool(kw.get("v_q4_0", False)))
 
 
 def compare_exports(gpu_cache, oc, layer: int) -> None:

@@ -70,7 +70,7 @@ def test_config_validation_on_host(lib):
     bad = [dict(head_dim=96), dict(n_q_heads=3), dict(n_q_heads=16), dict(k_bits=5),
            dict(evict_window=16), dict(n_dyn_sinks=5, n_sink=4), dict(mode="turboquant", k_bits=8),
            dict(max_tokens=8), dict(n_sink=33), dict(n_dyn_sinks=40), dict(mode="turboquant", n_dyn_sinks=2),
-           dict(rope_reposition=True)]
+           dict(rope_reposition=True), dict(v_q4_0=True, v_bits=2), dict(mode="turboquant", v_q4_0=True)]
     for kw in bad:
         st, _ = _status(lib, **kw)
         assert st in (B.KV_ERR_INVALID_ARG, B.KV_ERR_UNSUPPORTED), kw

@@ -174,3 +174,32 @@ def test_layers_are_independent(n_layers):
     for layer in range(n_layers):
         compare_exports(gc, oc, layer)
         _decode_both(gc, oc, layer, W.queries(w, 30 + layer), "f16")
+
+
+@pytest.mark.parametrize("kb,act", [(2, "bf16"), (4, "f16")])
+@pytest.mark.parametrize("D,H,Hq", [(128, 8, 32), (64, 4, 8)])
+def test_v_q4_0_prefill_then_appends(kb, act, D, H, Hq):
+    """V in the symmetric q4_0 form: prefill 1000 tokens (with a few rows of
+    zeros and of equal-magnitude values of both signs), then appends; codes,
+    scales and zeros bit-exact, attention within tolerance (the decode reads
+    it as scale d, zero -8 d)."""
+    w = W.scaled(W.WORKLOADS["llama8b"], batch=2, n_kv_heads=H, n_q_heads=Hq, head_dim=D, context=2048,
+                 k_bits=kb, v_bits=4, act_dtype=act)
+    kw = cache_kwargs(w, 2048, v_q4_0=True)
+    gc, oc = _pair(kw)
+    k, v = W.kv_tokens(w, 8, 1000)
+    v[:, :, 10, :] = 0.0                          # d = 0: every code 8
+    v[:, :, 11, :32] = 0.0
+    v[:, :, 11, 3], v[:, :, 11, 7] = -2.0, 2.0    # the first extreme sets the sign; 2.0 clamps at 15
+    gc.prefill_quantize(0, torch_act(k, act), torch_act(v, act))
+    oc.prefill_quantize(0, k, v)
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 8, 0), act)
+    pos = 1000
+    for i, n in enumerate([1, 3, 31, 1, 32, 7, 64, 1] * 2):
+        k, v = W.kv_tokens(w, 8, n, first_pos=pos)
+        gc.append(0, torch_act(k, act), torch_act(v, act))
+        oc.append(0, k, v)
+        pos += n
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 8, 1), act)
