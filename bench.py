@@ -42,6 +42,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Quantised-KV decode attn: HBM GB/s (% of peak), µs/step; append tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+APPEND_CALLS = 256  # kv_append calls timed on their own
 WORKLOAD = dict(batch=16, n_q_heads=32, n_kv_heads=8, head_dim=128, context=32768, act_dtype="bf16",
                 k_bits=2, v_bits=4, n_sink=4, window=128, layers_reported=32)
 WORKLOAD_NAME = ("llama8b decode attention: B16 Hq32 Hkv8 D128 context 32768 bf16, "
@@ -135,31 +136,31 @@ class ClockSampler:
 
 DECODE_SOURCES = ("decode_kivi.cuh", "decode_common.cuh", "decode.cu", "decode_d128.cu", "kvq_layout.h",
                   "kvq_internal.h", "kvq_device.cuh")
-TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "decode_llama8b_b8.md")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "decode_traffic_llama8b.json")
 
 
-def recorded_traffic():
-    """DRAM bytes (read + write) of one decode (split + merge) at batch 16,
-    from the committed ncu summary, if that capture was taken on the decode
-    sources as they are now (their sha256 is recorded beside the figure);
-    None otherwise."""
+def decode_sources_sha256():
+    """sha256 of the decode kernels' sources, concatenated in DECODE_SOURCES order."""
     import hashlib
     h = hashlib.sha256()
     for f in DECODE_SOURCES:
         with open(os.path.join(ROOT, "bit_kv_cache_append_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    fields = {}
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes (read + write) of one decode at batch 16 from the ncu
+    capture recorded in TRAFFIC_RECORD, if that capture was taken on the
+    decode sources as they are now; None otherwise."""
     try:
         with open(TRAFFIC_RECORD) as fh:
-            for line in fh:
-                if line.startswith("- ") and ": " in line:
-                    k, v = line[2:].split(": ", 1)
-                    fields[k.strip()] = v.strip()
-    except OSError:
+            rec = json.load(fh)
+    except (OSError, ValueError):
         return None
-    if fields.get("decode_sources_sha256") != h.hexdigest() or "dram_bytes_per_launch_b16" not in fields:
+    if rec.get("decode_sources_sha256") != decode_sources_sha256():
         return None
-    return int(fields["dram_bytes_per_launch_b16"])
+    return int(rec["dram_bytes_per_launch_b16"])
 
 
 def make_inputs(torch, w, seed, n_tokens, device):
@@ -234,8 +235,9 @@ def unit_bytes(oc):
 
 def cpu_baseline(repeats=6, seed=7):
     """The oracle as it stands, on a bounded sample: one sequence of the
-    workload (8 KV-head units, 32 query heads) decoded `repeats` times.
-    Returns (GB/s over the sample's algorithmic bytes, seconds, units)."""
+    workload (8 KV-head units, 32 query heads) decoded `repeats` times on one
+    host core. Returns (GB/s over the sample's algorithmic bytes, seconds,
+    units)."""
     oc, q = oracle_sequence(seed)
     t0 = time.perf_counter()
     for _ in range(repeats):
@@ -243,6 +245,51 @@ def cpu_baseline(repeats=6, seed=7):
     t = time.perf_counter() - t0
     units = repeats * oc.cfg.n_kv_heads
     return units * unit_bytes(oc) / t / 1e9, t, units
+
+
+def host_cpu_model():
+    """The host CPU's model name (lscpu), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20).stdout
+        for line in out.splitlines():
+            if line.split(":", 1)[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _oracle_worker(seed, repeats, barrier, queue):
+    """One process of the all-cores leg: its own sequence of the workload in
+    the oracle (built untimed), then, once every process is ready, `repeats`
+    decodes of it. Puts (units, seconds, bytes per unit) on the queue."""
+    oc, q = oracle_sequence(seed)
+    barrier.wait()
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        oc.decode_attn(0, q)
+    queue.put((repeats * oc.cfg.n_kv_heads, time.perf_counter() - t0, unit_bytes(oc)))
+
+
+def cpu_baseline_all_cores(repeats=2, n_proc=None):
+    """The oracle on every host core: one spawned process per core, each
+    decoding its own sequence (8 KV-head units) `repeats` times, all timed
+    together. Returns (GB/s over all processes' algorithmic bytes, seconds of
+    the slowest process, units, processes)."""
+    import multiprocessing
+    n_proc = n_proc or os.cpu_count() or 1
+    ctx = multiprocessing.get_context("spawn")
+    barrier, queue = ctx.Barrier(n_proc), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(100 + i, repeats, barrier, queue)) for i in range(n_proc)]
+    for p in procs:
+        p.start()
+    res = [queue.get() for _ in procs]
+    for p in procs:
+        p.join()
+    units = sum(r[0] for r in res)
+    t = max(r[1] for r in res)
+    return units * res[0][2] / t / 1e9, t, units, n_proc
 
 
 def run_reference(args, rank, world):
@@ -283,11 +330,11 @@ def run_ours(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
         pg = dist
-    w = dict(WORKLOAD, batch=args.batch)
+    w = dict(WORKLOAD, batch=args.batch or WORKLOAD["batch"])
     L = w["context"]
     n_steps_total = args.warmup + args.steps + 2
     ccfg = dict(n_layers=1, batch=w["batch"], n_kv_heads=w["n_kv_heads"], n_q_heads=w["n_q_heads"],
-                head_dim=w["head_dim"], max_tokens=L + 2 * n_steps_total + 64, k_bits=w["k_bits"],
+                head_dim=w["head_dim"], max_tokens=L + 2 * n_steps_total + APPEND_CALLS + 64, k_bits=w["k_bits"],
                 v_bits=w["v_bits"], n_sink=w["n_sink"], window=w["window"], act_dtype="bf16")
     warm_prefill(torch, binding, dev, ccfg, torch.bfloat16)
     cache = binding.KVCache(device=dev, **ccfg)
@@ -315,23 +362,28 @@ def run_ours(args, rank, world, local):
         cache.append(0, nk[i], nv[i])
         cache.decode_attn(0, q, out=out)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    stats0 = cache.stats(0)
-    # per-step events around the decode kernels (split + merge, recorded by the library)
+    # per-step events around the decode kernels (recorded by the library)
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a, b in kev:
         a.record(stream)
         b.record(stream)
+    # clocks are sampled from here to the end of the timed region, all of it
+    # under load: a ramp of untimed decodes of the same state (L unchanged)
+    # for about 0.4 s, the warm-up steps, then the timed steps
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_ramp = time.perf_counter()
+    while time.perf_counter() - t_ramp < 0.4:
+        for _ in range(200):
+            cache.decode_attn(0, q, out=out)
+        torch.cuda.synchronize()
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize()
-    bytes_steps = []
+    stats0 = cache.stats(0)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
     launches0 = binding.launch_count()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -358,6 +410,17 @@ def run_ours(args, rank, world, local):
             print(json.dumps({"ms_per_step": ms_total / args.steps, "kernel_us": kernel_avg_ms * 1e3,
                               "decode_bytes": int(dec_bytes), "launches": int(launches)}), flush=True)
         return
+    # kv_append alone: APPEND_CALLS calls of one token each, back to back
+    # (the tail write, and the group flush of every 32nd call)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a0.record(stream)
+    for i in range(APPEND_CALLS):
+        cache.append(0, nk[i % n_steps_total], nv[i % n_steps_total])
+    a1.record(stream)
+    torch.cuda.synchronize()
+    append_tok_s = w["batch"] * APPEND_CALLS / (a0.elapsed_time(a1) / 1e3)
+
     # e2e: host buffers through the public API, copies inside the timed region
     hk = nk[: args.steps].cpu().pin_memory()
     hv = nv[: args.steps].cpu().pin_memory()
@@ -408,6 +471,8 @@ def run_ours(args, rank, world, local):
     achieved = dec_bytes / (kernel_avg_ms / 1e3) / 1e9
     if rank == 0:
         cpu_gbs, cpu_t, cpu_n = cpu_baseline(repeats=args.cpu_repeats)
+        all_gbs, all_t, all_n, all_p = cpu_baseline_all_cores()
+        cpu_model = host_cpu_model()
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
@@ -419,20 +484,25 @@ def run_ours(args, rank, world, local):
             "us_per_step": round(ms_step * 1e3, 2),
             "us_per_model_step_x32": round(ms_step * 1e3 * w["layers_reported"], 1),
             "pct_of_peak": round(100 * achieved / peak, 2),
-            "append_tokens_per_s": round(w["batch"] / (ms_step / 1e3), 1),
+            "append_tokens_per_s": round(append_tok_s, 1),
+            "append_note": f"kv_append alone, {APPEND_CALLS} one-token calls back to back (B tokens per call)",
             "prefill_tokens_per_s": round(prefill_tok_s, 1),
             "copy_kernel_gbs": round(copy_gbs, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
                          "traffic": recorded_traffic() if w["batch"] == 16 else None,
-                         "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of split + merge "
-                                           "at batch 8, scaled by units to batch 16 (profiles/decode_llama8b_b8.md)",
+                         "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the decode "
+                                           "kernels at batch 8, scaled by units to batch 16 (profiles/)",
                          "kernel": "decode_kivi_kernel<128,2,4> + merge_kernel<128> (split-KV partitions; exact pools and LSE merge)",
                          "algorithmic_bytes_per_launch": int(dec_bytes), "peak_kind": f"{peak_kind} hbm_gbs",
                          "kernel_us": round(kernel_avg_ms * 1e3, 2)},
-            "cpu_baseline": {"value": round(cpu_gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{cpu_n} (sequence, KV head) units with 4 query heads each, "
-                                       f"32768-token context, decode only ({cpu_t:.1f} s)"},
+            "cpu_baseline": {"value": round(all_gbs, 6), "unit": "GB/s", "cores": all_p, "kind": "oracle",
+                             "sample": f"{all_n} (sequence, KV head) units with 4 query heads each over {all_p} "
+                                       f"spawned processes (one sequence each), 32768-token context, decode only "
+                                       f"({all_t:.1f} s, the slowest process)",
+                             "cpu_model": cpu_model,
+                             "one_core": {"value": round(cpu_gbs, 6), "unit": "GB/s", "cores": 1,
+                                          "sample": f"{cpu_n} units of one sequence, decode only ({cpu_t:.1f} s)"}},
             "e2e": {"value": round(whole_job_gbs(world, step_bytes, e2e_ms), 3), "unit": "GB/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
             "gpu_launches": int(launches),
@@ -472,7 +542,9 @@ def run_workload(args):
     device (timing does not depend on the values). Prints one JSON line."""
     import torch
     from bit_kv_cache_append_gb300 import binding
-    w = OTHER_WORKLOADS[args.workload]
+    w = dict(OTHER_WORKLOADS[args.workload])
+    if args.batch:
+        w["batch"] = args.batch
     dev = torch.device("cuda", 0)
     dt = torch.float16 if w["act_dtype"] == "f16" else torch.bfloat16
     B, H, Hq, D, L = w["batch"], w["n_kv_heads"], w["n_q_heads"], w["head_dim"], w["context"]
@@ -555,8 +627,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--batch", type=int, default=WORKLOAD["batch"],
-                    help="sequences (the workload has 16; smaller values give profiling cases)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences (0: the workload's own; smaller values give profiling cases)")
     ap.add_argument("--skip-extras", action="store_true",
                     help="time the steps only (no e2e, copy or CPU legs); prints a short line")
     ap.add_argument("--cpu-repeats", type=int, default=6,

@@ -27,7 +27,7 @@ SYMBOLS = ("kv_cache_required_bytes", "kv_cache_create", "kv_cache_destroy", "kv
            "kv_append", "kv_prefill_quantize", "kv_evict", "kv_decode_attn", "kv_cache_stats",
            "kv_cache_export_bytes", "kv_cache_export", "kv_cache_check_device_error",
            "kv_cache_set_timing_events", "kv_launch_count", "kv_copy_bandwidth_kernel",
-           "kv_last_error", "kv_decode_attn_noalloc")
+           "kv_last_error", "kv_decode_attn_noalloc", "kv_cache_test_bounded_wait")
 
 
 class KVError(RuntimeError):
@@ -73,6 +73,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kv_cache_export_bytes": [vp, i32, i32, ctypes.POINTER(sz)],
         "kv_cache_export": [vp, i32, i32, vp, sz, vp],
         "kv_cache_check_device_error": [vp, vp],
+        "kv_cache_test_bounded_wait": [vp, i64, ctypes.POINTER(i64), vp],
         "kv_cache_set_timing_events": [vp, vp, vp],
         "kv_copy_bandwidth_kernel": [vp, vp, sz, vp],
     }
@@ -136,6 +137,16 @@ def _dptr(t) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _check_f32_out(t, shape, device, name):
+    """An output tensor the library writes: float32, contiguous, on the
+    cache's device and of the exact shape (the C side sees only a pointer)."""
+    import torch
+    if t.dtype != torch.float32 or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be float32 of shape {list(shape)}")
+    if not t.is_cuda or t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor on {device}")
+
+
 class KVCache:
     """One quantised KV cache in a torch-allocated device arena."""
 
@@ -147,6 +158,7 @@ class KVCache:
         self.device = torch.device(device or "cuda")
         nbytes = required_bytes(self.cfg)
         self.arena = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        self.device = self.arena.device  # with its index ("cuda" alone has none)
         h = ctypes.c_void_p()
         check(lib().kv_cache_create(ctypes.byref(self.cfg), _dptr(self.arena), nbytes, ctypes.byref(h)))
         self.handle = h
@@ -186,14 +198,23 @@ class KVCache:
         check(lib().kv_evict(self.handle, layer, ctypes.byref(b), ctypes.byref(e)))
         return b.value, e.value
 
-    def decode_attn(self, layer, q, out=None, lse=None, stream=None):
-        import torch
+    def _decode_args(self, q, out, lse):
         c = self.cfg
         if q.dtype != self.act_dtype or tuple(q.shape) != (c.batch, c.n_q_heads, c.head_dim):
             raise ValueError("q must be [B, Hq, D] in the activation dtype")
+        if not q.is_cuda or q.device != self.device:
+            raise ValueError(f"q must be on {self.device}")
+        _check_f32_out(out, (c.batch, c.n_q_heads, c.head_dim), self.device, "out")
+        if lse is not None:
+            _check_f32_out(lse, (c.batch, c.n_q_heads), self.device, "lse")
+        return _dptr(lse) if lse is not None else None
+
+    def decode_attn(self, layer, q, out=None, lse=None, stream=None):
+        import torch
+        c = self.cfg
         if out is None:
-            out = torch.empty((c.batch, c.n_q_heads, c.head_dim), dtype=torch.float32, device=q.device)
-        lp = _dptr(lse) if lse is not None else None
+            out = torch.empty((c.batch, c.n_q_heads, c.head_dim), dtype=torch.float32, device=self.device)
+        lp = self._decode_args(q, out, lse)
         check(lib().kv_decode_attn(self.handle, layer, _dptr(q), _dptr(out), lp, _stream_ptr(stream)))
         return out
 
@@ -201,10 +222,7 @@ class KVCache:
         """kv_decode_attn_noalloc: decode into caller-given `out` (and `lse`)
         with the partials in the library's fixed device block; allocates
         nothing."""
-        c = self.cfg
-        if q.dtype != self.act_dtype or tuple(q.shape) != (c.batch, c.n_q_heads, c.head_dim):
-            raise ValueError("q must be [B, Hq, D] in the activation dtype")
-        lp = _dptr(lse) if lse is not None else None
+        lp = self._decode_args(q, out, lse)
         check(lib().kv_decode_attn_noalloc(self.handle, layer, _dptr(q), _dptr(out), lp, _stream_ptr(stream)))
         return out
 
@@ -255,6 +273,13 @@ class KVCache:
 
     def check_device_error(self, stream=None):
         check(lib().kv_cache_check_device_error(self.handle, _stream_ptr(stream)))
+
+    def test_bounded_wait(self, budget_cycles, stream=None):
+        """kv_cache_test_bounded_wait: the device waits run out on purpose;
+        returns the 5 result words (see kvq.h)."""
+        res = (ctypes.c_int64 * 5)()
+        check(lib().kv_cache_test_bounded_wait(self.handle, int(budget_cycles), res, _stream_ptr(stream)))
+        return [int(x) for x in res]
 
     def set_timing_events(self, ev_begin, ev_end):
         if ev_begin is None:

@@ -58,7 +58,6 @@ struct kv_cache {
   uint8_t* arena = nullptr;
   int device = 0;
   int sm_count = 0;
-  int split_ctas_per_sm = 4;
   int stream_ctas = 0;  // 0: SM count x occupancy
   std::vector<LayerState> layers;
   cudaEvent_t ev0 = nullptr, ev1 = nullptr;
@@ -332,7 +331,6 @@ kv_status kv_cache_create(const kv_cache_config* cfg, void* device_arena, size_t
   for (auto& l : c->layers) l.E = cfg->n_sink;
   cudaError_t e = cudaGetDevice(&c->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
-  if (const char* env = std::getenv("KVQ_SPLIT_CTAS_PER_SM")) c->split_ctas_per_sm = std::max(1, std::atoi(env));
   if (const char* env = std::getenv("KVQ_STREAM_CTAS")) c->stream_ctas = std::max(0, std::atoi(env));
   // host-built tables
   std::vector<float> tmp;
@@ -464,26 +462,13 @@ kv_status decode_attn_impl(kv_cache* cache, int layer, const void* q, float* out
     const int64_t g_end = (a.F + kGroup - 1) / kGroup;
     a.n_groups = static_cast<int>(g_end - a.g_begin);
     a.work = units * a.n_groups;
-    // TurboQuant partitions: about split_ctas_per_sm CTAs per SM in total
-    const int64_t target = static_cast<int64_t>(cache->sm_count) * cache->split_ctas_per_sm;
-    int64_t splits = (target + units - 1) / units;
-    splits = std::max<int64_t>(1, std::min<int64_t>({splits, g.max_splits, a.n_groups}));
-    a.groups_per_split = static_cast<int>((a.n_groups + splits - 1) / splits);
-    a.n_splits = static_cast<int>((a.n_groups + a.groups_per_split - 1) / a.groups_per_split);
   } else {
     a.g_begin = 0;
     a.n_groups = 0;
     a.work = 0;
-    a.groups_per_split = 0;
-    a.n_splits = 0;
   }
   a.n_ctas_hint = cache->stream_ctas;
   a.h2_magic = 0x64006400u;  // f16 1024.0 in both halves
-  for (int k = 0; k < 9; ++k) {  // 2^-k and -1024 * 2^-k as f16x2 (exact powers of two)
-    const uint32_t sc = static_cast<uint32_t>(15 - k) << 10, of = 0x8000u | (static_cast<uint32_t>(25 - k) << 10);
-    a.h2_scale[k] = sc | (sc << 16);
-    a.h2_offset[k] = of | (of << 16);
-  }
   a.ns = g.max_splits + 1;
   int64_t launches = 0;
   cudaError_t e = kvq::launch_decode(a, static_cast<cudaStream_t>(cuda_stream), cache->ev0, cache->ev1,
@@ -811,6 +796,27 @@ kv_status kv_cache_set_timing_events(kv_cache* cache, void* ev_begin, void* ev_e
   if ((ev_begin == nullptr) != (ev_end == nullptr)) return fail(KV_ERR_INVALID_ARG, "pass both events or neither");
   cache->ev0 = static_cast<cudaEvent_t>(ev_begin);
   cache->ev1 = static_cast<cudaEvent_t>(ev_end);
+  return KV_OK;
+}
+
+kv_status kv_cache_test_bounded_wait(kv_cache* cache, int64_t budget_cycles, int64_t* host_result,
+                                     void* cuda_stream) {
+  if (!cache) return fail(KV_ERR_INVALID_ARG, "cache is NULL");
+  if (!host_result) return fail(KV_ERR_INVALID_ARG, "host_result is NULL");
+  if (budget_cycles < 1000 || budget_cycles > (int64_t{1} << 31))
+    return fail(KV_ERR_INVALID_ARG, "budget_cycles must be in [1000, 2^31]");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  // the results go to the arena's error block, after the flag
+  long long* res = reinterpret_cast<long long*>(cache->arena + cache->geo.off_err + 64);
+  int64_t launches = 0;
+  cudaError_t e = cudaMemsetAsync(res, 0xff, 5 * sizeof(long long), s);
+  if (e == cudaSuccess)
+    e = kvq::launch_wait_probe(reinterpret_cast<int*>(cache->arena + cache->geo.off_err), res, budget_cycles, s,
+                               &launches);
+  g_launches += launches;
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(host_result, res, 5 * sizeof(long long), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_cache_test_bounded_wait");
   return KV_OK;
 }
 

@@ -200,6 +200,59 @@ __global__ void __launch_bounds__(256) copy_kernel(const uint4* __restrict__ src
 }
 }  // namespace
 
+// The bounded waits of the decode kernels made to run out, on purpose and
+// safely: two mbarriers that no thread arrives at and no copy completes on.
+// Warp 0 waits on the first with a short budget (warp_wait) and, giving up,
+// raises the CTA's abort flag; warp 1 waits on the second with the default
+// budget of about one second and must give up through that flag long before
+// its own budget; then thread 0 times out once more through wait_or_abort
+// (abort flag cleared first) and mbar_wait_bounded. res[0..3]: 1 where each
+// of the four waits returned "completed" (all must be 0), res[4]: SM clock
+// cycles warp 1 waited. Every give-up sets the error flag.
+namespace {
+__global__ void __launch_bounds__(64) wait_probe_kernel(int* err_flag, long long* res, long long budget) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  volatile int* ab = &abort_flag;
+  bool ok = false;
+  long long waited = 0;
+  if (warp == 0) {
+    ok = warp_wait(&bars[0], 0, ab, budget);
+  } else {
+    const long long t0 = clock64();
+    ok = warp_wait(&bars[1], 0, ab);
+    waited = clock64() - t0;
+  }
+  __syncthreads();
+  if (lane == 0) res[warp] = ok ? 1 : 0;
+  if (warp == 1 && lane == 0) res[4] = waited;
+  bool ok2 = false, ok3 = false;
+  if (threadIdx.x == 0) {
+    *ab = 0;
+    ok2 = wait_or_abort(&bars[0], 0, ab, budget);
+    ok3 = mbar_wait_bounded(&bars[0], 0, budget);
+    res[2] = ok2 ? 1 : 0;
+    res[3] = ok3 ? 1 : 0;
+  }
+  if (lane == 0 && (!ok || (threadIdx.x == 0 && (!ok2 || !ok3)))) set_error(err_flag, kErrTimeout);
+}
+}  // namespace
+
+cudaError_t launch_wait_probe(int* err_flag, long long* res, long long budget, cudaStream_t s,
+                              int64_t* launches) {
+  wait_probe_kernel<<<1, 64, 0, s>>>(err_flag, res, budget);
+  ++*launches;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_copy(const void* src, void* dst, size_t bytes, cudaStream_t s, int64_t* launches) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);

@@ -52,12 +52,13 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` for at most about one second of SM clock.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of `bar` for at most `budget` SM clock cycles
+// (about one second by default).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long budget = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > budget) return false;
   }
   return true;
 }
@@ -286,13 +287,15 @@ __device__ __forceinline__ void warp_fwht(float (&y)[D / 32]) {
   }
 }
 
-// Bounded wait that also gives up when another warp of the CTA has given up.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// Bounded wait (`budget` SM clock cycles, about one second by default) that
+// also gives up when another warp of the CTA has given up.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              long long budget = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > budget) {
       *abort_flag = 1;
       return false;
     }
@@ -356,16 +359,17 @@ constexpr int kExactTile = 32;
 // Warp-wide bounded wait for phase `parity` of `bar`: every decision is taken
 // by warp votes, so the warp stays converged and the common case (the phase
 // is already complete) costs one test and one vote. Gives up, raising the
-// CTA's abort flag, after about one second of SM clock or as soon as another
-// warp has raised it.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// CTA's abort flag, after `budget` SM clock cycles (about one second by
+// default) or as soon as another warp has raised it.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          long long budget = kWaitCycles) {
   const unsigned full = 0xffffffffu;
   if (__all_sync(full, mbar_test(bar, parity))) return true;
   const long long t0 = clock64();
   while (true) {
     if (__all_sync(full, mbar_try_wait(bar, parity))) return true;
     if (__any_sync(full, *abort_flag != 0)) return false;
-    if (__any_sync(full, clock64() - t0 > kWaitCycles)) {
+    if (__any_sync(full, clock64() - t0 > budget)) {
       *abort_flag = 1;
       return false;
     }

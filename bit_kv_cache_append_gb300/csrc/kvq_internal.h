@@ -60,23 +60,18 @@ struct DecodeArgs {
   int64_t L, F, qlo;    // quantised segment [qlo, F), tail [F, L)
   int64_t g_begin;      // first group of the quantised segment
   int n_groups;         // groups touching [qlo, F), per (sequence, KV head) unit
-  int64_t work;         // units * n_groups: the flat list the stream-K CTAs split
+  int64_t work;         // units * n_groups: the quantised items the stream-K CTAs split
   int n_ctas;           // stream-K CTAs (set at launch)
   int n_ctas_hint;      // 0 = SM count x occupancy
-  int groups_per_split; // TurboQuant: groups per partition
-  int n_splits;         // TurboQuant: quantised partitions
   int ns;               // partial slot stride per (sequence, query head)
   int n_sink_read;      // overlay: sink slots [0, n) read from the sink buffer
   int n_dyn_sel;        // KVSink: selected sinks (read when pos < F)
   int64_t sink_qpos;    // RoPE position of the query against the sink rows
                         // (L - 1, or L - 1 - (E - n_sink) when re-positioning)
   float qscale;         // log2(e) / sqrt(D)
-  // f16x2 constants of the code-to-f16 conversion, read from the parameter
-  // bank so that one instruction needs at most one immediate: the magic
-  // 1024.0 pair, and per shift k the scale 2^-k and offset -1024 * 2^-k.
+  // the f16x2 magic 1024.0 pair of the 8-bit code conversion, read from the
+  // parameter bank so that the instruction needs no second immediate
   uint32_t h2_magic;
-  uint32_t h2_scale[9];
-  uint32_t h2_offset[9];
 };
 
 // KVSink selection scratch.
@@ -109,6 +104,10 @@ cudaError_t launch_decode(DecodeArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEv
                           int64_t* launches);
 cudaError_t launch_copy(const void* src, void* dst, size_t bytes, cudaStream_t s,
                         int64_t* launches);
+// The decode kernels' bounded waits run out on barriers nobody completes
+// (a test of the give-up path; res: 5 device int64).
+cudaError_t launch_wait_probe(int* err_flag, long long* res, long long budget, cudaStream_t s,
+                              int64_t* launches);
 
 // Decode attention of one layer (the body of kv_decode_attn). With
 // `partials` NULL the split partials live in the cache's arena; otherwise in

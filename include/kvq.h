@@ -107,8 +107,14 @@ typedef struct {
                          32 values d = m / -8 with m the value of largest
                          magnitude (the first on ties), code
                          min(15, floor(x / d + 8.5)), value (code - 8) d;
-                         stored as scale d and zero -8 d (fp16), codes from
-                         the stored d. 0: the KIVI min/max affine form      */
+                         stored as scale d and zero -8 d (fp16). The codes
+                         divide x by the STORED fp16 d with a correctly
+                         rounded division (as the KIVI codes use the stored
+                         scale); the widely used q4_0 quantiser instead
+                         multiplies x by 1 / d of the fp32 d, so a code at
+                         a rounding boundary can differ by one step and the
+                         blocks are not interchangeable with such data.
+                         0: the KIVI min/max affine form                    */
 } kv_cache_config;
 
 typedef struct kv_cache kv_cache; /* opaque host-side handle */
@@ -231,6 +237,10 @@ kv_status kv_decode_attn(kv_cache* cache, int layer, const void* q, float* out,
  * The cache's device must be current (KV_ERR_INVALID_ARG otherwise). The
  * first call on a device looks up the block's device address once
  * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * The address is kept for the life of the process: after cudaDeviceReset
+ * (or anything else that creates a new primary context on the device) the
+ * block may load elsewhere, so make no further call of this entry point in
+ * that process.
  * Every call shares the one block and it keeps the last call's contents
  * (nothing in it needs clearing: each call writes every partial it reads).
  * Calls whose kernels overlap on the GPU (unordered streams, several host
@@ -283,6 +293,21 @@ kv_status kv_cache_export(kv_cache* cache, int layer, int what, void* host_dst, 
 /* Read and clear the device error flag that bounded waits set when they give
  * up. Synchronises `cuda_stream`. KV_ERR_TIMEOUT when it was set. */
 kv_status kv_cache_check_device_error(kv_cache* cache, void* cuda_stream);
+
+/* Test hook of the failure path: one launch whose bounded device waits run
+ * out on purpose (no fault, no hang). Two mbarriers that nothing arrives at
+ * and no copy completes on are waited for by the same wait routines the
+ * decode kernels use: one warp with `budget_cycles` SM clock cycles (in
+ * [1000, 2^31]), a second warp with the default budget of about one second,
+ * which must give up early through the abort flag the first warp raises,
+ * then one thread through the two single-thread forms. Each give-up sets the
+ * cache's device error flag, so a following kv_cache_check_device_error
+ * returns KV_ERR_TIMEOUT (and clears it); the cache's data is untouched.
+ * host_result receives 5 int64: per wait 1 if it returned "completed" (must
+ * all be 0), then the SM cycles the second warp waited. Synchronises
+ * `cuda_stream`. */
+kv_status kv_cache_test_bounded_wait(kv_cache* cache, int64_t budget_cycles, int64_t* host_result,
+                                     void* cuda_stream);
 
 /* Optional timing hook: when both are non-NULL, kv_decode_attn records
  * ev_begin (a cudaEvent_t) right before its split kernel and ev_end right

@@ -191,6 +191,10 @@ def test_v_q4_0_prefill_then_appends(kb, act, D, H, Hq):
     v[:, :, 10, :] = 0.0                          # d = 0: every code 8
     v[:, :, 11, :32] = 0.0
     v[:, :, 11, 3], v[:, :, 11, 7] = -2.0, 2.0    # the first extreme sets the sign; 2.0 clamps at 15
+    # small nonzero slices: |m| about 1e-4 makes d an fp16 subnormal, about
+    # 1e-7 rounds d to a few subnormal steps or to 0 while the values are not 0
+    v[:, :, 12, :] = W.round_to_act(v[:, :, 12, :] * np.float32(1e-4), act)
+    v[:, :, 13, :] = W.round_to_act(v[:, :, 13, :] * np.float32(1e-7), act)
     gc.prefill_quantize(0, torch_act(k, act), torch_act(v, act))
     oc.prefill_quantize(0, k, v)
     compare_exports(gc, oc, 0)
