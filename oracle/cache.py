@@ -438,8 +438,8 @@ class OracleCache:
         n_tail = B * (L - F)
         n_evicted = B * (E - cfg.n_sink)
         row16 = 2 * D * 2                     # K + V row of a 16-bit dtype
-        # stored bytes: 8 // bits codes per byte (3-bit codes two to a byte)
-        code = D // (8 // cfg.k_bits) + D // (8 // cfg.v_bits)
+        # stored bytes: D * bits / 8 per row (3-bit codes eight to three bytes)
+        code = D * cfg.k_bits // 8 + D * cfg.v_bits // 8
         if cfg.mode == "kivi":
             g_lo, g_hi = lo // GROUP, (F + GROUP - 1) // GROUP
             n_kgroups = max(0, g_hi - g_lo) if F > lo else 0

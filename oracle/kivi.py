@@ -13,7 +13,8 @@ Sources (page title, section):
     scales at the group boundary (the KIVI group idea), used here with
     32-token K groups and 32-channel V groups.
   * Foundry "TurboQuant KV Cache Compression - Spec", "Step 3: Packing":
-    [v0:2][v1:2][v2:2][v3:2] and [v0:4][v1:4] per byte.
+    [v0:2][v1:2][v2:2][v3:2] and [v0:4][v1:4] per byte; 3-bit codes eight to
+    three bytes (the page's no-waste form for the memory-bound case).
 
 Readings where the pages leave a step open:
   * Codes are stored unsigned: q_u = q - qMin, so the qMin offset drops out
@@ -23,7 +24,10 @@ Readings where the pages leave a step open:
     fp32, so quantise and dequantise use the same numbers.
   * The eps clamp is applied in fp32 before the fp16 rounding of the scale.
   * Packing puts v0 in the least-significant bits of each byte, and packs
-    along the channel axis of one token row.
+    along the channel axis of one token row. 3-bit codes are packed tight:
+    the row is one little-endian bit string with code i at bits 3i .. 3i+2
+    (eight codes in three bytes), the page's no-waste form rather than its
+    two-per-byte first cut, because the decode is memory-bound.
   * Every step is fp32 with each operation rounded on its own (numpy applies
     one ufunc at a time, so nothing is fused).
 """
@@ -142,17 +146,24 @@ def dequantize_v_rows(codes, s_h, z_h) -> np.ndarray:
 
 
 def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
-    """Pack codes along the last axis, v0 in the least-significant bits,
-    8 // bits codes per byte (Foundry spec, "Step 3: Packing": 2-bit
-    [v0:2][v1:2][v2:2][v3:2], 3-bit [v0:3][v1:3][__:2] with two bits unused,
-    4-bit [v0:4][v1:4]; 8-bit one code per byte).
+    """Pack codes along the last axis, v0 in the least-significant bits
+    (Foundry spec, "Step 3: Packing": 2-bit [v0:2][v1:2][v2:2][v3:2], 4-bit
+    [v0:4][v1:4], 8-bit one code per byte; 3-bit eight codes in three bytes,
+    code i at bits 3i .. 3i+2 of the row's little-endian bit string).
 
-    codes: uint8 [..., D] with values < 2^bits. Returns uint8 [..., D / (8 // bits)].
+    codes: uint8 [..., D] with values < 2^bits. Returns uint8 [..., D * bits / 8].
     """
-    per = 8 // bits
     D = codes.shape[-1]
-    if D % per:
+    if (D * bits) % 8 or (bits == 3 and D % 8):
         raise ValueError("row length must fill whole bytes")
+    if bits == 3:
+        c = codes.reshape(*codes.shape[:-1], D // 8, 8).astype(np.uint32)
+        word = np.zeros(c.shape[:-1], np.uint32)            # 24 bits per eight codes
+        for i in range(8):
+            word |= c[..., i] << np.uint32(3 * i)
+        out = np.stack([(word >> np.uint32(8 * k)) & np.uint32(0xFF) for k in range(3)], axis=-1)
+        return out.reshape(*codes.shape[:-1], D * 3 // 8).astype(np.uint8)
+    per = 8 // bits
     c = codes.reshape(*codes.shape[:-1], D // per, per).astype(np.uint16)
     out = np.zeros(c.shape[:-1], np.uint16)
     for i in range(per):
@@ -162,6 +173,11 @@ def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
 
 def unpack_codes(packed: np.ndarray, bits: int) -> np.ndarray:
     """Inverse of pack_codes."""
+    if bits == 3:
+        p = packed.reshape(*packed.shape[:-1], packed.shape[-1] // 3, 3).astype(np.uint32)
+        word = p[..., 0] | (p[..., 1] << np.uint32(8)) | (p[..., 2] << np.uint32(16))
+        c = np.stack([(word >> np.uint32(3 * i)) & np.uint32(7) for i in range(8)], axis=-1)
+        return c.reshape(*packed.shape[:-1], packed.shape[-1] * 8 // 3).astype(np.uint8)
     per = 8 // bits
     mask = (1 << bits) - 1
     p = packed.astype(np.uint16)[..., None]

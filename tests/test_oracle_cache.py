@@ -184,13 +184,13 @@ def test_byte_accounting_matches_pages():
         s = c.stats(0)
         assert s["code_bytes"] == keys + values
         assert s["kmeta_bytes"] + s["vmeta_bytes"] == meta // 2   # one float per vector, not two
-    # K3/V2 stored two codes per byte ("Step 3: Packing"): the keys take 4/3 of
-    # the tight count the memory table prints
+    # K3/V2 with 3-bit codes packed tight (eight in three bytes), the count
+    # the memory table prints
     H, D, kb, vb, keys, values, meta, total = fo["K3V2_16H_tight"]
     c = OracleCache(_cfg(batch=1, n_kv_heads=H, n_q_heads=H, head_dim=D,
                          mode="turboquant", k_bits=kb, v_bits=vb))
     c.append(0, _f16(rng, (1, H, 1, D)), _f16(rng, (1, H, 1, D)))
-    assert c.stats(0)["code_bytes"] == keys * 4 // 3 + values
+    assert c.stats(0)["code_bytes"] == keys + values
     # P3: FP16 2048 B/cell and q2k code bits 384 B/cell for 2 x 256 dims (= 4 x 128 here).
     pr = {r[0]: int(r[1]) for r in read_golden("pr2318_memory_math.txt")}
     c = OracleCache(_cfg(batch=1, n_kv_heads=4, n_q_heads=4, head_dim=128, k_bits=2, v_bits=4,

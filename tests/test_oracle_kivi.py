@@ -131,24 +131,34 @@ def test_k_groups_per_channel_v_per_token_axes():
 
 @pytest.mark.parametrize("bits", BITS)
 def test_pack_unpack_every_level(bits):
-    per = 8 // bits
     lb = (1 << bits) - 1
     codes = np.array([(i * 7 + 3) % (lb + 1) for i in range(4 * 256)], np.uint8).reshape(4, 256)
     codes[0, : lb + 1] = np.arange(lb + 1)
     packed = kivi.pack_codes(codes, bits)
-    assert packed.shape == (4, codes.shape[1] // per)
+    assert packed.shape == (4, codes.shape[1] * bits // 8)
     assert np.array_equal(kivi.unpack_codes(packed, bits), codes)
 
 
 def test_pack_layout_v0_in_low_bits():
-    """Foundry spec, "Step 3: Packing": [v0:2][v1:2][v2:2][v3:2],
-    [v0:3][v1:3][__:2] (two bits unused) and [v0:4][v1:4], read with v0 in
-    the least-significant bits."""
+    """Foundry spec, "Step 3: Packing": [v0:2][v1:2][v2:2][v3:2] and
+    [v0:4][v1:4], read with v0 in the least-significant bits; 3-bit codes
+    eight to three bytes. Worked by hand: codes 1..7, 0 are the bit string
+    001 010 011 100 101 110 111 000 from bit 0 up, i.e. the 24-bit value
+    0x1F58D1, stored D1 58 1F."""
     assert kivi.pack_codes(np.array([[1, 2, 3, 0]], np.uint8), 2)[0, 0] == 0b00111001
-    assert kivi.pack_codes(np.array([[5, 6]], np.uint8), 3)[0, 0] == 0b00110101
-    assert kivi.pack_codes(np.array([[7, 7, 0, 1]], np.uint8), 3).tolist() == [[0b00111111, 0b00001000]]
+    assert kivi.pack_codes(np.array([[1, 2, 3, 4, 5, 6, 7, 0]], np.uint8), 3).tolist() == [[0xD1, 0x58, 0x1F]]
+    assert kivi.pack_codes(np.array([[0, 0, 0, 0, 0, 0, 0, 7]], np.uint8), 3).tolist() == [[0x00, 0x00, 0xE0]]
+    assert kivi.pack_codes(np.array([[0, 0, 7, 0, 0, 7, 0, 0]], np.uint8), 3).tolist() == [[0xC0, 0x81, 0x03]]
     assert kivi.pack_codes(np.array([[0xA, 0x5]], np.uint8), 4)[0, 0] == 0x5A
     assert list(kivi.pack_codes(np.array([[7, 200]], np.uint8), 8)[0]) == [7, 200]
+
+
+def test_pack_3bit_is_three_quarters_of_4bit():
+    """The 3-bit form stores no unused bits: a row takes 3/4 of the 4-bit
+    row's bytes (the page's memory table counts K3 this way)."""
+    for D in (64, 128):
+        c = np.zeros((1, D), np.uint8)
+        assert kivi.pack_codes(c, 3).shape[-1] * 4 == kivi.pack_codes(c, 4).shape[-1] * 3
 
 
 # ------------------------------------------------------------------ q4_0 V form
