@@ -523,6 +523,12 @@ OTHER_WORKLOADS = {
                             mode="turboquant", k_bits=3, v_bits=2),
     "llama8b_q4_0v": dict(batch=16, n_kv_heads=8, n_q_heads=32, head_dim=128, context=32768, act_dtype="bf16",
                           mode="kivi", k_bits=2, v_bits=4, v_q4_0=True),
+    "llama8b_k4v4": dict(batch=16, n_kv_heads=8, n_q_heads=32, head_dim=128, context=32768, act_dtype="bf16",
+                         mode="kivi", k_bits=4, v_bits=4),
+    "llama8b_k3v4": dict(batch=16, n_kv_heads=8, n_q_heads=32, head_dim=128, context=32768, act_dtype="bf16",
+                         mode="kivi", k_bits=3, v_bits=4),
+    "llama8b_k3v3": dict(batch=16, n_kv_heads=8, n_q_heads=32, head_dim=128, context=32768, act_dtype="bf16",
+                         mode="kivi", k_bits=3, v_bits=3),
     "kvsink": dict(batch=4, n_kv_heads=8, n_q_heads=32, head_dim=128, context=131072, act_dtype="f16",
                    mode="kivi", k_bits=2, v_bits=2, n_dyn_sinks=5),
     "ring_int8": dict(batch=64, n_kv_heads=8, n_q_heads=8, head_dim=64, context=4100, act_dtype="f16",

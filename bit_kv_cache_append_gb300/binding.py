@@ -251,7 +251,7 @@ class KVCache:
         R = st["length"] - st["fp16_begin"]
         if what in ("k_codes", "v_codes"):
             bits = c.k_bits if what == "k_codes" else c.v_bits
-            return buf.reshape(B, H, n, D // (8 // bits))   # 8 // bits codes per byte
+            return buf.reshape(B, H, n, D * bits // 8)      # rows packed tight
         if what in ("k_scale", "k_zero"):
             return buf.view(np.float16).reshape(B, H, G, D)
         if what in ("v_scale", "v_zero"):

@@ -130,7 +130,7 @@ Geometry make_geometry(const kv_cache_config* c) {
   g.tail_cap = next_pow2(std::max(c->window, kGroup - 1) + 1);
   g.n_sink_slots = std::max(1, std::max(c->n_sink, c->n_dyn_sinks));
   g.max_splits = c->max_splits ? c->max_splits : 64;
-  g.chunk = kvq::chunk_layout(g.mode_tq, g.D, kvq::storage_bits(g.kb), kvq::storage_bits(g.vb));
+  g.chunk = kvq::chunk_layout(g.mode_tq, g.D, g.kb, g.vb);
   g.rope_max_pos = c->rope_base > 0.0 ? c->rope_max_pos : 0;
   g.rope_repos = c->rope_reposition ? 1 : 0;
   g.v_q4_0 = c->v_q4_0 ? 1 : 0;
@@ -529,7 +529,7 @@ kv_status kv_cache_stats(kv_cache* cache, int layer, kv_cache_stats_t* out) {
   out->n_tail = B * (L - F);
   out->n_evicted = B * (E - g.n_sink);
   const int64_t row16 = 2 * D * 2;
-  out->code_bytes = out->n_quant * H * (D * (kvq::storage_bits(g.kb) + kvq::storage_bits(g.vb)) / 8);
+  out->code_bytes = out->n_quant * H * (D * (g.kb + g.vb) / 8);
   if (!g.mode_tq) {
     const int64_t groups = F > lo ? (F + kGroup - 1) / kGroup - lo / kGroup : 0;
     out->kmeta_bytes = groups * B * H * 4 * D;
@@ -569,8 +569,8 @@ kv_status export_size(const kv_cache* c, int layer, int what, size_t* bytes) {
   const size_t B = g.B, H = g.H, D = g.D;
   const bool tq = g.mode_tq;
   switch (what) {
-    case KV_EXPORT_K_CODES: *bytes = B * H * p.n * D * kvq::storage_bits(g.kb) / 8; return KV_OK;
-    case KV_EXPORT_V_CODES: *bytes = B * H * p.n * D * kvq::storage_bits(g.vb) / 8; return KV_OK;
+    case KV_EXPORT_K_CODES: *bytes = B * H * p.n * D * g.kb / 8; return KV_OK;
+    case KV_EXPORT_V_CODES: *bytes = B * H * p.n * D * g.vb / 8; return KV_OK;
     case KV_EXPORT_K_SCALE:
     case KV_EXPORT_K_ZERO:
       if (tq) break;
@@ -722,31 +722,69 @@ kv_status kv_cache_export(kv_cache* cache, int layer, int what, void* host_dst, 
           const int64_t gi = grp - g0;
           const int ntok = static_cast<int>(std::min<int64_t>(kGroup, p.T1 - grp * kGroup));
           if (what == KV_EXPORT_K_CODES || what == KV_EXPORT_V_CODES) {
+            // canonical rows: D bits / 8 bytes, code c at bits c bits .. of
+            // the row's little-endian bit string
             const bool isk = what == KV_EXPORT_K_CODES;
-            // canonical rows: 8 / bits codes per byte, code c at bit
-            // (c mod per) * bits of byte c / per; storage puts 3-bit codes
-            // in the 4-bit layout
-            const int bits = isk ? g.kb : g.vb, sbits = kvq::storage_bits(bits), per = 8 / bits;
-            const int rowb = static_cast<int>(D) / per;
+            const int bits = isk ? g.kb : g.vb;
+            const int rowb = static_cast<int>(D) * bits / 8;
             uint8_t* o = dst + (bh * p.n + gi * kGroup) * rowb;
             const uint8_t* reg = chunk.data() + (isk ? g.chunk.kc_off : g.chunk.vc_off);
-            if (g.mode_tq && sbits == bits) {
-              std::memcpy(o, reg, static_cast<size_t>(ntok) * rowb);
-            } else if (g.mode_tq) {  // two 3-bit codes per stored byte, at bits 0 and 4
-              for (int i = 0; i < ntok * rowb; ++i)
-                o[i] = static_cast<uint8_t>((reg[i] & 0x7) | ((reg[i] >> 4) & 0x7) << 3);
-            } else {
-              const uint32_t mask = (1u << sbits) - 1;
+            auto put = [&](int tok, int ch, uint32_t code) {
+              if (tok >= ntok) return;
+              for (int k = 0; k < bits; ++k)
+                if ((code >> k) & 1u) o[tok * rowb + (ch * bits + k) / 8] |= static_cast<uint8_t>(1u << ((ch * bits + k) % 8));
+            };
+            const int wpl = static_cast<int>(D) * bits / 32, pw = kvq::piece_words(wpl);
+            auto lane_word = [&](int lane, int w) {
+              uint32_t x;
+              std::memcpy(&x, reg + kvq::code_word_offset(lane, w, pw), 4);
+              return x;
+            };
+            const uint32_t fmask = (1u << (2 * bits)) - 1u;
+            if (g.mode_tq && !isk) {  // token-pair rows
+              const int rb = kvq::tq_vrow_bytes(static_cast<int>(D), bits);
+              for (int pr = 0; pr < kGroup / 2; ++pr)
+                for (int c = 0; c < D; ++c) {
+                  const int fbit = kvq::tq_vfield_bit(static_cast<int>(D), bits, c);
+                  uint32_t f = 0;
+                  for (int k = 0; k < 2 * bits; ++k)
+                    f |= ((reg[pr * rb + (fbit + k) / 8] >> ((fbit + k) % 8)) & 1u) << k;
+                  put(2 * pr, c, f & ((1u << bits) - 1u));
+                  put(2 * pr + 1, c, f >> bits);
+                }
+            } else if (g.mode_tq) {  // K fields in fragment order
+              for (int lane = 0; lane < 32; ++lane) {
+                std::vector<uint32_t> w(wpl + 1, 0u);
+                for (int k = 0; k < wpl; ++k) w[k] = lane_word(lane, k);
+                const int gg = lane >> 2, t = lane & 3;
+                for (int b = 0; b < 4; ++b)
+                  for (int j = 0; j < D / 8; ++j) {
+                    const int fbit = kvq::tq_kfield_bit(static_cast<int>(D), bits, b, j);
+                    const uint64_t two = w[fbit / 32] | (static_cast<uint64_t>(w[fbit / 32 + 1]) << 32);
+                    const uint32_t f = static_cast<uint32_t>(two >> (fbit % 32)) & fmask;
+                    const int tok = 16 * (b >> 1) + gg + 8 * (b & 1), c0 = 16 * (j >> 1) + 2 * t + 8 * (j & 1);
+                    put(tok, c0, f & ((1u << bits) - 1u));
+                    put(tok, c0 + 1, f >> bits);
+                  }
+              }
+            } else {  // KIVI fragment order
+              const uint32_t mask = (1u << bits) - 1;
               for (int lane = 0; lane < 32; ++lane)
                 for (int f = 0; f < D; ++f) {
-                  int tok, ch, w, bit;
+                  int tok, ch;
                   if (isk) kvq::k_frag_pos(static_cast<int>(D), lane, f, &tok, &ch);
                   else kvq::v_frag_pos(static_cast<int>(D), lane, f, &tok, &ch);
-                  kvq::frag_bits(sbits, f, &w, &bit);
-                  uint32_t word;
-                  std::memcpy(&word, reg + kvq::code_word_offset(lane, w), 4);
-                  const uint32_t code = (word >> bit) & mask;
-                  o[tok * rowb + ch / per] |= static_cast<uint8_t>(code << ((ch % per) * bits));
+                  uint32_t code;
+                  if (bits == 3) {
+                    const uint32_t blk[3] = {lane_word(lane, 3 * (f / 32)), lane_word(lane, 3 * (f / 32) + 1),
+                                             lane_word(lane, 3 * (f / 32) + 2)};
+                    code = kvq::frag3_get(blk, f % 32);
+                  } else {
+                    int w, bit;
+                    kvq::frag_bits(bits, f, &w, &bit);
+                    code = (lane_word(lane, w) >> bit) & mask;
+                  }
+                  put(tok, ch, code);
                 }
             }
           } else if (what == KV_EXPORT_K_SCALE || what == KV_EXPORT_K_ZERO) {

@@ -96,13 +96,76 @@ __device__ __forceinline__ int word_bit(int i) {
   return 8 * j + 16 * e;
 }
 
-// KB, VB: code widths (levels 2^bits - 1); the codes are packed with their
-// storage widths (a 3-bit code in the 4-bit layout).
+// Byte offset, from the lane's base (K: cs[g][t D / 4], V: cs[2t][g]), of
+// the code of fragment element f of lane (g, t) (kvq_layout.h k_frag_pos,
+// v_frag_pos): a constant, so that packing loads each code with one
+// shared-memory byte load (rows are D + 4 bytes: the lanes' loads fall in
+// distinct banks or share a word).
+template <int D, bool IS_K>
+__device__ __forceinline__ constexpr int frag_code_offset(int f) {
+  const int e = f & 1, r = (f >> 1) & 3, hi = f >> 3;
+  if (IS_K) {
+    const int mt = hi / (D / 16), s = hi % (D / 16);
+    return (16 * mt + 8 * (r & 1)) * (D + 4) + 4 * s + 2 * (r >> 1) + e;
+  }
+  const int m = hi >> 1, kb = hi & 1;
+  return (16 * kb + e + 8 * (r >> 1)) * (D + 4) + 16 * m + 8 * (r & 1);
+}
+
+// Words [W0, W0 + NW) of every lane's K (IS_K) or V fragment block, packed
+// by this warp's thread `lane` for fragment lane `lane`; 3-bit codes in
+// blocks of three words (W0, NW multiples of 3).
+template <int D, int BITS, bool IS_K, int W0, int NW>
+__device__ __forceinline__ void pack_words(const uint8_t (*cs)[D + 4], uint8_t* region, int lane) {
+  constexpr int WPL = D * BITS / 32, PW = piece_words(WPL);
+  const int g = lane >> 2, t = lane & 3;
+  const uint8_t* base = IS_K ? &cs[g][t * (D / 4)] : &cs[2 * t][g];
+  if constexpr (BITS == 3) {
+#pragma unroll
+    for (int blk = W0 / 3; blk < (W0 + NW) / 3; ++blk) {
+      uint32_t w[3] = {0u, 0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 32; ++i) frag3_put(w, i, base[frag_code_offset<D, IS_K>(32 * blk + i)]);
+#pragma unroll
+      for (int q = 0; q < 3; ++q)
+        *reinterpret_cast<uint32_t*>(region + code_word_offset(lane, 3 * blk + q, PW)) = w[q];
+    }
+  } else {
+    constexpr int PER = 32 / BITS;
+#pragma unroll
+    for (int w = W0; w < W0 + NW; ++w) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+        word |= static_cast<uint32_t>(base[frag_code_offset<D, IS_K>(w * PER + i)]) << word_bit<BITS>(i);
+      *reinterpret_cast<uint32_t*>(region + code_word_offset(lane, w, PW)) = word;
+    }
+  }
+}
+
+// The codes of one group (cs[token][channel]) in the decode kernel's
+// fragment order: the D / 32 warps of the CTA take equal shares of the
+// words of every lane's block.
+template <int D, int BITS, bool IS_K>
+__device__ __forceinline__ void pack_fragments(const uint8_t (*cs)[D + 4], uint8_t* region, int tid) {
+  constexpr int NWARP = D / 32, NW = D * BITS / 32 / NWARP;
+  static_assert(NW * NWARP == D * BITS / 32 && (BITS != 3 || NW % 3 == 0), "equal shares");
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp == 0) pack_words<D, BITS, IS_K, 0, NW>(cs, region, lane);
+  else if (warp == 1) pack_words<D, BITS, IS_K, NW, NW>(cs, region, lane);
+  if constexpr (NWARP > 2) {
+    if (warp == 2) pack_words<D, BITS, IS_K, 2 * NW, NW>(cs, region, lane);
+    else if (warp == 3) pack_words<D, BITS, IS_K, 3 * NW, NW>(cs, region, lane);
+  }
+}
+
+// KB, VB: code widths (levels 2^bits - 1), packed tight (3-bit codes in
+// blocks of three words, kvq_layout.h frag3_put).
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
   constexpr int HALF = D / 2, NV = D / 32, CPR = HALF / 8;
   constexpr int LK = (1 << KB) - 1, LV = (1 << VB) - 1;
-  constexpr int SK = storage_bits(KB), SV = storage_bits(VB);
+  constexpr int SK = KB, SV = VB;
   // the group's rows as activation-dtype bits (rows padded by 16 bytes so
   // that 16-byte row stores stay aligned and column reads spread over banks)
   __shared__ __align__(16) uint16_t xk[32][D + 8];
@@ -241,30 +304,8 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
   __syncthreads();
 
   // pack in the decode kernel's fragment order (kvq_layout.h)
-  constexpr int KPER = 32 / SK, VPER = 32 / SV;
-  constexpr int KWPL = D * SK / 32, VWPL = D * SV / 32;  // words per lane block
-  for (int wi = tid; wi < 32 * KWPL; wi += D) {
-    const int lane = wi / KWPL, w = wi % KWPL;
-    uint32_t word = 0;
-#pragma unroll
-    for (int i = 0; i < KPER; ++i) {
-      int tok, ch;
-      k_frag_pos(D, lane, w * KPER + i, &tok, &ch);
-      word |= static_cast<uint32_t>(ck[tok][ch]) << word_bit<SK>(i);
-    }
-    *reinterpret_cast<uint32_t*>(chunk + G.chunk.kc_off + code_word_offset(lane, w)) = word;
-  }
-  for (int wi = tid; wi < 32 * VWPL; wi += D) {
-    const int lane = wi / VWPL, w = wi % VWPL;
-    uint32_t word = 0;
-#pragma unroll
-    for (int i = 0; i < VPER; ++i) {
-      int tok, ch;
-      v_frag_pos(D, lane, w * VPER + i, &tok, &ch);
-      word |= static_cast<uint32_t>(cv[tok][ch]) << word_bit<SV>(i);
-    }
-    *reinterpret_cast<uint32_t*>(chunk + G.chunk.vc_off + code_word_offset(lane, w)) = word;
-  }
+  pack_fragments<D, SK, true>(ck, chunk + G.chunk.kc_off, tid);
+  pack_fragments<D, SV, false>(cv, chunk + G.chunk.vc_off, tid);
   if (G.n_dyn && h == 0 && tid == 0) a.lay.sink_mask[b * G.n_slots + slot] = smask;
 }
 
@@ -343,10 +384,17 @@ __device__ __forceinline__ float tq_code_row(float (&x)[D / 32], const float* si
   return n;
 }
 
+// One warp per token pair (2 pi, 2 pi + 1) of a group, for the tokens of
+// the pair this call appends. Codes go to the decode's layouts
+// (kvq_layout.h): K in fragment order (each token's fields are whole bytes
+// of four lanes' strings, written as 16-bit halves), V in token-pair rows
+// (a field holds both tokens' codes, so the warp writes the whole row; where
+// only one token of the pair is in this call, the other's bits are kept).
+// The norms go to the group's norm arrays.
 template <int D>
-__global__ void __launch_bounds__(128) tq_quantize_kernel(AppendArgs a, int row_begin, int n_rows) {
+__global__ void __launch_bounds__(128) tq_quantize_kernel(AppendArgs a, int64_t pair_begin, int n_pairs) {
   constexpr int NS = D / 32;
-  __shared__ uint8_t codes[4][D];
+  __shared__ uint8_t codes[4][2][2][D];  // [warp][K, V][token of the pair][channel]
   __shared__ float s_signs[D];
   __shared__ float s_bk[16], s_bv[16];
   const Geometry& G = a.geo;
@@ -357,50 +405,85 @@ __global__ void __launch_bounds__(128) tq_quantize_kernel(AppendArgs a, int row_
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = row_begin + blockIdx.x * 4 + warp;
-  if (row >= row_begin + n_rows) return;
+  const int pi_idx = blockIdx.x * 4 + warp;
+  if (pi_idx >= n_pairs) return;
+  const int64_t pi = pair_begin + pi_idx;
   const int bh = blockIdx.y;
-  const int64_t pos = a.L0 + row;
-  const size_t in_row = (static_cast<size_t>(bh) * a.n + row) * D;
   const int bf16 = G.act_bf16;
   const float rsq = static_cast<float>(1.0 / sqrt(static_cast<double>(D)));
-  float xk[NS], xv[NS];
-#pragma unroll
-  for (int i = 0; i < NS; ++i) {
-    xk[i] = act_to_float(a.k[in_row + i * 32 + lane], bf16);
-    xv[i] = act_to_float(a.v[in_row + i * 32 + lane], bf16);
-  }
-  if (a.tab.rope) {
-    const float* tr = a.tab.rope + static_cast<size_t>(pos) * D;
-#pragma unroll
-    for (int i = 0; i < NS / 2; ++i) {
-      const int c = i * 32 + lane;
-      float rx, ry;
-      rope_pair(xk[i], xk[i + NS / 2], tr[2 * c], tr[2 * c + 1], &rx, &ry);
-      xk[i] = act_to_float(float_to_act(rx, bf16), bf16);
-      xk[i + NS / 2] = act_to_float(float_to_act(ry, bf16), bf16);
-    }
-  }
-  const int slot = static_cast<int>((pos / kGroup) % G.n_slots);
-  const int r = static_cast<int>(pos % kGroup);
+  const int64_t p0 = 2 * pi;
+  const int slot = static_cast<int>((p0 / kGroup) % G.n_slots);
   uint8_t* chunk = a.lay.chunks + (static_cast<size_t>(bh) * G.n_slots + slot) * G.chunk.bytes;
-  for (int which = 0; which < 2; ++which) {
-    const int bits = which ? G.vb : G.kb;
-    const float n = which ? tq_code_row<D>(xv, s_signs, s_bv, bits, rsq, codes[warp])
-                          : tq_code_row<D>(xk, s_signs, s_bk, bits, rsq, codes[warp]);
-    __syncwarp();
-    const int sbits = storage_bits(bits);  // 3-bit codes are stored as nibbles
-    const int row_words = D * sbits / 32, per = 32 / sbits;
-    uint32_t* dst = reinterpret_cast<uint32_t*>(chunk + (which ? G.chunk.vc_off : G.chunk.kc_off) +
-                                                r * (D * sbits / 8));
-    if (lane < row_words) {
-      uint32_t word = 0;
-      for (int i = 0; i < per; ++i) word |= static_cast<uint32_t>(codes[warp][lane * per + i]) << (sbits * i);
-      dst[lane] = word;
+  const int kb = G.kb, vb = G.vb;
+  bool have[2];
+  for (int e = 0; e < 2; ++e) {
+    const int64_t pos = p0 + e;
+    have[e] = pos >= a.L0 && pos < a.L0 + a.n;
+    if (!have[e]) continue;
+    const size_t in_row = (static_cast<size_t>(bh) * a.n + (pos - a.L0)) * D;
+    float xk[NS], xv[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      xk[i] = act_to_float(a.k[in_row + i * 32 + lane], bf16);
+      xv[i] = act_to_float(a.v[in_row + i * 32 + lane], bf16);
     }
-    if (lane == 0)
-      reinterpret_cast<float*>(chunk + (which ? G.chunk.vmeta_off : G.chunk.kmeta_off))[r] = n;
+    if (a.tab.rope) {
+      const float* tr = a.tab.rope + static_cast<size_t>(pos) * D;
+#pragma unroll
+      for (int i = 0; i < NS / 2; ++i) {
+        const int c = i * 32 + lane;
+        float rx, ry;
+        rope_pair(xk[i], xk[i + NS / 2], tr[2 * c], tr[2 * c + 1], &rx, &ry);
+        xk[i] = act_to_float(float_to_act(rx, bf16), bf16);
+        xk[i + NS / 2] = act_to_float(float_to_act(ry, bf16), bf16);
+      }
+    }
+    const int r = static_cast<int>(pos % kGroup);
+    const float nk = tq_code_row<D>(xk, s_signs, s_bk, kb, rsq, codes[warp][0][e]);
+    const float nv = tq_code_row<D>(xv, s_signs, s_bv, vb, rsq, codes[warp][1][e]);
+    if (lane == 0) {
+      reinterpret_cast<float*>(chunk + G.chunk.kmeta_off)[r] = nk;
+      reinterpret_cast<float*>(chunk + G.chunk.vmeta_off)[r] = nv;
+    }
     __syncwarp();
+    // K: block b = 2 (r / 16) + (r / 8) % 2 of lanes 4 (r % 8) + t; lane
+    // 2 BBK / 2 ... writes 16-bit half h of the block of lane t
+    const int bbk = D * kb / 32;  // bytes per token block
+    const int pw = piece_words(D * kb / 32);
+    const int blk = 2 * (r >> 4) + ((r >> 3) & 1);
+    if (lane < 2 * bbk) {
+      const int t = lane / (bbk / 2), hw = lane % (bbk / 2);
+      uint32_t half = 0;
+      for (int j = (16 * hw) / (2 * kb); j * 2 * kb < 16 * hw + 16; ++j) {  // the fields that meet this half
+        const int c0 = 16 * (j >> 1) + 2 * t + 8 * (j & 1);
+        const uint32_t f = codes[warp][0][e][c0] | (static_cast<uint32_t>(codes[warp][0][e][c0 + 1]) << kb);
+        const int sh = 2 * kb * j - 16 * hw;
+        half |= sh >= 0 ? (f << sh) : (f >> -sh);
+      }
+      half &= 0xffffu;
+      const int L = 4 * (r & 7) + t;
+      *reinterpret_cast<uint16_t*>(chunk + G.chunk.kc_off + lane_byte_offset(L, blk * bbk + 2 * hw, pw)) =
+          static_cast<uint16_t>(half);
+    }
+    __syncwarp();
+  }
+  // V: the pair row, 16-bit halves; a token not in this call keeps its bits
+  const int rb = tq_vrow_bytes(D, vb);
+  uint16_t* row = reinterpret_cast<uint16_t*>(chunk + G.chunk.vc_off + static_cast<size_t>((p0 % kGroup) / 2) * rb);
+  const uint32_t lo_mask = (1u << vb) - 1u;
+  const uint32_t keep = (have[0] ? lo_mask : 0u) | (have[1] ? lo_mask << vb : 0u);  // bits of a field written here
+  for (int hw = lane; hw < rb / 2; hw += 32) {
+    uint32_t half = 0, mask = 0;
+    for (int f = (16 * hw) / (2 * vb); f * 2 * vb < 16 * hw + 16; ++f) {  // the fields that meet this half
+      const int c = 8 * (f % (D / 8)) + f / (D / 8);  // the channel of field position f
+      const uint32_t v = (have[0] ? codes[warp][1][0][c] : 0u) | (have[1] ? static_cast<uint32_t>(codes[warp][1][1][c]) << vb : 0u);
+      const int sh = 2 * vb * f - 16 * hw;
+      half |= sh >= 0 ? (v << sh) : (v >> -sh);
+      mask |= sh >= 0 ? (keep << sh) : (keep >> -sh);
+    }
+    mask &= 0xffffu;
+    if (mask != 0xffffu) half = (row[hw] & ~mask) | (half & mask);
+    row[hw] = static_cast<uint16_t>(half);
   }
 }
 
@@ -441,10 +524,12 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int64_t* launches
     else launch_flush<64>(a, grid, s);
     ++*launches;
   }
-  if (G.mode_tq && a.n > 0) {
-    dim3 grid((a.n + 3) / 4, BH);
-    if (G.D == 128) tq_quantize_kernel<128><<<grid, 128, 0, s>>>(a, 0, a.n);
-    else tq_quantize_kernel<64><<<grid, 128, 0, s>>>(a, 0, a.n);
+  if (G.mode_tq && a.n > 0) {  // token pairs (2 pi, 2 pi + 1) that meet [L0, L0 + n)
+    const int64_t pair_begin = a.L0 / 2, pair_end = (a.L0 + a.n + 1) / 2;
+    const int n_pairs = static_cast<int>(pair_end - pair_begin);
+    dim3 grid((n_pairs + 3) / 4, BH);
+    if (G.D == 128) tq_quantize_kernel<128><<<grid, 128, 0, s>>>(a, pair_begin, n_pairs);
+    else tq_quantize_kernel<64><<<grid, 128, 0, s>>>(a, pair_begin, n_pairs);
     ++*launches;
   }
   // rows [r0, r1) of the append that go to the sink buffer or the tail: the

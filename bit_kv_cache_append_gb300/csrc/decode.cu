@@ -5,8 +5,23 @@
 
 namespace kvq {
 
-cudaError_t launch_kivi_d64(DecodeArgs& a, cudaStream_t s, int sm_count);
-cudaError_t launch_kivi_d128(DecodeArgs& a, cudaStream_t s, int sm_count);
+// The split kernels' launchers, instantiated in decode_d{64,128}_{k2,k3,k4,k8,tq}.cu.
+template <int D, int K>
+cudaError_t launch_kivi_k(DecodeArgs& a, cudaStream_t s, int sm_count);
+template <int D>
+cudaError_t launch_tq_d(DecodeArgs& a, cudaStream_t s, int sm_count);
+
+template <int D>
+cudaError_t launch_split(DecodeArgs& a, cudaStream_t s, int sm_count) {
+  if (a.geo.mode_tq) return launch_tq_d<D>(a, s, sm_count);
+  switch (a.geo.kb) {
+    case 2: return launch_kivi_k<D, 2>(a, s, sm_count);
+    case 3: return launch_kivi_k<D, 3>(a, s, sm_count);
+    case 4: return launch_kivi_k<D, 4>(a, s, sm_count);
+    case 8: return launch_kivi_k<D, 8>(a, s, sm_count);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 namespace {
 
@@ -172,7 +187,7 @@ cudaError_t launch_decode(DecodeArgs& a, cudaStream_t s, cudaEvent_t ev0, cudaEv
   const Geometry& G = a.geo;
   cudaError_t e;
   if (ev0) cudaEventRecord(ev0, s);
-  e = (G.D == 128) ? launch_kivi_d128(a, s, sm_count) : launch_kivi_d64(a, s, sm_count);
+  e = (G.D == 128) ? launch_split<128>(a, s, sm_count) : launch_split<64>(a, s, sm_count);
   if (e != cudaSuccess) return e;
   const bool split_ran = a.work > 0;
   if (split_ran) ++*launches;

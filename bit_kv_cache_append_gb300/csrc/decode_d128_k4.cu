@@ -1,0 +1,6 @@
+// KIVI decode kernels for head_dim 128, 4-bit K codes.
+#include "decode_kivi.cuh"
+
+namespace kvq {
+template cudaError_t launch_kivi_k<128, 4>(DecodeArgs& a, cudaStream_t s, int sm_count);
+}  // namespace kvq

@@ -86,7 +86,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // over codes (a power of two, so the rescale is exact).
 template <int BITS>
 struct CodeConsts {
-  static constexpr float kCodeInv = BITS == 2 ? 2.0f : (BITS == 4 ? 512.0f : 1.0f);
+  static constexpr float kCodeInv = BITS == 2 ? 2.0f : (BITS == 3 ? 8.0f : (BITS == 4 ? 512.0f : 1.0f));
   uint32_t magic;
   __device__ __forceinline__ void load(const DecodeArgs& a) {
     if (BITS == 8) magic = pin(a.h2_magic);
@@ -111,6 +111,26 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t m) {
   return d;
 }
 
+template <int HALF>
+__device__ __forceinline__ uint32_t cvt_e2m3x2(uint32_t m) {
+  uint32_t d;
+  if (HALF == 0) asm("{.reg .b16 l, h; mov.b32 {l, h}, %1; cvt.rn.f16x2.e2m3x2 %0, l;}" : "=r"(d) : "r"(m));
+  if (HALF == 1) asm("{.reg .b16 l, h; mov.b32 {l, h}, %1; cvt.rn.f16x2.e2m3x2 %0, h;}" : "=r"(d) : "r"(m));
+  return d;
+}
+
+// Pair j (0 .. 15) of a 3-bit block of three words w (kvq_layout.h
+// frag3_put) as an exact f16x2 of code / 8: quad j / 2 holds four codes, one
+// in the low three bits of each byte, which as e2m3 (exponent field 0) are
+// the evenly spaced values code / 8.
+__device__ __forceinline__ uint32_t code_pair3(const uint32_t* w, int j) {
+  const int q = j >> 1;
+  uint32_t m;
+  if (q < 6) m = (w[q >> 1] >> (3 * (q & 1))) & 0x07070707u;
+  else m = ((w[q - 6] >> 6) & 0x03030303u) | ((w[2] >> (4 + (q - 6))) & 0x04040404u);
+  return (j & 1) ? cvt_e2m3x2<1>(m) : cvt_e2m3x2<0>(m);
+}
+
 // Pair j of a packed word (the lane's fragment elements 2P, 2P + 1 where
 // P = word * pairs-per-word + j) as an exact f16x2 of code * unit. j is a
 // constant after unrolling, so the selections below fold away.
@@ -133,6 +153,18 @@ __device__ __forceinline__ uint32_t code_pair(const CodeConsts<BITS>& k, uint32_
   }
 }
 
+// Pair P (fragment elements 2P, 2P + 1) of a lane's code words w (from the
+// start of the lane's block) as an exact f16x2 of code * unit.
+template <int BITS>
+__device__ __forceinline__ uint32_t pair_at(const CodeConsts<BITS>& k, const uint32_t* w, int P) {
+  if constexpr (BITS == 3) {
+    return code_pair3(w + 3 * (P >> 4), P & 15);
+  } else {
+    constexpr int PPW = 16 / BITS;
+    return code_pair<BITS>(k, w[P / PPW], P % PPW);
+  }
+}
+
 #ifndef KVQ_LAZY_RESCALE
 #define KVQ_LAZY_RESCALE 8.0f
 #endif
@@ -150,8 +182,8 @@ constexpr float kLazyRescale = KVQ_LAZY_RESCALE;
 
 template <int D, int KB, int VB, bool TQ = false>
 struct KiviTile {
-  // chunk layout (kvq_layout.h): KIVI codes and meta, or TurboQuant
-  // row-major codes with one f32 norm per token
+  // chunk layout (kvq_layout.h): KIVI codes and meta, or TurboQuant K codes
+  // in fragment order and V codes in token-pair rows, one f32 norm per token
   static constexpr int KC = 32 * D * KB / 8;
   static constexpr int KMETA = KC;
   static constexpr int VC = KMETA + (TQ ? 4 * 32 : 4 * D);
@@ -160,63 +192,104 @@ struct KiviTile {
   static constexpr int NP = KVQ_DECODE_PAIRS;           // warp pairs per CTA
   // groups per stage: a pair takes runs of GPB consecutive groups, so the
   // waits, hand-off and rescale decision are paid once per run (KIVI chunks
-  // up to 6 KB); one for TurboQuant, whose tables and tiles leave less
-  // shared memory, and for larger chunks
+  // up to 6 KB); one for TurboQuant, whose tables leave less shared memory,
+  // and for larger chunks
   static constexpr int GPB = (TQ || CHUNK > 6144) ? 1 : 2;
   static constexpr int STAGE = GPB * CHUNK;
   static constexpr int PBUF = GPB * 32 * 8 + 16;         // weights (4 f16, 8 B per lane per group) + 4 rescale factors
-  // TurboQuant codebook tables: code pair -> f16x2 of the two values
-  // 2 c[code] - 1, NLUT interleaved copies (lane & 7 picks one) against
-  // bank conflicts
-  static constexpr int NLUT = 8;
-  static constexpr int LUTK = TQ ? (1 << (2 * KB)) * NLUT * 4 : 0;
-  static constexpr int LUTV = TQ ? (1 << (2 * VB)) * NLUT * 4 : 0;
-  static constexpr int VT_ROW = D + 8;
   static constexpr int RED_FLOATS = NP * kMaxGqa * (D + 2);  // one merged state per pair
-  // shared memory of the CTA with nst stages per pair (the layout below)
-  static constexpr int smem_for(int nst) {
-    return NP * nst * STAGE + NP * 2 * PBUF + (D / 16) * 32 * 16 + (TQ ? kMaxGqa * D * 4 : 0) + LUTK + LUTV +
-           (TQ ? NP * 32 * VT_ROW * 2 : 0) + RED_FLOATS * 4 + NP * (nst + 4) * 8 + 16;
+  // TurboQuant codebook tables: a field (two codes, low | high << bits) ->
+  // f16x2 of their values 2 c[code] - 1, in NLUT interleaved copies (entry e
+  // of copy cp at e NLUT + cp, lane % NLUT picks the copy): with 32 copies
+  // every lane reads its own bank
+  static constexpr int lut_bytes(int bits, int nlut) { return TQ ? (1 << (2 * bits)) * nlut * 4 : 0; }
+  static constexpr int smem_for(int nst, int nlut) {
+    return NP * nst * STAGE + NP * 2 * PBUF + (D / 16) * 32 * 16 + (TQ ? kMaxGqa * D * 4 : 0) +
+           lut_bytes(KB, nlut) + lut_bytes(VB, nlut) + RED_FLOATS * 4 + NP * (nst + 4) * 8 + 16;
   }
   // what one of two CTAs may take of an SM's 228 KB (1 KB of each CTA's
   // share is reserved by the hardware)
   static constexpr int kTwoCtaSmem = 228 * 1024 / 2 - 1024;
-#ifndef KVQ_DECODE_STAGES
   // bulk-copy stages per pair: three where they leave room for two CTAs per
-  // SM (runs of two groups up to 4 KB each; single groups), else two
-  static constexpr int NST = smem_for(3) <= kTwoCtaSmem ? 3 : 2;
+  // SM (runs of two groups up to 4 KB each; single groups), else two; the
+  // tables keep 32 copies unless even two stages leave no room for them
+  static constexpr int NLUT = (!TQ || smem_for(2, 32) <= kTwoCtaSmem) ? 32 : 16;
+#ifndef KVQ_DECODE_STAGES
+  static constexpr int NST = smem_for(3, NLUT) <= kTwoCtaSmem ? 3 : 2;
 #else
   static constexpr int NST = KVQ_DECODE_STAGES;
 #endif
+  static constexpr int LUTK = lut_bytes(KB, NLUT);
+  static constexpr int LUTV = lut_bytes(VB, NLUT);
   // shared memory: stages | weight buffers | query operand | query scratch |
   // tables | red | barriers | abort flag
   static constexpr int OFF_PBUF = NP * NST * STAGE;
   static constexpr int OFF_Q = OFF_PBUF + NP * 2 * PBUF;  // [D/16 k-steps][32 lanes] x 16 B
   static constexpr int OFF_QF = OFF_Q + (D / 16) * 32 * 16;  // TurboQuant: rotated queries [kMaxGqa][D] f32
   static constexpr int OFF_LUT = OFF_QF + (TQ ? kMaxGqa * D * 4 : 0);
-  // TurboQuant: each PV warp's dequantised V tile, 32 token rows of D f16
-  // padded by 8 halves (conflict-free row stores and transposed ldmatrix)
-  static constexpr int OFF_VT = OFF_LUT + LUTK + LUTV;
-  static constexpr int OFF_RED = OFF_VT + (TQ ? NP * 32 * VT_ROW * 2 : 0);
+  static constexpr int OFF_RED = OFF_LUT + LUTK + LUTV;
   static constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
   static constexpr int NBAR = NP * (NST + 4);             // full[NST], pfull[2], pempty[2]
   static constexpr int OFF_ABORT = OFF_BAR + NBAR * 8;
   static constexpr size_t smem_bytes() { return OFF_ABORT + 16; }
-  static_assert(smem_bytes() == static_cast<size_t>(smem_for(NST)), "layout and its size agree");
+  static_assert(smem_bytes() == static_cast<size_t>(smem_for(NST, NLUT)), "layout and its size agree");
   static_assert(OFF_BAR % 8 == 0, "mbarriers are 8-byte aligned");
+  static_assert(!TQ || smem_bytes() <= static_cast<size_t>(kTwoCtaSmem), "two CTAs per SM");
 };
-
-// TurboQuant: the codebook table entry of a code pair (index = low code |
-// high code << BITS), in copy `cp`.
-template <int BITS>
-__device__ __forceinline__ uint32_t tq_lut(const uint32_t* lut, uint32_t idx, int cp) {
-  return lut[idx * 8 + cp];
-}
 
 // CTA that owns flattened item i under the equal split of `work` items into
 // `n` ranges [floor(c work / n), floor((c+1) work / n)).
 __device__ __forceinline__ int owner_cta(int64_t i, int64_t work, int n) {
   return static_cast<int>(((i + 1) * n - 1) / work);
+}
+
+// The W words of this lane's block of a code region whose lane blocks are
+// interleaved in pieces of PW words (kvq_layout.h code_word_offset).
+template <int W, int PW>
+__device__ __forceinline__ void load_lane_words(const uint8_t* region, int lane, uint32_t* w) {
+#pragma unroll
+  for (int pc = 0; pc < W / PW; ++pc) {
+    if constexpr (PW == 4) {
+      const uint4 v = reinterpret_cast<const uint4*>(region)[pc * 32 + lane];
+      w[4 * pc] = v.x, w[4 * pc + 1] = v.y, w[4 * pc + 2] = v.z, w[4 * pc + 3] = v.w;
+    } else {
+      const uint2 v = reinterpret_cast<const uint2*>(region)[pc * 32 + lane];
+      w[2 * pc] = v.x, w[2 * pc + 1] = v.y;
+    }
+  }
+}
+
+// Words [first, first + N) of this lane's block (first a constant after
+// unrolling), lane blocks interleaved in pieces of PW words.
+template <int N, int PW>
+__device__ __forceinline__ void load_lane_range(const uint8_t* region, int lane, int first, uint32_t* out) {
+  const int p0 = first / PW, p1 = (first + N - 1) / PW;
+#pragma unroll
+  for (int pc = p0; pc <= p1; ++pc) {
+    uint32_t tmp[PW];
+    if constexpr (PW == 4) {
+      const uint4 v = reinterpret_cast<const uint4*>(region)[pc * 32 + lane];
+      tmp[0] = v.x, tmp[1] = v.y, tmp[2] = v.z, tmp[3] = v.w;
+    } else {
+      const uint2 v = reinterpret_cast<const uint2*>(region)[pc * 32 + lane];
+      tmp[0] = v.x, tmp[1] = v.y;
+    }
+#pragma unroll
+    for (int k = 0; k < PW; ++k) {
+      const int w = pc * PW + k;
+      if (w >= first && w < first + N) out[w - first] = tmp[k];
+    }
+  }
+}
+
+// The field of 2 BITS bits at bit `bit` of a lane's bit string (w[] has one
+// word of padding after the string).
+template <int BITS>
+__device__ __forceinline__ uint32_t lane_field(const uint32_t* w, int bit) {
+  constexpr uint32_t M = (1u << (2 * BITS)) - 1u;
+  const int wi = bit >> 5, sh = bit & 31;
+  if (sh + 2 * BITS <= 32) return (w[wi] >> sh) & M;
+  return __funnelshift_r(w[wi], w[wi + 1], sh) & M;
 }
 
 // Walks the runs of pair p inside its CTA's range [i0, i1): per unit (run of
@@ -285,7 +358,6 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
   constexpr int NP = T::NP, NST = T::NST, CHUNK = T::CHUNK;
   constexpr int S = D / 16, MV = D / 16, NVG = D / 32;
   constexpr int KW = D * KB / 32;
-  constexpr int KPPW = 16 / KB, VPPW = 16 / VB;  // code pairs per 32-bit word
   extern __shared__ __align__(128) uint8_t smem[];
   float* red = reinterpret_cast<float*>(smem + T::OFF_RED);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_ABORT);
@@ -319,10 +391,9 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
   uint32_t* lut_k = reinterpret_cast<uint32_t*>(smem + T::OFF_LUT);
   uint32_t* lut_v = reinterpret_cast<uint32_t*>(smem + T::OFF_LUT + T::LUTK);
   if constexpr (TQ) {  // value of code c: 2 c[c] - 1 (Foundry TurboQuant spec, "Algorithm Detail")
-    // KB, VB are the stored field widths; the codebooks have 2^bits levels
-    // (a 3-bit code sits in a 4-bit field, whose upper values never occur)
-    const int nk = 1 << KB, nv = 1 << VB, lk = 1 << G.kb, lv = 1 << G.vb;
-    auto level = [](const float* cb, int l, int c) { return c < l ? 2.0f * cb[l - 1 + c] - 1.0f : 0.0f; };
+    // a field is (low code | high code << bits); the codebooks have 2^bits levels
+    const int nk = 1 << KB, nv = 1 << VB, lk = nk, lv = nv;
+    auto level = [](const float* cb, int l, int c) { return 2.0f * cb[l - 1 + c] - 1.0f; };
     for (int i = threadIdx.x; i < (1 << (2 * KB)) * T::NLUT; i += blockDim.x) {
       const int e = i / T::NLUT;
       lut_k[i] = f2_to_h2(level(a.tab.cb_k, lk, e & (nk - 1)), level(a.tab.cb_k, lk, e >> KB));
@@ -461,41 +532,27 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
       // scores of one group into the lane's C fragment
       auto qk_scores = [&](const uint8_t* tile, float (&sc)[2][4]) {
         if constexpr (TQ) {
-          // scores in the rotated domain: codes row-major, token rows of RW
-          // words; the pair of channels (16 s + 2t, +1) of a row is byte t
-          // of word 2s (4-bit) or nibble t of word s (2-bit), the pair
-          // (+8, +9) the next byte / nibble t + 4; the table turns a pair
-          // into its f16x2 values; the K norm of each token scales its row
-          constexpr int RW = D * KB / 32;
-          const uint32_t* krows = reinterpret_cast<const uint32_t*>(tile);
-          const uint32_t* lk = lut_k + (lane & 7);
+          // scores in the rotated domain: the lane's K fields (fragment order,
+          // kvq_layout.h tq_kfield_bit) from its own words of the tile, each
+          // field turned into the f16x2 of its two codebook values by the
+          // lane's copy of the table; the K norm of each token scales its row
+          constexpr int KWT = D * KB / 32, PWT = piece_words(KWT);
+          uint32_t kw[KWT + 1];
+          load_lane_words<KWT, PWT>(tile, lane, kw);
+          kw[KWT] = 0u;
+          const uint32_t* lk = lut_k + (lane % T::NLUT);
           float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            uint32_t w0[RW], w1[RW];  // token rows 16 mt + g and 16 mt + g + 8
-#pragma unroll
-            for (int i = 0; i < RW / 4; ++i) {
-              *reinterpret_cast<uint4*>(&w0[4 * i]) = reinterpret_cast<const uint4*>(krows + (16 * mt + g) * RW)[i];
-              *reinterpret_cast<uint4*>(&w1[4 * i]) = reinterpret_cast<const uint4*>(krows + (16 * mt + g + 8) * RW)[i];
-            }
+          for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int s = 0; s < S; ++s) {
               const uint4 q4 = qsm[s * 32 + lane];
-              uint32_t i00, i10, i01, i11;  // pair index of (row 0 / 1, channel pair +0 / +8)
-              if (KB == 4) {
-                i00 = (w0[2 * s] >> (8 * t)) & 0xFFu;
-                i10 = (w1[2 * s] >> (8 * t)) & 0xFFu;
-                i01 = (w0[2 * s + 1] >> (8 * t)) & 0xFFu;
-                i11 = (w1[2 * s + 1] >> (8 * t)) & 0xFFu;
-              } else {
-                i00 = (w0[s] >> (4 * t)) & 0xFu;
-                i10 = (w1[s] >> (4 * t)) & 0xFu;
-                i01 = (w0[s] >> (4 * t + 16)) & 0xFu;
-                i11 = (w1[s] >> (4 * t + 16)) & 0xFu;
-              }
-              mma_f16(acc[mt], lk[i00 * 8], lk[i10 * 8], lk[i01 * 8], lk[i11 * 8], q4.y, q4.w);
+              const uint32_t a0 = lk[lane_field<KB>(kw, tq_kfield_bit(D, KB, 2 * mt, 2 * s)) * T::NLUT];
+              const uint32_t a1 = lk[lane_field<KB>(kw, tq_kfield_bit(D, KB, 2 * mt + 1, 2 * s)) * T::NLUT];
+              const uint32_t a2 = lk[lane_field<KB>(kw, tq_kfield_bit(D, KB, 2 * mt, 2 * s + 1)) * T::NLUT];
+              const uint32_t a3 = lk[lane_field<KB>(kw, tq_kfield_bit(D, KB, 2 * mt + 1, 2 * s + 1)) * T::NLUT];
+              mma_f16(acc[mt], a0, a1, a2, a3, q4.y, q4.w);
             }
-          }
           const float* kn = reinterpret_cast<const float*>(tile + T::KMETA);
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt) {
@@ -507,9 +564,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           }
         } else {
           uint32_t kr[KW];
-#pragma unroll
-          for (int i = 0; i < KW / 4; ++i)
-            *reinterpret_cast<uint4*>(&kr[4 * i]) = reinterpret_cast<const uint4*>(tile)[i * 32 + lane];
+          load_lane_words<KW, piece_words(KW)>(tile, lane, kr);
           const uint4* ks = reinterpret_cast<const uint4*>(tile + T::KMETA);
           // the zero-point operand: every row is the k-step's zero row
           const uint8_t* zrow = tile + T::KMETA + 2 * D + ((lane >> 4) & 1) * 16;
@@ -533,10 +588,10 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
 #pragma unroll
               for (int mt = 0; mt < 2; ++mt) {
                 const int pbase = (mt * S + s) * 4;
-                const uint32_t a0 = code_pair<KB>(kc, kr[(pbase + 0) / KPPW], (pbase + 0) % KPPW);
-                const uint32_t a1 = code_pair<KB>(kc, kr[(pbase + 1) / KPPW], (pbase + 1) % KPPW);
-                const uint32_t a2 = code_pair<KB>(kc, kr[(pbase + 2) / KPPW], (pbase + 2) % KPPW);
-                const uint32_t a3 = code_pair<KB>(kc, kr[(pbase + 3) / KPPW], (pbase + 3) % KPPW);
+                const uint32_t a0 = pair_at<KB>(kc, kr, pbase + 0);
+                const uint32_t a1 = pair_at<KB>(kc, kr, pbase + 1);
+                const uint32_t a2 = pair_at<KB>(kc, kr, pbase + 2);
+                const uint32_t a3 = pair_at<KB>(kc, kr, pbase + 3);
                 mma_f16(sa[mt][s & 1], a0, a1, a2, a3, bq[0], bq[1]);
               }
             }
@@ -556,10 +611,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
         const uint8_t* tl[2] = {t0, t1};
         uint32_t kr[2][KW];
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-          for (int i = 0; i < KW / 4; ++i)
-            *reinterpret_cast<uint4*>(&kr[q][4 * i]) = reinterpret_cast<const uint4*>(tl[q])[i * 32 + lane];
+        for (int q = 0; q < 2; ++q) load_lane_words<KW, piece_words(KW)>(tl[q], lane, kr[q]);
         float zb[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
         float sa[2][2][4] = {};
 #pragma unroll
@@ -589,10 +641,10 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
 #pragma unroll
               for (int mt = 0; mt < 2; ++mt) {
                 const int pbase = (mt * S + s) * 4;
-                const uint32_t a0 = code_pair<KB>(kc, kr[q][(pbase + 0) / KPPW], (pbase + 0) % KPPW);
-                const uint32_t a1 = code_pair<KB>(kc, kr[q][(pbase + 1) / KPPW], (pbase + 1) % KPPW);
-                const uint32_t a2 = code_pair<KB>(kc, kr[q][(pbase + 2) / KPPW], (pbase + 2) % KPPW);
-                const uint32_t a3 = code_pair<KB>(kc, kr[q][(pbase + 3) / KPPW], (pbase + 3) % KPPW);
+                const uint32_t a0 = pair_at<KB>(kc, kr[q], pbase + 0);
+                const uint32_t a1 = pair_at<KB>(kc, kr[q], pbase + 1);
+                const uint32_t a2 = pair_at<KB>(kc, kr[q], pbase + 2);
+                const uint32_t a3 = pair_at<KB>(kc, kr[q], pbase + 3);
                 mma_f16(sa[q][mt], a0, a1, a2, a3, bq[0], bq[1]);
               }
             }
@@ -721,50 +773,47 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
       // values of one group with its weights ph into oacc, zacc
       auto pv_values = [&](const uint8_t* tile, const uint32_t (&ph)[4]) {
         if constexpr (TQ) {
-          // out^T += V^T (p n_v) with one B operand for every m-tile. The V
-          // rows are dequantised into this warp's f16 tile first (lane r
-          // takes token row r; a pair of adjacent channels is one table
-          // entry), then read back transposed by ldmatrix.
-          constexpr int RWV = D * VB / 32;
-          constexpr int PPW = 16 / VB;  // channel pairs per code word
-          constexpr uint32_t PM = (1u << (2 * VB)) - 1u;
-          uint16_t* vt = reinterpret_cast<uint16_t*>(smem + T::OFF_VT) + pair * 32 * T::VT_ROW;
-          {
-            const uint32_t* row = reinterpret_cast<const uint32_t*>(tile + T::VC) + lane * RWV;
-            const uint32_t* lv = lut_v + (lane & 7);
-            uint16_t* dst = vt + lane * T::VT_ROW;
-#pragma unroll
-            for (int w4 = 0; w4 < RWV / 4; ++w4) {
-              const uint4 cw = reinterpret_cast<const uint4*>(row)[w4];
-              const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-              for (int k2 = 0; k2 < 4; ++k2) {
-                uint32_t hv[PPW];
-#pragma unroll
-                for (int j = 0; j < PPW; ++j) hv[j] = lv[((wv[k2] >> (2 * VB * j)) & PM) * 8];
-                uint4* d4 = reinterpret_cast<uint4*>(dst + ((w4 * 4 + k2) * PPW) * 2);
-#pragma unroll
-                for (int j = 0; j < PPW / 4; ++j) d4[j] = make_uint4(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3]);
-              }
-            }
-          }
-          __syncwarp();
-          uint32_t bb[2][2];
+          // out^T += V^T (p n_v) with one B operand for every m-tile; the A
+          // fragments come straight from the token-pair rows (kvq_layout.h):
+          // lane (g, t) needs tokens 16 kb + 2t (+1) and 16 kb + 2t + 8 (+9),
+          // i.e. pair rows 8 kb + t and 8 kb + t + 4, and in each the fields
+          // of channels g + 8 j: block g of the row, whose fields are exactly
+          // its A pairs (channel, two tokens); the lane's copy of the table
+          // turns them into f16x2
+          constexpr int RB = tq_vrow_bytes(D, VB), BB = D * VB / 32, BW = (BB + 3) / 4;
+          const uint32_t* lv = lut_v + (lane % T::NLUT);
+          const uint8_t* vrows = tile + T::VC;
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
-            bb[kb][0] = movmatrix_t(ph[2 * kb]);
-            bb[kb][1] = movmatrix_t(ph[2 * kb + 1]);
-          }
+            const uint32_t b0 = movmatrix_t(ph[2 * kb]);
+            const uint32_t b1 = movmatrix_t(ph[2 * kb + 1]);
+            uint32_t A[MV][4];
 #pragma unroll
-          for (int m = 0; m < MV; ++m)
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint8_t* blk = vrows + (8 * kb + t + 4 * hh) * RB + g * BB;
+              uint32_t bw[BW + 1];
+              if constexpr (BB % 16 == 0) {
+                const uint4 v = *reinterpret_cast<const uint4*>(blk);
+                bw[0] = v.x, bw[1] = v.y, bw[2] = v.z, bw[3] = v.w;
+              } else if constexpr (BB % 8 == 0) {
+                const uint2 v = *reinterpret_cast<const uint2*>(blk);
+                bw[0] = v.x, bw[1] = v.y;
+              } else if constexpr (BB % 4 == 0) {
 #pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-              uint32_t A[4];
-              ldmatrix_x4_trans(A, vt + (16 * kb + 8 * (lane >> 4) + (lane & 7)) * T::VT_ROW + 16 * m +
-                                       8 * ((lane >> 3) & 1));
-              mma_f16(oacc[m], A[0], A[1], A[2], A[3], bb[kb][0], bb[kb][1]);
+                for (int k = 0; k < BW; ++k) bw[k] = reinterpret_cast<const uint32_t*>(blk)[k];
+              } else {  // 6-byte blocks (3-bit codes, head_dim 64)
+                const uint16_t* h16 = reinterpret_cast<const uint16_t*>(blk);
+                bw[0] = h16[0] | (static_cast<uint32_t>(h16[1]) << 16);
+                bw[1] = h16[2];
+              }
+              bw[BW] = 0u;
+#pragma unroll
+              for (int jj = 0; jj < 2 * MV; ++jj)
+                A[jj >> 1][2 * hh + (jj & 1)] = lv[lane_field<VB>(bw, 2 * VB * jj) * T::NLUT];
             }
-          __syncwarp();  // the tile is read before the next group overwrites it
+#pragma unroll
+            for (int m = 0; m < MV; ++m) mma_f16(oacc[m], A[m][0], A[m][1], A[m][2], A[m][3], b0, b1);
+          }
         } else {
         // the weights as the B operand (column g, token pairs 2t + 8 kk,
         // + 1; the odd columns are zero), shared by the zero-point MMA and
@@ -792,16 +841,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           // the VB code words of channel group v (m-tiles 2v, 2v + 1), loaded
           // when first needed to keep them live briefly
           uint32_t vr[VB];
-#pragma unroll
-          for (int i = 0; i < (VB + 3) / 4; ++i) {
-            const uint4 w4 = vcode[((v * VB) / 4 + i) * 32 + lane];
-            const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) {
-              const int wi = i * 4 + k2 - (v * VB) % 4;
-              if (wi >= 0 && wi < VB) vr[wi] = ww[k2];
-            }
-          }
+          load_lane_range<VB, piece_words(D * VB / 32)>(reinterpret_cast<const uint8_t*>(vcode), lane, v * VB, vr);
           const uint4 s4 = vsc[v * 4 + t];
           const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
@@ -813,10 +853,10 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
             for (int hh = 0; hh < 2; ++hh) {
               const int m = 2 * v + hh;
               const int pbase = (m * 2 + kb) * 4;
-              const uint32_t a0 = code_pair<VB>(vc, vr[(pbase + 0) / VPPW - v * VB], (pbase + 0) % VPPW);
-              const uint32_t a1 = code_pair<VB>(vc, vr[(pbase + 1) / VPPW - v * VB], (pbase + 1) % VPPW);
-              const uint32_t a2 = code_pair<VB>(vc, vr[(pbase + 2) / VPPW - v * VB], (pbase + 2) % VPPW);
-              const uint32_t a3 = code_pair<VB>(vc, vr[(pbase + 3) / VPPW - v * VB], (pbase + 3) % VPPW);
+              const uint32_t a0 = pair_at<VB>(vc, vr, pbase + 0 - 16 * v);
+              const uint32_t a1 = pair_at<VB>(vc, vr, pbase + 1 - 16 * v);
+              const uint32_t a2 = pair_at<VB>(vc, vr, pbase + 2 - 16 * v);
+              const uint32_t a3 = pair_at<VB>(vc, vr, pbase + 3 - 16 * v);
               mma_f16(oacc[m], a0, a1, a2, a3, b0, b1);
             }
           }
@@ -920,26 +960,29 @@ cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
   return cudaGetLastError();
 }
 
-template <int D>
-cudaError_t launch_kivi_d(DecodeArgs& a, cudaStream_t s, int sm_count) {
-  // stored field widths: 3-bit codes run in the 4-bit kernels
-  const int kb = storage_bits(a.geo.kb), vb = storage_bits(a.geo.vb);
-  if (a.geo.mode_tq) {
-#define KVQ_CASE(K, V) \
-  if (kb == K && vb == V) return launch_kivi_instance<D, K, V, true, false>(a, s, sm_count);
-    KVQ_CASE(2, 2) KVQ_CASE(2, 4) KVQ_CASE(4, 2) KVQ_CASE(4, 4)
-#undef KVQ_CASE
-    return cudaErrorInvalidValue;
-  }
+// KIVI decode of K width K (the V width and the query form picked at run
+// time): one translation unit per (head_dim, K width) keeps the build parallel.
+template <int D, int K>
+cudaError_t launch_kivi_k(DecodeArgs& a, cudaStream_t s, int sm_count) {
   // an exact query operand unless RoPE is applied to the query here
   const bool qx = a.tab.rope == nullptr;
-#define KVQ_CASE(K, V)                                                                                    \
-  if (kb == K && vb == V)                                                                                 \
+#define KVQ_CASE(V)                                                                                       \
+  if (a.geo.vb == V)                                                                                      \
     return qx ? launch_kivi_instance<D, K, V, false, true>(a, s, sm_count)                               \
               : launch_kivi_instance<D, K, V, false, false>(a, s, sm_count);
-  KVQ_CASE(2, 2) KVQ_CASE(2, 4) KVQ_CASE(2, 8)
-  KVQ_CASE(4, 2) KVQ_CASE(4, 4) KVQ_CASE(4, 8)
-  KVQ_CASE(8, 2) KVQ_CASE(8, 4) KVQ_CASE(8, 8)
+  KVQ_CASE(2) KVQ_CASE(3) KVQ_CASE(4) KVQ_CASE(8)
+#undef KVQ_CASE
+  return cudaErrorInvalidValue;
+}
+
+// TurboQuant decode (K and V widths 2, 3 or 4).
+template <int D>
+cudaError_t launch_tq_d(DecodeArgs& a, cudaStream_t s, int sm_count) {
+#define KVQ_CASE(K, V) \
+  if (a.geo.kb == K && a.geo.vb == V) return launch_kivi_instance<D, K, V, true, false>(a, s, sm_count);
+  KVQ_CASE(2, 2) KVQ_CASE(2, 3) KVQ_CASE(2, 4)
+  KVQ_CASE(3, 2) KVQ_CASE(3, 3) KVQ_CASE(3, 4)
+  KVQ_CASE(4, 2) KVQ_CASE(4, 3) KVQ_CASE(4, 4)
 #undef KVQ_CASE
   return cudaErrorInvalidValue;
 }

@@ -6,9 +6,13 @@
 //   KIVI:       [K codes 32*D*kb/8][K scales D f16][K zeros D f16]
 //               [V codes 32*D*vb/8][V scales 32 x D/32 f16][V zeros D/32 x 32 f16]
 //               (both group-major, scales in lane order: vscale_pos, vzero_pos)
-//   TurboQuant: [K codes 32 x D*kb/8 row-major][K norms 32 f32]
+//   TurboQuant: [K codes 32*D*kb/8 in fragment order (tq_kfield_bit)][K norms 32 f32]
 //               [V codes 32 x D*vb/8 row-major][V norms 32 f32]
 // Chunk sizes are multiples of 16 bytes so one 1-D bulk copy moves a chunk.
+// 3-bit codes are packed tight, eight to three bytes (Foundry spec, "Step 3:
+// Packing", the no-waste form): a row-major code row is one little-endian
+// bit string with code c at bits 3c .. 3c+2; the fragment-order forms are
+// given below.
 //
 // KIVI codes are stored in the order the decode kernel's tensor-core
 // fragments consume them (the canonical, page-defined order is produced by
@@ -25,7 +29,10 @@
 // frag_bits gives: placed so that one mask turns a pair of codes into a pair
 // of narrow floats (e2m1 for 2-bit, e4m3 for 4-bit) or, for 8-bit, into a
 // pair of bytes 16 bits apart, each converted to an exact f16x2 by one
-// instruction in the decode kernel. Words are interleaved across
+// instruction in the decode kernel. 3-bit elements go in blocks of 32 (f /
+// 32) of three words each (frag3_bits), placed so that a mask or two turn
+// four codes into four bytes, each an e2m3 value code / 8 (the subnormal
+// binade, evenly spaced), converted two at a time. Words are interleaved across
 // lanes in 16-byte pieces (word w of lane L at byte ((w/4) * 32 + L) * 16 +
 // (w % 4) * 4) so that a warp's 16-byte loads are contiguous.
 // K scales are kept in the order the B operand is built: f16 position
@@ -54,11 +61,7 @@ struct Chunk {
   int kc_off, kmeta_off, vc_off, vmeta_off, bytes;
 };
 
-// Bits a code occupies in storage: 3-bit codes are kept two to a byte, in
-// the 4-bit layout (Foundry spec, "Step 3: Packing": [v0:3][v1:3][__:2]).
-KVQ_HD constexpr int storage_bits(int bits) { return bits == 3 ? 4 : bits; }
-
-// kb, vb: storage bits (storage_bits of the code widths).
+// kb, vb: code widths (2, 3, 4 or 8; codes packed tight).
 KVQ_HD Chunk chunk_layout(int mode_tq, int D, int kb, int vb) {
   Chunk c;
   c.kc_off = 0;
@@ -94,8 +97,14 @@ KVQ_HD void v_frag_pos(int D, int lane, int f, int* token, int* channel) {
   *token = 16 * kb + 2 * t + e + 8 * (r >> 1);
 }
 
-// Byte offset of 32-bit word w of lane `lane` inside a code region.
-KVQ_HD int code_word_offset(int lane, int w) { return (((w >> 2) * 32 + lane) << 4) + ((w & 3) << 2); }
+// Words per interleaved piece of a lane block of `words` words: 16-byte
+// pieces, or 8-byte ones where the block is not a whole number of 16-byte
+// pieces (3-bit codes at head_dim 64: 6 words per lane).
+KVQ_HD constexpr int piece_words(int words) { return words % 4 == 0 ? 4 : 2; }
+
+// Byte offset of 32-bit word w of lane `lane` inside a code region whose
+// lane blocks are interleaved in pieces of pw words.
+KVQ_HD int code_word_offset(int lane, int w, int pw = 4) { return ((w / pw) * 32 + lane) * (4 * pw) + (w % pw) * 4; }
 
 // f16 position of channel c inside the K scale array.
 KVQ_HD int kmeta_pos(int D, int c) {
@@ -140,6 +149,53 @@ KVQ_HD void frag_bits(int bits, int f, int* word, int* bit) {
   else if (bits == 4) *bit = 16 * (j & 1) + 4 * (j >> 1) + 8 * e;
   else *bit = 8 * j + 16 * e;
 }
+
+// 3-bit fragment blocks: element i (0 .. 31) of a block of three words
+// w0, w1, w2. Pair j = i / 2 (element e = i % 2) lies in quad q = j / 2 at
+// byte k = 2 (j % 2) + e of the quad's 32-bit value, which holds one code in
+// the low three bits of each byte:
+//   q 0..5: word q / 2, bits 8k + 3 (q % 2) .. +2 (quad = (w >> 3 (q % 2)) & 0x07070707)
+//   q 6:    low two bits at w0 bits 8k + 6, 7; high bit at w2 bit 8k + 6
+//   q 7:    low two bits at w1 bits 8k + 6, 7; high bit at w2 bit 8k + 7
+// (quads 6 and 7 = ((w0 or w1) >> 6 & 0x03030303) | (w2 >> 4 or 5 & 0x04040404)).
+KVQ_HD void frag3_put(uint32_t* w, int i, uint32_t code) {
+  const int j = i >> 1, e = i & 1, q = j >> 1, k = 2 * (j & 1) + e;
+  if (q < 6) {
+    w[q >> 1] |= (code & 7u) << (8 * k + 3 * (q & 1));
+  } else {
+    w[q - 6] |= (code & 3u) << (8 * k + 6);
+    w[2] |= ((code >> 2) & 1u) << (8 * k + 6 + (q - 6));
+  }
+}
+KVQ_HD uint32_t frag3_get(const uint32_t* w, int i) {
+  const int j = i >> 1, e = i & 1, q = j >> 1, k = 2 * (j & 1) + e;
+  if (q < 6) return (w[q >> 1] >> (8 * k + 3 * (q & 1))) & 7u;
+  return ((w[q - 6] >> (8 * k + 6)) & 3u) | (((w[2] >> (8 * k + 6 + (q - 6))) & 1u) << 2);
+}
+
+// TurboQuant K codes in fragment order. The A operand of scores^T = K q^T
+// (m16n8k16, rows = tokens, k = channels in natural order): lane (g, t) of
+// m-tile mt holds at k-step s the channel pairs (16 s + 2 t + 8 p, +1) of
+// the tokens 16 mt + g + 8 rh (p, rh in {0, 1}). One pair is one field (low
+// code | high code << kb, 2 kb bits). A lane's fields form one bit string of
+// D kb bits: four token blocks b = 2 mt + rh, each the D / 8 fields
+// j = 2 s + p in order, so one token's fields in one lane are a run of whole
+// bytes (D kb / 32 of them) and a writer of one token shares no byte with
+// another token. The strings are interleaved across lanes in pieces like
+// the KIVI words (byte k of lane L at lane_byte_offset(L, k, pw) with pw =
+// piece_words(D kb / 32)).
+KVQ_HD int tq_kfield_bit(int D, int kb, int b, int j) { return (b * (D / 8) + j) * 2 * kb; }
+KVQ_HD int lane_byte_offset(int lane, int k, int pw) { return code_word_offset(lane, k >> 2, pw) + (k & 3); }
+
+// TurboQuant V codes in token-pair rows: pair row pi (tokens 2 pi, 2 pi + 1
+// of the group, 16 rows per group) holds for every channel c one field (code
+// of token 2 pi | code of token 2 pi + 1 << vb, 2 vb bits): the A-operand
+// pair (channel c, tokens 2 pi, 2 pi + 1) of out^T = V^T p. The fields are in
+// the order c' = (c mod 8) D / 8 + c / 8 of one little-endian bit string of
+// D vb / 4 bytes, so the fields a decode lane g needs (channels g + 8 j) are
+// one block of D vb / 32 bytes at byte (c mod 8) D vb / 32, read as a whole.
+KVQ_HD constexpr int tq_vrow_bytes(int D, int vb) { return D * vb / 4; }
+KVQ_HD int tq_vfield_bit(int D, int vb, int c) { return 2 * vb * ((c % 8) * (D / 8) + c / 8); }
 
 // Arena geometry shared by every layer.
 struct Geometry {

@@ -71,8 +71,8 @@ typedef struct {
                          newest token may not exceed it                      */
   kv_mode mode;
   int k_bits, v_bits; /* KIVI: 2, 3, 4 or 8 each. TurboQuant: 2, 3 or 4.
-                         3-bit codes are stored two per byte ([P2] "Step 3:
-                         Packing": [v0:3][v1:3], two bits unused)            */
+                         Codes are packed tight: 3-bit codes eight to three
+                         bytes ([P2] "Step 3: Packing", the no-waste form)  */
   int group_size;     /* KIVI token/channel group: must be 32               */
   int residual;       /* fp16 residual tail before a group is quantised:
                          32 (one group) in KIVI mode, 0 in TurboQuant mode  */
@@ -257,13 +257,12 @@ kv_status kv_cache_stats(kv_cache* cache, int layer, kv_cache_stats_t* out);
  * quantised tokens [T0, T1) = [32 * floor(E / 32), Q_end), n = T1 - T0;
  * G = n / 32 groups (KIVI); S = sinks stored per sequence; R = L - F. */
 enum {
-  KV_EXPORT_K_CODES = 0,  /* u8  [B][Hkv][n][D/(8/k_bits)] packed along D,
-                             8/k_bits codes per byte (integer division: two
-                             3-bit codes per byte), code 0 in the least-
-                             significant bits                               */
+  KV_EXPORT_K_CODES = 0,  /* u8  [B][Hkv][n][D*k_bits/8]: each row one
+                             little-endian bit string along D, code c at
+                             bits c*k_bits .. (c+1)*k_bits-1                */
   KV_EXPORT_K_SCALE = 1,  /* f16 [B][Hkv][G][D]     (KIVI)                   */
   KV_EXPORT_K_ZERO = 2,   /* f16 [B][Hkv][G][D]     (KIVI)                   */
-  KV_EXPORT_V_CODES = 3,  /* u8  [B][Hkv][n][D/(8/v_bits)]                  */
+  KV_EXPORT_V_CODES = 3,  /* u8  [B][Hkv][n][D*v_bits/8], as K_CODES        */
   KV_EXPORT_V_SCALE = 4,  /* f16 [B][Hkv][n][D/32]  (KIVI)                   */
   KV_EXPORT_V_ZERO = 5,   /* f16 [B][Hkv][n][D/32]  (KIVI)                   */
   KV_EXPORT_K_NORM = 6,   /* f32 [B][Hkv][n]        (TurboQuant)             */

@@ -51,7 +51,8 @@ def test_tiny_one_at_a_time_and_prefill():
 
 @pytest.mark.parametrize("kb,vb,act", [(2, 4, "bf16"), (2, 2, "f16"), (4, 4, "f16"), (8, 8, "bf16"),
                                        (4, 2, "bf16"), (2, 8, "f16"), (8, 4, "f16"),
-                                       (3, 3, "f16"), (3, 2, "bf16"), (2, 3, "f16"), (8, 3, "bf16")])
+                                       (3, 3, "f16"), (3, 2, "bf16"), (2, 3, "f16"), (8, 3, "bf16"),
+                                       (3, 4, "bf16"), (4, 3, "f16"), (3, 8, "f16")])
 @pytest.mark.parametrize("D,H,Hq", [(128, 8, 32), (64, 4, 8), (128, 2, 2)])
 def test_prefill_then_appends(kb, vb, act, D, H, Hq):
     """Several tiles and a ragged tail: prefill 1000 tokens, then 45 appends

@@ -78,7 +78,7 @@ def test_ring_capacity_requires_eviction():
 
 @pytest.mark.parametrize("act", ["f16", "bf16"])
 @pytest.mark.parametrize("D", [128, 64])
-@pytest.mark.parametrize("kb,vb", [(4, 2), (4, 4), (2, 2), (2, 4), (3, 2), (4, 3), (3, 3)])
+@pytest.mark.parametrize("kb,vb", [(4, 2), (4, 4), (2, 2), (2, 4), (3, 2), (4, 3), (3, 3), (2, 3), (3, 4)])
 def test_turboquant_codes_and_attention(kb, vb, D, act):
     w = W.scaled(W.WORKLOADS["turboquant_k4v2"], batch=2, n_kv_heads=2, n_q_heads=8, head_dim=D,
                  k_bits=kb, v_bits=vb, act_dtype=act)
