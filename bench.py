@@ -134,7 +134,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-DECODE_SOURCES = ("decode_kivi.cuh", "decode_common.cuh", "decode.cu", "decode_d128.cu", "kvq_layout.h",
+DECODE_SOURCES = ("decode_kivi.cuh", "decode_common.cuh", "decode.cu", "decode_d128_k2.cu", "kvq_layout.h",
                   "kvq_internal.h", "kvq_device.cuh")
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "decode_traffic_llama8b.json")
 
