@@ -17,6 +17,13 @@ Sources (page title, section):
     window holds tokens until a group fills; dynamic top-k sinks.
   * Foundry "TurboQuant KV Cache Compression - Spec": per-token quantisation,
     attention over dequantised keys and values.
+  * posttrainllm "StreamingLLM + KIVI", "RoPE caveat": the "true"
+    re-positioning stores K before RoPE and rotates on read; "Caveats": per-
+    channel K quantisation then sees a basis that does not turn with the
+    position. With k_pre_rope the stored keys (codes, sinks, tail) are the
+    un-rotated inputs; attention rotates each retained key (dequantised, in
+    double) at its absolute position, or at its cache slot when
+    re-positioning, and the query as usual.
 
 Segments of one layer after L appended tokens (absolute positions), with
 N_s overlay sinks, W overlay window, E the eviction end ([N_s, E) evicted):
@@ -74,6 +81,7 @@ class CacheConfig:
     rope_base: float = 0.0
     rope_reposition: bool = False   # StreamingLLM position re-encoding at read
     v_q4_0: bool = False            # V in the symmetric q4_0 form (KIVI, 4-bit V)
+    k_pre_rope: bool = False        # keys stored before RoPE, rotated at read
 
 
 def validate(cfg: CacheConfig) -> None:
@@ -103,6 +111,8 @@ def validate(cfg: CacheConfig) -> None:
         raise ValueError("the q4_0 V form is a 4-bit KIVI V format")
     if cfg.rope_reposition and not cfg.rope_base:
         raise ValueError("re-positioning needs the cache to apply RoPE")
+    if cfg.k_pre_rope and (not cfg.rope_base or cfg.mode != "kivi" or cfg.n_dyn_sinks):
+        raise ValueError("pre-RoPE keys need RoPE in the cache, KIVI mode and no KVSink sinks")
     if cfg.n_dyn_sinks and (cfg.n_sink or cfg.window or cfg.evict_window):
         raise ValueError("KVSink sinks exclude the StreamingLLM overlay and eviction")
     if cfg.n_dyn_sinks > 32:
@@ -182,7 +192,7 @@ class OracleCache:
         st = self.layers[layer]
         if not self._capacity_ok(st, k.shape[2]):
             raise OverflowError("capacity")
-        if self.cfg.rope_base:
+        if self.cfg.rope_base and not self.cfg.k_pre_rope:
             k = rope.rotate_keys(k, st.L, self.cfg.rope_base, self.cfg.act_dtype)
         self._fold_sinks(layer, k, v)
         self._append_rotated(layer, k, v)
@@ -408,7 +418,12 @@ class OracleCache:
         for (b, h), js in by_kv.items():
             pos, K, V, _ = self.read_set(layer, b, h)
             K64 = K.astype(np.float64)
-            if cfg.rope_reposition:
+            if cfg.k_pre_rope:
+                # keys stored before RoPE: rotated here, at their cache slot
+                # when re-positioning, else at their absolute position
+                kpos = self.cache_position(layer, pos) if cfg.rope_reposition else pos
+                K64 = rope.rotate64(K64, kpos, cfg.rope_base)
+            elif cfg.rope_reposition:
                 # StreamingLLM re-positioning: un-rotate each stored key at
                 # its absolute position, rotate it at its cache slot
                 K64 = rope.rotate64(rope.rotate64(K64, -pos, cfg.rope_base),

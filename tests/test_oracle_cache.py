@@ -373,3 +373,94 @@ def test_reposition_is_vanilla_without_eviction_or_sinks():
     a = _ring_stream(False, 4, 300, seed=7)
     b = _ring_stream(True, 4, 300, seed=7)
     assert not np.allclose(a.decode_attn(0, q)[0], b.decode_attn(0, q)[0], rtol=1e-3)
+
+
+# ------------------------------------------------------------------ K before RoPE
+
+def test_pre_rope_codes_do_not_turn_with_the_position():
+    """posttrainllm "StreamingLLM + KIVI", "Caveats": K quantised before RoPE
+    sees a per-channel basis that does not turn with the position. The same
+    rows appended at position 0 or at 1024 get identical codes, scales and
+    zeros with k_pre_rope, and different ones with RoPE baked in."""
+    rng = np.random.default_rng(3)
+    xk, xv = _f16(rng, (1, 2, 64, 64)), _f16(rng, (1, 2, 64, 64))
+    filler = _f16(rng, (1, 2, 1024, 64))
+    for pre in (True, False):
+        kw = dict(batch=1, n_kv_heads=2, n_q_heads=2, head_dim=64, rope_base=10000.0, k_pre_rope=pre,
+                  max_tokens=2048)
+        a, b = OracleCache(_cfg(**kw)), OracleCache(_cfg(**kw))
+        a.append(0, xk, xv)
+        b.append(0, filler, filler)
+        b.append(0, xk, xv)
+        ea, eb = a.export(0), b.export(0)
+        same_codes = np.array_equal(ea["k_codes"], eb["k_codes"][:, :, 1024:])
+        same_scales = np.array_equal(ea["k_scale"].view(np.uint16), eb["k_scale"][:, :, 32:].view(np.uint16))
+        assert same_codes == pre and same_scales == pre
+        assert np.array_equal(ea["v_codes"], eb["v_codes"][:, :, 1024:])   # V never rotates
+
+
+def _one_pair_cache(pre, reposition, n_sink, keep, T, a_q=6.0, b_k=1.0, D=64):
+    """T tokens whose keys are b e_0 (the first RoPE pair, theta_0 = 1) and
+    whose values are zero except the first token's (e_1), streamed one by one
+    with eviction (every kept row exact: the window is the kept span);
+    returns the cache and q = a e_0."""
+    c = OracleCache(_cfg(batch=1, n_kv_heads=1, n_q_heads=1, head_dim=D, k_bits=8, v_bits=8,
+                         n_sink=n_sink, window=keep or 4096, evict_window=keep, rope_base=10000.0,
+                         rope_reposition=reposition, k_pre_rope=pre, max_tokens=4096 + 64))
+    for t in range(T):
+        k = np.zeros((1, 1, 1, D), np.float32)
+        v = np.zeros((1, 1, 1, D), np.float32)
+        k[0, 0, 0, 0] = b_k
+        if t == 0:
+            v[0, 0, 0, 1] = 1.0
+        c.append(0, k, v)
+        c.evict(0)
+    q = np.zeros((1, 1, D), np.float32)
+    q[0, 0, 0] = a_q
+    return c, q
+
+
+def test_pre_rope_scores_follow_the_relative_rotation():
+    """Keys rotated on read: a key d positions behind the query meets it
+    rotated by d theta_0 in the first pair, so with q = a e_0 and every key
+    b e_0 its score is a b cos(d) / sqrt(D), whatever the absolute position
+    (all rows exact: the window covers them). The first token's value is e_1,
+    so out[1] is its softmax weight: e^s0 / sum_p e^sp."""
+    D, T, a, b = 64, 40, 6.0, 1.0
+    c, q = _one_pair_cache(True, False, 0, 0, T, a, b, D)
+    s = [a * b * math.cos(T - 1 - p) / math.sqrt(D) for p in range(T)]
+    w0 = math.exp(s[0]) / sum(math.exp(x) for x in s)
+    out, _ = c.decode_attn(0, q)
+    assert abs(float(out[0, 0, 1]) - w0) < 1e-6
+    assert np.all(np.delete(out[0, 0], 1) == 0.0)
+
+
+def test_pre_rope_reposition_closed_form_after_eviction():
+    """"True" re-positioning (posttrainllm "RoPE caveat": store K pre-RoPE and
+    rotate at the compressed index): after eviction the sink keeps slot 0,
+    the kept tokens slots 1 .. keep and the query slot keep; each score is
+    a b cos(slot_q - slot) / sqrt(D). The first token is the sink (value
+    e_1). Without re-positioning the sink sits T - 1 back."""
+    D, T, keep, a, b = 64, 200, 48, 6.0, 1.0
+    for reposition in (True, False):
+        c, q = _one_pair_cache(True, reposition, 1, keep, T, a, b, D)
+        assert c.layers[0].E == T - keep
+        kept = [0] + list(range(T - keep, T))            # absolute positions still read
+        if reposition:
+            slots = [0] + list(range(1, keep + 1))
+            qslot = keep
+        else:
+            slots, qslot = kept, T - 1
+        s = [a * b * math.cos(qslot - sl) / math.sqrt(D) for sl in slots]
+        w0 = math.exp(s[0]) / sum(math.exp(x) for x in s)
+        out, _ = c.decode_attn(0, q)
+        assert abs(float(out[0, 0, 1]) - w0) < 1e-6
+
+
+def test_pre_rope_rules():
+    with pytest.raises(ValueError):
+        OracleCache(_cfg(k_pre_rope=True))                                   # needs RoPE in the cache
+    with pytest.raises(ValueError):
+        OracleCache(_cfg(k_pre_rope=True, rope_base=10000.0, mode="turboquant"))
+    with pytest.raises(ValueError):
+        OracleCache(_cfg(k_pre_rope=True, rope_base=10000.0, n_dyn_sinks=3))
