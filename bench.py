@@ -538,6 +538,12 @@ OTHER_WORKLOADS = {
     "ring_int4_repos": dict(batch=64, n_kv_heads=8, n_q_heads=8, head_dim=64, context=4100, act_dtype="f16",
                             mode="kivi", k_bits=4, v_bits=4, n_sink=4, evict_window=4096, rope_base=10000.0,
                             rope_reposition=True, layers=12),
+    "ring_int4_prerope": dict(batch=64, n_kv_heads=8, n_q_heads=8, head_dim=64, context=4100, act_dtype="f16",
+                              mode="kivi", k_bits=4, v_bits=4, n_sink=4, evict_window=4096, rope_base=10000.0,
+                              k_pre_rope=True, layers=12),
+    "ring_int4_prerope_repos": dict(batch=64, n_kv_heads=8, n_q_heads=8, head_dim=64, context=4100,
+                                    act_dtype="f16", mode="kivi", k_bits=4, v_bits=4, n_sink=4, evict_window=4096,
+                                    rope_base=10000.0, k_pre_rope=True, rope_reposition=True, layers=12),
 }
 
 
@@ -561,7 +567,8 @@ def run_workload(args):
                k_bits=w["k_bits"], v_bits=w["v_bits"], n_sink=w.get("n_sink", 0), window=0,
                evict_window=w.get("evict_window", 0), n_dyn_sinks=w.get("n_dyn_sinks", 0), act_dtype=w["act_dtype"],
                rope_base=w.get("rope_base", 0.0), rope_max_pos=(L + n_total + 64 if w.get("rope_base") else 0),
-               rope_reposition=w.get("rope_reposition", False), v_q4_0=w.get("v_q4_0", False))
+               rope_reposition=w.get("rope_reposition", False), v_q4_0=w.get("v_q4_0", False),
+               k_pre_rope=w.get("k_pre_rope", False))
     warm_prefill(torch, binding, dev, cfg, dt)
     cache = binding.KVCache(device=dev, **cfg)
     g = torch.Generator(device=dev)

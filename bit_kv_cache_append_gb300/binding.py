@@ -44,7 +44,7 @@ class CacheConfig(ctypes.Structure):
                 ("window", ctypes.c_int), ("evict_window", ctypes.c_int), ("n_dyn_sinks", ctypes.c_int),
                 ("act_dtype", ctypes.c_int), ("seed", ctypes.c_uint64), ("rope_base", ctypes.c_double),
                 ("rope_max_pos", ctypes.c_int64), ("max_splits", ctypes.c_int),
-                ("rope_reposition", ctypes.c_int), ("v_q4_0", ctypes.c_int)]
+                ("rope_reposition", ctypes.c_int), ("v_q4_0", ctypes.c_int), ("k_pre_rope", ctypes.c_int)]
 
 
 class CacheStats(ctypes.Structure):
@@ -106,13 +106,14 @@ def check(status: int) -> None:
 def make_config(*, n_layers, batch, n_kv_heads, n_q_heads, head_dim, max_tokens, mode="kivi", k_bits=2,
                 v_bits=4, n_sink=0, window=0, evict_window=0, n_dyn_sinks=0, act_dtype="f16", seed=0,
                 rope_base=0.0, rope_max_pos=0, max_splits=0, rope_reposition=False,
-                v_q4_0=False) -> CacheConfig:
+                v_q4_0=False, k_pre_rope=False) -> CacheConfig:
     tq = mode == "turboquant"
     return CacheConfig(n_layers, batch, n_kv_heads, n_q_heads, head_dim, max_tokens,
                        KV_MODE_TURBOQUANT if tq else KV_MODE_KIVI, k_bits, v_bits, 32, 0 if tq else 32,
                        n_sink, window, evict_window, n_dyn_sinks,
                        KV_DT_BF16 if act_dtype == "bf16" else KV_DT_F16, seed, float(rope_base),
-                       rope_max_pos, max_splits, int(bool(rope_reposition)), int(bool(v_q4_0)))
+                       rope_max_pos, max_splits, int(bool(rope_reposition)), int(bool(v_q4_0)),
+                       int(bool(k_pre_rope)))
 
 
 def required_bytes(cfg: CacheConfig) -> int:

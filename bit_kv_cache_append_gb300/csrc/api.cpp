@@ -107,6 +107,8 @@ kv_status check_config(const kv_cache_config* c) {
   if (c->rope_reposition && !(c->rope_base > 0.0))
     return fail(KV_ERR_INVALID_ARG, "rope_reposition needs the cache to apply RoPE (rope_base > 0)");
   if (c->max_splits < 0 || c->max_splits > 4096) return fail(KV_ERR_INVALID_ARG, "max_splits out of range");
+  if (c->k_pre_rope && (!(c->rope_base > 0.0) || c->mode != KV_MODE_KIVI || c->n_dyn_sinks))
+    return fail(KV_ERR_INVALID_ARG, "k_pre_rope needs rope_base > 0, KIVI mode and no KVSink sinks");
   return KV_OK;
 }
 
@@ -134,6 +136,7 @@ Geometry make_geometry(const kv_cache_config* c) {
   g.rope_max_pos = c->rope_base > 0.0 ? c->rope_max_pos : 0;
   g.rope_repos = c->rope_reposition ? 1 : 0;
   g.v_q4_0 = c->v_q4_0 ? 1 : 0;
+  g.k_pre_rope = c->k_pre_rope ? 1 : 0;
 
   const size_t B = g.B, H = g.H, D = g.D;
   size_t off = 0;
@@ -248,6 +251,7 @@ kv_status do_append(kv_cache* c, int layer, const void* k, const void* v, int n,
   a.geo = g;
   a.lay = layer_dev(c, layer);
   a.tab = tables_dev(c);
+  if (g.k_pre_rope) a.tab.rope = nullptr;  // keys are stored before RoPE
   a.k = static_cast<const uint16_t*>(k);
   a.v = static_cast<const uint16_t*>(v);
   a.n = n;
@@ -455,6 +459,8 @@ kv_status decode_attn_impl(kv_cache* cache, int layer, const void* q, float* out
   a.n_dyn_sel = ls.n_dyn_sel;
   // re-positioning moves the query against the sinks by the evicted span
   a.sink_qpos = ls.L - 1 - (g.rope_repos ? ls.E - g.n_sink : 0);
+  a.key_shift = (g.k_pre_rope && g.rope_repos) ? ls.E - g.n_sink : 0;
+  a.q_pos = ls.L - 1 - a.key_shift;
   a.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(g.D)));
   const int64_t units = static_cast<int64_t>(g.B) * g.H;
   if (a.F > a.qlo) {
@@ -772,7 +778,7 @@ kv_status kv_cache_export(kv_cache* cache, int layer, int what, void* host_dst, 
               for (int lane = 0; lane < 32; ++lane)
                 for (int f = 0; f < D; ++f) {
                   int tok, ch;
-                  if (isk) kvq::k_frag_pos(static_cast<int>(D), lane, f, &tok, &ch);
+                  if (isk) kvq::k_frag_pos(static_cast<int>(D), lane, f, &tok, &ch, g.k_pre_rope != 0);
                   else kvq::v_frag_pos(static_cast<int>(D), lane, f, &tok, &ch);
                   uint32_t code;
                   if (bits == 3) {
@@ -791,8 +797,9 @@ kv_status kv_cache_export(kv_cache* cache, int layer, int what, void* host_dst, 
             uint16_t* o = reinterpret_cast<uint16_t*>(dst) + (bh * p.G + gi) * D;
             const bool zero = what == KV_EXPORT_K_ZERO;
             for (int ch = 0; ch < D; ++ch) {
-              const int pos = zero ? static_cast<int>(D) + kvq::kzero_pos(static_cast<int>(D), ch)
-                                   : kvq::kmeta_pos(static_cast<int>(D), ch);
+              const int pos = g.k_pre_rope ? (zero ? static_cast<int>(D) + ch : ch)
+                              : zero       ? static_cast<int>(D) + kvq::kzero_pos(static_cast<int>(D), ch)
+                                           : kvq::kmeta_pos(static_cast<int>(D), ch);
               std::memcpy(o + ch, chunk.data() + g.chunk.kmeta_off + pos * 2, 2);
             }
           } else if (what == KV_EXPORT_V_SCALE || what == KV_EXPORT_V_ZERO) {

@@ -76,12 +76,17 @@ __device__ __forceinline__ void quantize_slice_params(float mn, float mx, int bi
 // more than 1e-4 the two round to the same integer, and beyond 257 the clamp
 // decides; within 1e-4 of a half-integer the correctly rounded division is
 // taken, so the code equals rint(fl((x - z) / s)) in every case.
+// The correctly rounded quotient's integer, out of line: it runs only for
+// quotients within 1e-4 of a half-integer, and inlined it would multiply the
+// size of every quantisation loop.
+__device__ __noinline__ float rint_of_quotient(float d, float s) { return rintf(__fdiv_rn(d, s)); }
+
 template <int LB>
 __device__ __forceinline__ uint32_t quantize_code(float x, float s, float z, float rs) {
   const float d = __fsub_rn(x, z);
   const float q = __fmul_rn(d, rs);
   float qr = rintf(q);
-  if (fabsf(__fsub_rn(q, qr)) > 0.4999f) qr = rintf(__fdiv_rn(d, s));  // within 1e-4 of a half-integer
+  if (fabsf(__fsub_rn(q, qr)) > 0.4999f) qr = rint_of_quotient(d, s);  // within 1e-4 of a half-integer
   qr = fminf(fmaxf(qr, 0.0f), static_cast<float>(LB));
   return static_cast<uint32_t>(qr);
 }
@@ -101,11 +106,12 @@ __device__ __forceinline__ int word_bit(int i) {
 // v_frag_pos): a constant, so that packing loads each code with one
 // shared-memory byte load (rows are D + 4 bytes: the lanes' loads fall in
 // distinct banks or share a word).
-template <int D, bool IS_K>
+template <int D, bool IS_K, bool PR>
 __device__ __forceinline__ constexpr int frag_code_offset(int f) {
   const int e = f & 1, r = (f >> 1) & 3, hi = f >> 3;
   if (IS_K) {
     const int mt = hi / (D / 16), s = hi % (D / 16);
+    if (PR) return (16 * mt + 8 * (r & 1)) * (D + 4) + 2 * s + (r >> 1) + e * (D / 2);
     return (16 * mt + 8 * (r & 1)) * (D + 4) + 4 * s + 2 * (r >> 1) + e;
   }
   const int m = hi >> 1, kb = hi & 1;
@@ -114,18 +120,19 @@ __device__ __forceinline__ constexpr int frag_code_offset(int f) {
 
 // Words [W0, W0 + NW) of every lane's K (IS_K) or V fragment block, packed
 // by this warp's thread `lane` for fragment lane `lane`; 3-bit codes in
-// blocks of three words (W0, NW multiples of 3).
-template <int D, int BITS, bool IS_K, int W0, int NW>
+// blocks of three words (W0, NW multiples of 3). PR: the K channel order of
+// keys stored before RoPE (kvq_layout.h k_frag_pos).
+template <int D, int BITS, bool IS_K, bool PR, int W0, int NW>
 __device__ __forceinline__ void pack_words(const uint8_t (*cs)[D + 4], uint8_t* region, int lane) {
   constexpr int WPL = D * BITS / 32, PW = piece_words(WPL);
   const int g = lane >> 2, t = lane & 3;
-  const uint8_t* base = IS_K ? &cs[g][t * (D / 4)] : &cs[2 * t][g];
+  const uint8_t* base = IS_K ? &cs[g][t * (PR ? D / 8 : D / 4)] : &cs[2 * t][g];
   if constexpr (BITS == 3) {
 #pragma unroll
     for (int blk = W0 / 3; blk < (W0 + NW) / 3; ++blk) {
       uint32_t w[3] = {0u, 0u, 0u};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) frag3_put(w, i, base[frag_code_offset<D, IS_K>(32 * blk + i)]);
+      for (int i = 0; i < 32; ++i) frag3_put(w, i, base[frag_code_offset<D, IS_K, PR>(32 * blk + i)]);
 #pragma unroll
       for (int q = 0; q < 3; ++q)
         *reinterpret_cast<uint32_t*>(region + code_word_offset(lane, 3 * blk + q, PW)) = w[q];
@@ -137,7 +144,7 @@ __device__ __forceinline__ void pack_words(const uint8_t (*cs)[D + 4], uint8_t* 
       uint32_t word = 0;
 #pragma unroll
       for (int i = 0; i < PER; ++i)
-        word |= static_cast<uint32_t>(base[frag_code_offset<D, IS_K>(w * PER + i)]) << word_bit<BITS>(i);
+        word |= static_cast<uint32_t>(base[frag_code_offset<D, IS_K, PR>(w * PER + i)]) << word_bit<BITS>(i);
       *reinterpret_cast<uint32_t*>(region + code_word_offset(lane, w, PW)) = word;
     }
   }
@@ -146,16 +153,16 @@ __device__ __forceinline__ void pack_words(const uint8_t (*cs)[D + 4], uint8_t* 
 // The codes of one group (cs[token][channel]) in the decode kernel's
 // fragment order: the D / 32 warps of the CTA take equal shares of the
 // words of every lane's block.
-template <int D, int BITS, bool IS_K>
+template <int D, int BITS, bool IS_K, bool PR = false>
 __device__ __forceinline__ void pack_fragments(const uint8_t (*cs)[D + 4], uint8_t* region, int tid) {
   constexpr int NWARP = D / 32, NW = D * BITS / 32 / NWARP;
   static_assert(NW * NWARP == D * BITS / 32 && (BITS != 3 || NW % 3 == 0), "equal shares");
   const int warp = tid >> 5, lane = tid & 31;
-  if (warp == 0) pack_words<D, BITS, IS_K, 0, NW>(cs, region, lane);
-  else if (warp == 1) pack_words<D, BITS, IS_K, NW, NW>(cs, region, lane);
+  if (warp == 0) pack_words<D, BITS, IS_K, PR, 0, NW>(cs, region, lane);
+  else if (warp == 1) pack_words<D, BITS, IS_K, PR, NW, NW>(cs, region, lane);
   if constexpr (NWARP > 2) {
-    if (warp == 2) pack_words<D, BITS, IS_K, 2 * NW, NW>(cs, region, lane);
-    else if (warp == 3) pack_words<D, BITS, IS_K, 3 * NW, NW>(cs, region, lane);
+    if (warp == 2) pack_words<D, BITS, IS_K, PR, 2 * NW, NW>(cs, region, lane);
+    else if (warp == 3) pack_words<D, BITS, IS_K, PR, 3 * NW, NW>(cs, region, lane);
   }
 }
 
@@ -170,8 +177,8 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
   // that 16-byte row stores stay aligned and column reads spread over banks)
   __shared__ __align__(16) uint16_t xk[32][D + 8];
   __shared__ __align__(16) uint16_t xv[32][D + 8];
-  __shared__ uint8_t ck[32][D + 4];  // rows padded by a word: the packing gathers down columns
-  __shared__ uint8_t cv[32][D + 4];
+  __shared__ __align__(16) uint8_t ck[32][D + 4];  // rows padded by a word: the packing gathers down columns
+  __shared__ __align__(16) uint8_t cv[32][D + 4];
   __shared__ int sub[32];
   __shared__ uint32_t smask;
   const Geometry& G = a.geo;
@@ -230,81 +237,119 @@ __global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
   __syncthreads();
 
   uint8_t* chunk = a.lay.chunks + (static_cast<size_t>(bh) * G.n_slots + slot) * G.chunk.bytes;
-  {  // K: channel tid over the 32 tokens
-    const int c = tid;
-    float mn = act_to_float(xk[0][c], bf16), mx = mn;
-#pragma unroll 8
+  // the first half of the threads quantise K (two channels each, over the
+  // 32 tokens), the second half V (two (token, 32-channel group) slices
+  // each); every value is read from shared memory once (32-bit and 16-byte
+  // loads) and kept in registers between min/max and the codes
+  if (tid < D / 2) {  // K: channels 2 tid, 2 tid + 1
+    const int c = 2 * tid;
+    auto kpair = [&](int r) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(&xk[r][c]);
+      return make_float2(act_to_float(static_cast<uint16_t>(w & 0xffffu), bf16),
+                         act_to_float(static_cast<uint16_t>(w >> 16), bf16));
+    };
+    float2 x = kpair(0);
+    float mn0 = x.x, mx0 = x.x, mn1 = x.y, mx1 = x.y;
+#pragma unroll 4
     for (int r = 1; r < 32; ++r) {
-      const float x = act_to_float(xk[r][c], bf16);
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
+      x = kpair(r);
+      mn0 = fminf(mn0, x.x), mx0 = fmaxf(mx0, x.x);
+      mn1 = fminf(mn1, x.y), mx1 = fmaxf(mx1, x.y);
     }
-    __half sh, zh;
-    float s, z;
-    quantize_slice_params(mn, mx, KB, &sh, &zh, &s, &z);
-    const float rs = __frcp_rn(s);
-#pragma unroll 8
-    for (int r = 0; r < 32; ++r)
-      ck[r][c] = static_cast<uint8_t>(quantize_code<LK>(act_to_float(xk[r][c], bf16), s, z, rs));
+    __half sh0, zh0, sh1, zh1;
+    float s0, z0, s1, z1;
+    quantize_slice_params(mn0, mx0, KB, &sh0, &zh0, &s0, &z0);
+    quantize_slice_params(mn1, mx1, KB, &sh1, &zh1, &s1, &z1);
+    const float rs0 = __frcp_rn(s0), rs1 = __frcp_rn(s1);
+#pragma unroll 4
+    for (int r = 0; r < 32; ++r) {
+      x = kpair(r);
+      const uint32_t q0 = quantize_code<LK>(x.x, s0, z0, rs0), q1 = quantize_code<LK>(x.y, s1, z1, rs1);
+      *reinterpret_cast<uint16_t*>(&ck[r][c]) = static_cast<uint16_t>(q0 | (q1 << 8));
+    }
+    // K scales and zeros in the decode's B-operand orders (keys stored
+    // before RoPE: the natural channel order)
     __half* km = reinterpret_cast<__half*>(chunk + G.chunk.kmeta_off);
-    km[kmeta_pos(D, c)] = sh;
-    km[D + kzero_pos(D, c)] = zh;
-  }
-  {  // V: token r, channel group vg (index rotated by 8 vg to spread banks)
-    const int r = tid / NV, vg = tid % NV, base = 32 * vg;
-    float mn = act_to_float(xv[r][base + ((8 * vg) & 31)], bf16), mx = mn;
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i) {
-      const float x = act_to_float(xv[r][base + ((i + 8 * vg) & 31)], bf16);
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
-    }
-    __half sh, zh;
-    if (VB == 4 && G.v_q4_0) {
-      // the symmetric q4_0 form ([P3] "Summary"): d = m / -8 with m the value
-      // of largest magnitude (the first in channel order on ties), code
-      // min(15, floor(x / d + 8.5)) from the stored d, zero -8 d
-      float m = 0.0f, am = -1.0f;
-      int mi = 32;
-#pragma unroll 8
-      for (int i = 0; i < 32; ++i) {
-        const int j = (i + 8 * vg) & 31;
-        const float x = act_to_float(xv[r][base + j], bf16);
-        const float ax = fabsf(x);
-        if (ax > am || (ax == am && j < mi)) {
-          am = ax;
-          m = x;
-          mi = j;
+    const bool pr = G.k_pre_rope;
+    km[pr ? c : kmeta_pos(D, c)] = sh0;
+    km[D + (pr ? c : kzero_pos(D, c))] = zh0;
+    km[pr ? c + 1 : kmeta_pos(D, c + 1)] = sh1;
+    km[D + (pr ? c + 1 : kzero_pos(D, c + 1))] = zh1;
+  } else {  // V: two (token r, channel group vg) slices
+#pragma unroll 1
+    for (int k = 0; k < 2; ++k) {
+      const int si = tid - D / 2 + k * (D / 2);
+      const int r = si % 32, vg = si / 32, base = 32 * vg;  // a warp's lanes take 32 rows: no bank conflicts
+      const uint4* row = reinterpret_cast<const uint4*>(&xv[r][base]);  // 4 x 8 values
+      auto unpack8 = [&](const uint4& u, float (&o)[8]) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          o[2 * i] = act_to_float(static_cast<uint16_t>(w[i] & 0xffffu), bf16);
+          o[2 * i + 1] = act_to_float(static_cast<uint16_t>(w[i] >> 16), bf16);
+        }
+      };
+      __half sh, zh;
+      float o[8];
+      if (VB == 4 && G.v_q4_0) {
+        // the symmetric q4_0 form ([P3] "Summary"): d = m / -8 with m the value
+        // of largest magnitude (the first in channel order on ties), code
+        // min(15, floor(x / d + 8.5)) from the stored d, zero -8 d
+        float m = 0.0f, am = -1.0f;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          unpack8(row[q], o);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (fabsf(o[i]) > am) am = fabsf(o[i]), m = o[i];
+        }
+        sh = __float2half_rn(__fdiv_rn(m, -8.0f));
+        const float d = __half2float(sh);
+        zh = __float2half_rn(__fmul_rn(d, -8.0f));  // exact: a power-of-two multiple
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          unpack8(row[q], o);
+          uint32_t cw[2] = {0u, 0u};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float qv = 8.0f;
+            if (d != 0.0f) qv = fminf(fmaxf(floorf(__fadd_rn(__fdiv_rn(o[i], d), 8.5f)), 0.0f), 15.0f);
+            cw[i >> 2] |= static_cast<uint32_t>(qv) << (8 * (i & 3));
+          }
+          reinterpret_cast<uint32_t*>(&cv[r][base + 8 * q])[0] = cw[0];  // rows of D + 4 bytes: 4-byte aligned
+          reinterpret_cast<uint32_t*>(&cv[r][base + 8 * q])[1] = cw[1];
+        }
+      } else {
+        float mn = INFINITY, mx = -INFINITY;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          unpack8(row[q], o);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mn = fminf(mn, o[i]), mx = fmaxf(mx, o[i]);
+        }
+        float sv, zv;
+        quantize_slice_params(mn, mx, VB, &sh, &zh, &sv, &zv);
+        const float rs = __frcp_rn(sv);
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          unpack8(row[q], o);
+          uint32_t cw[2] = {0u, 0u};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) cw[i >> 2] |= quantize_code<LV>(o[i], sv, zv, rs) << (8 * (i & 3));
+          reinterpret_cast<uint32_t*>(&cv[r][base + 8 * q])[0] = cw[0];  // rows of D + 4 bytes: 4-byte aligned
+          reinterpret_cast<uint32_t*>(&cv[r][base + 8 * q])[1] = cw[1];
         }
       }
-      sh = __float2half_rn(__fdiv_rn(m, -8.0f));
-      const float d = __half2float(sh);
-      zh = __float2half_rn(__fmul_rn(d, -8.0f));  // exact: a power-of-two multiple
-#pragma unroll 8
-      for (int i = 0; i < 32; ++i) {
-        const int c = base + ((i + 8 * vg) & 31);
-        float q = 8.0f;
-        if (d != 0.0f) q = fminf(fmaxf(floorf(__fadd_rn(__fdiv_rn(act_to_float(xv[r][c], bf16), d), 8.5f)), 0.0f), 15.0f);
-        cv[r][c] = static_cast<uint8_t>(q);
-      }
-    } else {
-      float s, z;
-      quantize_slice_params(mn, mx, VB, &sh, &zh, &s, &z);
-      const float rs = __frcp_rn(s);
-#pragma unroll 8
-      for (int i = 0; i < 32; ++i) {
-        const int c = base + ((i + 8 * vg) & 31);
-        cv[r][c] = static_cast<uint8_t>(quantize_code<LV>(act_to_float(xv[r][c], bf16), s, z, rs));
-      }
+      __half* vm = reinterpret_cast<__half*>(chunk + G.chunk.vmeta_off);
+      vm[vscale_pos(NV, r, vg)] = sh;
+      vm[vzero_pos(NV, r, vg)] = zh;
     }
-    __half* vm = reinterpret_cast<__half*>(chunk + G.chunk.vmeta_off);
-    vm[vscale_pos(NV, r, vg)] = sh;
-    vm[vzero_pos(NV, r, vg)] = zh;
   }
   __syncthreads();
 
   // pack in the decode kernel's fragment order (kvq_layout.h)
-  pack_fragments<D, SK, true>(ck, chunk + G.chunk.kc_off, tid);
+  if (G.k_pre_rope) pack_fragments<D, SK, true, true>(ck, chunk + G.chunk.kc_off, tid);
+  else pack_fragments<D, SK, true>(ck, chunk + G.chunk.kc_off, tid);
   pack_fragments<D, SV, false>(cv, chunk + G.chunk.vc_off, tid);
   if (G.n_dyn && h == 0 && tid == 0) a.lay.sink_mask[b * G.n_slots + slot] = smask;
 }

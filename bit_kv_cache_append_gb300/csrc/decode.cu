@@ -54,7 +54,9 @@ size_t merge_smem_bytes(int stage_bytes) {
 // (x = D FWHT(y) / sqrt(d)) before the exact part, which is in the original
 // domain, is added (Foundry "TurboQuant KV Cache Compression - Spec",
 // "Optimization: Fused dequant-dot": rotate the accumulated output once).
-template <int D, bool REPOS>
+// XM: 0 the exact rows as stored, 1 re-positioning (sinks re-scored against
+// the query at sink_qpos), 2 keys stored before RoPE (rotated on read).
+template <int D, int XM>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(DecodeArgs a, int stage_bytes) {
   constexpr int NS = D / 32, NW = kMergeWarps;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -63,8 +65,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(DecodeArgs a, i
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 1);
   const Geometry& G = a.geo;
   const int u = blockIdx.x, b = u / G.H, h = u % G.H;
-  const bool ok = G.act_bf16 ? exact_states_tc<D, NW, true, REPOS>(a, b, h, red, smem, stage_bytes, bar, abort_flag)
-                             : exact_states_tc<D, NW, false, REPOS>(a, b, h, red, smem, stage_bytes, bar, abort_flag);
+  bool ok = true;
+  if constexpr (XM == 2)
+    exact_states_prerope<D, NW>(a, b, h, red, reinterpret_cast<float*>(smem));
+  else
+    ok = G.act_bf16 ? exact_states_tc<D, NW, true, XM == 1>(a, b, h, red, smem, stage_bytes, bar, abort_flag)
+                    : exact_states_tc<D, NW, false, XM == 1>(a, b, h, red, smem, stage_bytes, bar, abort_flag);
   if (!ok && threadIdx.x == 0) set_error(a.tab.err_flag, kErrTimeout);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= G.gqa) return;
@@ -146,7 +152,7 @@ int merge_stage_bytes(const Geometry& G) {
 // scheduled before it ends (programmatic dependent launch); otherwise it is
 // an ordinary launch, since its exact pools read rows the appends before it
 // wrote.
-template <int D, bool REPOS>
+template <int D, int XM>
 cudaError_t launch_merge_instance(DecodeArgs& a, cudaStream_t s, bool after_split) {
   const int stage = merge_stage_bytes(a.geo);
   const size_t smem = merge_smem_bytes<D>(stage);
@@ -156,7 +162,7 @@ cudaError_t launch_merge_instance(DecodeArgs& a, cudaStream_t s, bool after_spli
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (smem > configured[dev]) {
-    e = cudaFuncSetAttribute(merge_kernel<D, REPOS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(merge_kernel<D, XM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     configured[dev] = smem;
@@ -171,13 +177,14 @@ cudaError_t launch_merge_instance(DecodeArgs& a, cudaStream_t s, bool after_spli
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = after_split ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, merge_kernel<D, REPOS>, a, stage);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<D, XM>, a, stage);
 }
 
 template <int D>
 cudaError_t launch_merge(DecodeArgs& a, cudaStream_t s, bool after_split) {
-  return a.sink_qpos != a.L - 1 ? launch_merge_instance<D, true>(a, s, after_split)
-                                : launch_merge_instance<D, false>(a, s, after_split);
+  if (a.geo.k_pre_rope) return launch_merge_instance<D, 2>(a, s, after_split);
+  return a.sink_qpos != a.L - 1 ? launch_merge_instance<D, 1>(a, s, after_split)
+                                : launch_merge_instance<D, 0>(a, s, after_split);
 }
 
 }  // namespace

@@ -178,9 +178,10 @@ __device__ __forceinline__ uint32_t split_h2(float x0, float x1, bool lo) {
   return f2_to_h2(__fsub_rn(x0, hf.x), __fsub_rn(x1, hf.y));
 }
 
-// The query of one GQA row at full precision: RoPE at position L - 1 when the
-// cache applies it (float32, not rounded), then times log2(e) / sqrt(D).
-__device__ __forceinline__ float query_value(const DecodeArgs& a, int b, int hq, int c) {
+// The query of one GQA row at full precision: RoPE at position qpos (L - 1
+// unless keys are re-positioned) when the cache applies it (float32, not
+// rounded), then times log2(e) / sqrt(D).
+__device__ __forceinline__ float query_value(const DecodeArgs& a, int b, int hq, int c, int64_t qpos = -1) {
   const Geometry& G = a.geo;
   const int D = G.D, half = D / 2;
   const uint16_t* qrow = a.q + (static_cast<size_t>(b) * G.Hq + hq) * D;
@@ -188,7 +189,7 @@ __device__ __forceinline__ float query_value(const DecodeArgs& a, int b, int hq,
   if (a.tab.rope) {
     const int i = c < half ? c : c - half;
     const float y = act_to_float(qrow[c < half ? c + half : c - half], G.act_bf16);
-    const float* tr = a.tab.rope + static_cast<size_t>(a.L - 1) * D;
+    const float* tr = a.tab.rope + static_cast<size_t>(qpos >= 0 ? qpos : a.L - 1) * D;
     float ra, rb;
     if (c < half) rope_pair(x, y, tr[2 * i], tr[2 * i + 1], &ra, &rb), x = ra;
     else rope_pair(y, x, tr[2 * i], tr[2 * i + 1], &ra, &rb), x = rb;
@@ -350,6 +351,91 @@ __device__ __forceinline__ uint32_t split_act2(float x0, float x1, bool lo) {
   if (!lo) return h;
   const float2 hf = unpack_act2<BF>(h);
   return pack_act2<BF>(__fsub_rn(x0, hf.x), __fsub_rn(x1, hf.y));
+}
+
+// The exact pools of one (b, h) when keys are stored before RoPE: every
+// row's key is rotated at its position (its cache slot: p below n_sink, else
+// p - key_shift) in fp32 with the table and scored against the query (RoPE
+// at q_pos, scale in) by warp dot products, values as stored. Warp w takes
+// rows w, w + NW, ...; lane l holds channels l + 32 k, so the RoPE partners
+// c and c + D/2 are in one lane. `qs` is shared memory for kMaxGqa * D
+// floats. Leaves the warps' states in `red` like exact_states_tc.
+template <int D, int NW>
+__device__ void exact_states_prerope(const DecodeArgs& a, int b, int h, float* red, float* qs) {
+  constexpr int NS = D / 32, HS = NS / 2;
+  const unsigned full = 0xffffffffu;
+  const Geometry& G = a.geo;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = G.gqa, bh = b * G.H + h;
+  for (int idx = threadIdx.x; idx < gq * D; idx += NW * 32)
+    qs[idx] = query_value(a, b, h * gq + idx / D, idx % D, a.q_pos);
+  __syncthreads();
+  const int n_sink_items = a.n_sink_read;
+  const int n_items = n_sink_items + static_cast<int>(a.L - a.F);
+  float m_run[kMaxGqa], l_run[kMaxGqa], o[kMaxGqa][NS];
+#pragma unroll
+  for (int j = 0; j < kMaxGqa; ++j) {
+    m_run[j] = -INFINITY, l_run[j] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NS; ++k) o[j][k] = 0.0f;
+  }
+  for (int it = warp; it < n_items; it += NW) {
+    int64_t pos;
+    const uint16_t *krow, *vrow;
+    if (it < n_sink_items) {
+      pos = it;
+      krow = a.lay.sink_k + (static_cast<size_t>(bh) * G.n_sink_slots + it) * D;
+      vrow = a.lay.sink_v + (static_cast<size_t>(bh) * G.n_sink_slots + it) * D;
+    } else {
+      pos = a.F + (it - n_sink_items);
+      const size_t off = (static_cast<size_t>(bh) * G.tail_cap + (pos & (G.tail_cap - 1))) * D;
+      krow = a.lay.tail_k + off;
+      vrow = a.lay.tail_v + off;
+    }
+    const int64_t kpos = pos < G.n_sink ? pos : pos - a.key_shift;
+    const float* tr = a.tab.rope + static_cast<size_t>(kpos) * D;
+    float k[NS], v[NS];
+#pragma unroll
+    for (int kk = 0; kk < NS; ++kk) {
+      k[kk] = act_to_float(krow[kk * 32 + lane], G.act_bf16);
+      v[kk] = act_to_float(vrow[kk * 32 + lane], G.act_bf16);
+    }
+#pragma unroll
+    for (int kk = 0; kk < HS; ++kk) {  // channel i = lane + 32 kk and its partner i + D/2
+      const float2 cs = *reinterpret_cast<const float2*>(tr + 2 * (lane + 32 * kk));
+      float ra, rb;
+      rope_pair(k[kk], k[kk + HS], cs.x, cs.y, &ra, &rb);
+      k[kk] = ra, k[kk + HS] = rb;
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxGqa; ++j) {
+      if (j >= gq) break;
+      float d = 0.0f;
+#pragma unroll
+      for (int kk = 0; kk < NS; ++kk) d = fmaf(k[kk], qs[j * D + kk * 32 + lane], d);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) d += __shfl_xor_sync(full, d, off);
+      const float mn = fmaxf(m_run[j], d);
+      const float al = fast_exp2(m_run[j] - mn);  // 0 while nothing was seen
+      const float p = fast_exp2(d - mn);
+      m_run[j] = mn;
+      l_run[j] = fmaf(l_run[j], al, p);
+#pragma unroll
+      for (int kk = 0; kk < NS; ++kk) o[j][kk] = fmaf(o[j][kk], al, p * v[kk]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxGqa; ++j) {
+    if (j >= gq) break;
+    float* rj = red + (warp * kMaxGqa + j) * (D + 2);
+#pragma unroll
+    for (int kk = 0; kk < NS; ++kk) rj[kk * 32 + lane] = o[j][kk];
+    if (lane == 0) {
+      rj[D] = m_run[j];
+      rj[D + 1] = l_run[j];
+    }
+  }
+  __syncthreads();
 }
 
 // Rows per tile of the exact pools and the row capacity a stage of

@@ -180,7 +180,7 @@ constexpr float kLazyRescale = KVQ_LAZY_RESCALE;
 #define KVQ_DECODE_MIN_CTAS (8 / KVQ_DECODE_PAIRS)
 #endif
 
-template <int D, int KB, int VB, bool TQ = false>
+template <int D, int KB, int VB, bool TQ = false, bool PR = false>
 struct KiviTile {
   // chunk layout (kvq_layout.h): KIVI codes and meta, or TurboQuant K codes
   // in fragment order and V codes in token-pair rows, one f32 norm per token
@@ -194,7 +194,7 @@ struct KiviTile {
   // waits, hand-off and rescale decision are paid once per run (KIVI chunks
   // up to 6 KB); one for TurboQuant, whose tables leave less shared memory,
   // and for larger chunks
-  static constexpr int GPB = (TQ || CHUNK > 6144) ? 1 : 2;
+  static constexpr int GPB = (TQ || PR || CHUNK > 6144) ? 1 : 2;
   static constexpr int STAGE = GPB * CHUNK;
   static constexpr int PBUF = GPB * 32 * 8 + 16;         // weights (4 f16, 8 B per lane per group) + 4 rescale factors
   static constexpr int RED_FLOATS = NP * kMaxGqa * (D + 2);  // one merged state per pair
@@ -352,9 +352,12 @@ struct RunCursor {
 // product and its exact residual in two operations; the score scale is
 // applied in the softmax. Otherwise (RoPE applied here, or TurboQuant) the
 // query is an fp32 value carried as f16 value + residual with the scale in.
-template <int D, int KB, int VB, bool TQ, bool QX>
+// PR: keys stored before RoPE (KIVI with RoPE in the cache): the QK warp
+// dequantises each key, rotates it at its position and scores it in two
+// MMAs (f16 value and residual of the rotated key).
+template <int D, int KB, int VB, bool TQ, bool QX, bool PR = false>
 __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(DecodeArgs a) {
-  using T = KiviTile<D, KB, VB, TQ>;
+  using T = KiviTile<D, KB, VB, TQ, PR>;
   constexpr int NP = T::NP, NST = T::NST, CHUNK = T::CHUNK;
   constexpr int S = D / 16, MV = D / 16, NVG = D / 32;
   constexpr int KW = D * KB / 32;
@@ -483,6 +486,25 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           qsm[s * 32 + lane] = make_uint4(v[0], v[1], v[2], v[3]);
         }
         named_barrier_sync(1, NP * 32);  // the QK warps only
+      } else if constexpr (PR) {
+        // keys stored before RoPE: k-step s of lane (g, t) holds the RoPE
+        // partners c = t D/8 + 2s + p and c + D/2 (kvq_layout.h k_frag_pos);
+        // the query is rotated at q_pos, scale in, value or residual by column
+        const int jc = g >> 1;
+        const bool col_lo = g & 1;
+        for (int s = pair; s < S; s += NP) {
+          uint32_t v[4];
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            const int c0 = t * (D / 8) + 2 * s + p;
+            const float x0 = jc < gq ? query_value(a, b, h * gq + jc, c0, a.q_pos) : 0.0f;
+            const float x1 = jc < gq ? query_value(a, b, h * gq + jc, c0 + D / 2, a.q_pos) : 0.0f;
+            v[2 * p] = 0u;
+            v[2 * p + 1] = split_h2(x0, x1, col_lo);
+          }
+          qsm[s * 32 + lane] = make_uint4(v[0], v[1], v[2], v[3]);
+        }
+        named_barrier_sync(1, NP * 32);  // the QK warps only
       } else {
         const int jc = g >> 1;        // query head of this lane's B column
         const bool col_lo = g & 1;    // B column holds the residual part
@@ -530,7 +552,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
         }
       };
       // scores of one group into the lane's C fragment
-      auto qk_scores = [&](const uint8_t* tile, float (&sc)[2][4]) {
+      auto qk_scores = [&](const uint8_t* tile, float (&sc)[2][4], int64_t kpos0) {
         if constexpr (TQ) {
           // scores in the rotated domain: the lane's K fields (fragment order,
           // kvq_layout.h tq_kfield_bit) from its own words of the tile, each
@@ -562,6 +584,61 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
             sc[mt][2] = acc[mt][2] * n1;
             sc[mt][3] = acc[mt][3] * n1;
           }
+        } else if constexpr (PR) {
+          // each key dequantised (code s + z, fp32), rotated at its position
+          // kpos0 + token (the table, clamped: masked tokens may lie outside
+          // it) and split into an f16 value and residual, two MMAs per k-step
+          uint32_t kr[KW];
+          load_lane_words<KW, piece_words(KW)>(tile, lane, kr);
+          const __half* ksc = reinterpret_cast<const __half*>(tile + T::KMETA);
+          const __half* kzr = ksc + D;
+          const int i0 = t * (D / 8);
+          const int64_t pmax = a.geo.rope_max_pos - 1;
+          float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+          const float* rope_rows[2][2];  // table rows of tokens 16 mt + g (+ 8), clamped
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int rh = 0; rh < 2; ++rh) {
+              int64_t kp = kpos0 + 16 * mt + g + 8 * rh;
+              kp = kp < 0 ? 0 : (kp > pmax ? pmax : kp);
+              rope_rows[mt][rh] = a.tab.rope + static_cast<size_t>(kp) * D + 2 * i0;
+            }
+#pragma unroll
+          for (int s = 0; s < S; ++s) {
+            const uint4 q4 = qsm[s * 32 + lane];
+            float sk[2][2], zk[2][2];  // scale (unit folded in) and zero of channels i0 + 2s + pp and + D/2
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int c = i0 + 2 * s + pp + hh * (D / 2);
+                sk[pp][hh] = __half2float(ksc[c]) * CodeConsts<KB>::kCodeInv;
+                zk[pp][hh] = __half2float(kzr[c]);
+              }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              uint32_t ah[4], al[4];
+#pragma unroll
+              for (int reg = 0; reg < 4; ++reg) {
+                const int pp = reg >> 1, rh = reg & 1;
+                const float2 cs = *reinterpret_cast<const float2*>(rope_rows[mt][rh] + 2 * (2 * s + pp));
+                const float2 cf = h2_to_f2(pair_at<KB>(kc, kr, (mt * S + s) * 4 + reg));
+                float ra, rb;
+                rope_pair(fmaf(cf.x, sk[pp][0], zk[pp][0]), fmaf(cf.y, sk[pp][1], zk[pp][1]), cs.x, cs.y, &ra, &rb);
+                ah[reg] = f2_to_h2(ra, rb);
+                const float2 hf = h2_to_f2(ah[reg]);
+                al[reg] = f2_to_h2(ra - hf.x, rb - hf.y);
+              }
+              mma_f16(acc[mt], ah[0], ah[1], ah[2], ah[3], q4.y, q4.w);
+              mma_f16(acc[mt], al[0], al[1], al[2], al[3], q4.y, q4.w);
+            }
+            asm volatile("" ::: "memory");  // keep the next k-step's loads from being hoisted here
+          }
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[mt][e] = acc[mt][e];
         } else {
           uint32_t kr[KW];
           load_lane_words<KW, piece_words(KW)>(tile, lane, kr);
@@ -670,7 +747,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
         if constexpr (GPB == 2) {  // a short run scores its one group twice (the copy is discarded)
           qk_scores_pair(stages + st * STAGE, stages + st * STAGE + (cnt > 1 ? CHUNK : 0), scr);
         } else {
-          qk_scores(stages + st * STAGE, scr[0]);
+          qk_scores(stages + st * STAGE, scr[0], (a.g_begin + (f - ubase)) * kGroup - a.key_shift);
         }
         float pr[GPB][2][2];
 #pragma unroll
@@ -929,9 +1006,9 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
   }
 }
 
-template <int D, int KB, int VB, bool TQ, bool QX>
+template <int D, int KB, int VB, bool TQ, bool QX, bool PR = false>
 cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
-  using T = KiviTile<D, KB, VB, TQ>;
+  using T = KiviTile<D, KB, VB, TQ, PR>;
   const size_t smem = T::smem_bytes();
   static int occ_of[kMaxDevices] = {};  // per device: the attribute is per device
   int dev = 0;
@@ -940,10 +1017,10 @@ cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   int& occupancy = occ_of[dev];
   if (!occupancy) {
-    e = cudaFuncSetAttribute(decode_kivi_kernel<D, KB, VB, TQ, QX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kivi_kernel<D, KB, VB, TQ, QX, PR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, decode_kivi_kernel<D, KB, VB, TQ, QX>, 64 * T::NP, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, decode_kivi_kernel<D, KB, VB, TQ, QX, PR>, 64 * T::NP, smem);
     if (e != cudaSuccess) return e;
     if (occupancy < 1) occupancy = 1;
   }
@@ -956,7 +1033,7 @@ cudaError_t launch_kivi_instance(DecodeArgs& a, cudaStream_t s, int sm_count) {
   if (n < 1) n = 1;
   a.n_ctas = static_cast<int>(n);
   if (a.work <= 0) return cudaSuccess;  // nothing quantised to read: the merge does it all
-  decode_kivi_kernel<D, KB, VB, TQ, QX><<<a.n_ctas, 64 * T::NP, smem, s>>>(a);
+  decode_kivi_kernel<D, KB, VB, TQ, QX, PR><<<a.n_ctas, 64 * T::NP, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -968,8 +1045,9 @@ cudaError_t launch_kivi_k(DecodeArgs& a, cudaStream_t s, int sm_count) {
   const bool qx = a.tab.rope == nullptr;
 #define KVQ_CASE(V)                                                                                       \
   if (a.geo.vb == V)                                                                                      \
-    return qx ? launch_kivi_instance<D, K, V, false, true>(a, s, sm_count)                               \
-              : launch_kivi_instance<D, K, V, false, false>(a, s, sm_count);
+    return a.geo.k_pre_rope ? launch_kivi_instance<D, K, V, false, false, true>(a, s, sm_count)          \
+           : qx             ? launch_kivi_instance<D, K, V, false, true>(a, s, sm_count)                 \
+                            : launch_kivi_instance<D, K, V, false, false>(a, s, sm_count);
   KVQ_CASE(2) KVQ_CASE(3) KVQ_CASE(4) KVQ_CASE(8)
 #undef KVQ_CASE
   return cudaErrorInvalidValue;

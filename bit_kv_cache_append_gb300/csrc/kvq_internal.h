@@ -68,6 +68,10 @@ struct DecodeArgs {
   int n_dyn_sel;        // KVSink: selected sinks (read when pos < F)
   int64_t sink_qpos;    // RoPE position of the query against the sink rows
                         // (L - 1, or L - 1 - (E - n_sink) when re-positioning)
+  int64_t key_shift;    // keys stored before RoPE: positions >= n_sink are
+                        // rotated at p - key_shift (E - n_sink when
+                        // re-positioning, else 0), the query at q_pos
+  int64_t q_pos;
   float qscale;         // log2(e) / sqrt(D)
   // the f16x2 magic 1024.0 pair of the 8-bit code conversion, read from the
   // parameter bank so that the instruction needs no second immediate

@@ -78,13 +78,15 @@ KVQ_HD Chunk chunk_layout(int mode_tq, int D, int kb, int vb) {
   return c;
 }
 
-// (token, channel) of fragment element f of lane (g, t) for K.
-KVQ_HD void k_frag_pos(int D, int lane, int f, int* token, int* channel) {
+// (token, channel) of fragment element f of lane (g, t) for K. With keys
+// stored before RoPE (pr) the two elements of a pair are RoPE partners:
+// channel t D/8 + 2s + (r >> 1) and that + D/2, so one lane rotates them.
+KVQ_HD void k_frag_pos(int D, int lane, int f, int* token, int* channel, bool pr = false) {
   const int g = lane >> 2, t = lane & 3, S = D / 16;
   const int e = f & 1, r = (f >> 1) & 3, ms = f >> 3;  // ms = mt * S + s
   const int mt = ms / S, s = ms % S;
   *token = 16 * mt + g + 8 * (r & 1);
-  *channel = t * (D / 4) + 4 * s + 2 * (r >> 1) + e;
+  *channel = pr ? t * (D / 8) + 2 * s + (r >> 1) + e * (D / 2) : t * (D / 4) + 4 * s + 2 * (r >> 1) + e;
 }
 
 // (token, channel) of fragment element f of lane (g, t) for V.
@@ -106,7 +108,8 @@ KVQ_HD constexpr int piece_words(int words) { return words % 4 == 0 ? 4 : 2; }
 // lane blocks are interleaved in pieces of pw words.
 KVQ_HD int code_word_offset(int lane, int w, int pw = 4) { return ((w / pw) * 32 + lane) * (4 * pw) + (w % pw) * 4; }
 
-// f16 position of channel c inside the K scale array.
+// f16 position of channel c inside the K scale array (keys stored before
+// RoPE: the natural order, callers pass c itself).
 KVQ_HD int kmeta_pos(int D, int c) {
   const int q = D / 4, t = c / q, r = c % q;
   return ((r >> 3) * 4 + t) * 8 + (r & 7);
@@ -204,6 +207,7 @@ struct Geometry {
   int n_sink, window, evict_window, n_dyn;
   int rope_repos;     // StreamingLLM position re-encoding at read
   int v_q4_0;         // V in the symmetric q4_0 form (scale d, zero -8 d)
+  int k_pre_rope;     // keys stored before RoPE, rotated when read
   int act_bf16;
   int64_t max_tokens;
   int n_slots;        // group chunks per (layer, b, h)

@@ -115,6 +115,15 @@ typedef struct {
                          a rounding boundary can differ by one step and the
                          blocks are not interchangeable with such data.
                          0: the KIVI min/max affine form                    */
+  int k_pre_rope;     /* 1 (KIVI, rope_base > 0, n_dyn_sinks = 0): keys are
+                         stored (quantised, and in the exact pools) before
+                         RoPE and rotated when read, at their absolute
+                         position or, with rope_reposition, at their slot in
+                         the cache (the query at its own slot) ([P1] "RoPE
+                         caveat": the "true" re-positioning; "Caveats": the
+                         per-channel K groups then see a basis that does not
+                         turn with the position). 0: keys rotated before
+                         they are stored                                    */
 } kv_cache_config;
 
 typedef struct kv_cache kv_cache; /* opaque host-side handle */

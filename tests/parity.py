@@ -47,7 +47,7 @@ def oracle_config(kw):
                        evict_window=kw["evict_window"], n_dyn_sinks=kw["n_dyn_sinks"],
                        act_dtype=kw["act_dtype"], seed=kw["seed"], rope_base=kw["rope_base"],
                        rope_reposition=bool(kw.get("rope_reposition", False)),
-                       v_q4_0=bool(kw.get("v_q4_0", False)))
+                       v_q4_0=bool(kw.get("v_q4_0", False)), k_pre_rope=bool(kw.get("k_pre_rope", False)))
 
 
 def compare_exports(gpu_cache, oc, layer: int) -> None:

@@ -26,15 +26,18 @@ def _decode_both(gc, oc, layer, q, act, heads=None):
 
 # ------------------------------------------------------------------ ring
 
+@pytest.mark.parametrize("pre_rope", [False, True])
 @pytest.mark.parametrize("reposition", [False, True])
 @pytest.mark.parametrize("name", ["ring_int8", "ring_int4"])
-def test_ring_stream_with_rope_and_eviction(name, reposition):
+def test_ring_stream_with_rope_and_eviction(name, reposition, pre_rope):
     """Shortened StreamingLLM stream: 2 layers, per step append 1 -> evict ->
     decode; identical eviction ranges, codes and attention, with keys read
-    at their absolute positions or re-positioned at their cache slots."""
+    at their absolute positions or re-positioned at their cache slots, and
+    keys rotated before they are stored or stored before RoPE and rotated
+    when read."""
     w = W.scaled(W.WORKLOADS[name], batch=4, n_kv_heads=4, n_q_heads=4, evict_window=96, n_layers=2)
     steps = 400
-    kw = cache_kwargs(w, 96 + 64, rope_max_pos=steps, rope_reposition=reposition)
+    kw = cache_kwargs(w, 96 + 64, rope_max_pos=steps, rope_reposition=reposition, k_pre_rope=pre_rope)
     gc, oc = _pair(kw)
     ranges_g, ranges_o = [], []
     for t in range(steps):
@@ -266,3 +269,31 @@ def test_kvsink_group_of_only_sinks():
     compare_exports(gc, oc, 0)
     _decode_both(gc, oc, 0, W.queries(w, 3), "f16")
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("kb,vb,act", [(2, 4, "bf16"), (4, 4, "f16"), (3, 8, "bf16")])
+@pytest.mark.parametrize("D", [128, 64])
+def test_pre_rope_prefill_then_appends(kb, vb, act, D):
+    """Keys stored before RoPE (posttrainllm "RoPE caveat"): prefill 1000
+    tokens, then appends of mixed sizes, with a sink overlay and a window;
+    codes, scales and zeros (the stored, un-rotated keys) bit-exact and
+    attention, with every key rotated on read, within tolerance."""
+    w = W.scaled(W.WORKLOADS["llama8b"], batch=2, n_kv_heads=2, n_q_heads=8, head_dim=D, context=2048,
+                 k_bits=kb, v_bits=vb, act_dtype=act, n_sink=4, window=40, rope_base=10000.0)
+    kw = cache_kwargs(w, 2048, rope_max_pos=2048, k_pre_rope=True)
+    gc, oc = _pair(kw)
+    k, v = W.kv_tokens(w, 12, 1000)
+    gc.prefill_quantize(0, torch_act(k, act), torch_act(v, act))
+    oc.prefill_quantize(0, k, v)
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 12, 0), act)
+    pos = 1000
+    for i, n in enumerate([1, 3, 31, 1, 32, 7, 64, 1]):
+        k, v = W.kv_tokens(w, 12, n, first_pos=pos)
+        gc.append(0, torch_act(k, act), torch_act(v, act))
+        oc.append(0, k, v)
+        pos += n
+        if i % 3 == 2:
+            _decode_both(gc, oc, 0, W.queries(w, 12, pos), act)
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 12, 99), act)
