@@ -1,6 +1,6 @@
-// Append-side kernels: exact tail ring and sink buffer writes, KIVI group
-// quantisation (with KVSink calibration exclusion), TurboQuant per-token
-// quantisation, and the KVSink sink-row gather.
+// Append-side kernels: exact tail ring and sink buffer writes, TurboQuant
+// per-token quantisation and the KVSink sink-row gather; the launch of the
+// KIVI group quantisation (flush.cuh).
 #include <algorithm>
 
 #include "kvq_device.cuh"
@@ -43,327 +43,6 @@ __global__ void tail_write_kernel(AppendArgs a, int row_begin, int n_rows) {
     *reinterpret_cast<uint4*>(a.lay.sink_v + t + c0) = vlo;
     *reinterpret_cast<uint4*>(a.lay.sink_v + t + half + c0) = vhi;
   }
-}
-
-// ---------------------------------------------------------------- KIVI flush
-// One CTA per (completed group, b, h); D threads. Quantisation follows
-// posttrainllm "StreamingLLM + KIVI", "Affine quantisation formula", in the
-// unsigned-code form: scale = max((max - min) / (2^b - 1), 1e-5) in fp32,
-// scale and zero (= min) stored as fp16, code = rint((x - zero) / scale)
-// clamped to [0, 2^b - 1], computed from the stored fp16 values promoted to
-// fp32. K: one (scale, zero) per channel over the group's 32 tokens; V: one
-// per token per 32-channel group (the KIVI group idea, same page, "Caveats").
-// KVSink (VeloxQuant-MLX "KVSink-Adapted Sink Protection", "How it works" 3):
-// before calibration every sink row of the group is replaced by its nearest
-// non-sink row (ties to the earlier row); sink rows keep the substitute's
-// codes and the group's mask bit tells attention to skip them.
-__device__ __forceinline__ void quantize_slice_params(float mn, float mx, int bits, __half* sh,
-                                                      __half* zh, float* s, float* z) {
-  const float lb = static_cast<float>((1 << bits) - 1);
-  const float s32 = fmaxf(__fdiv_rn(__fsub_rn(mx, mn), lb), 1e-5f);
-  *sh = __float2half_rn(s32);
-  *zh = __float2half_rn(mn);
-  *s = __half2float(*sh);
-  *z = __half2float(*zh);
-}
-
-// Code of x for a slice with stored scale s, zero z and reciprocal rs =
-// 1/s (correctly rounded): rint of the correctly rounded quotient (x - z) / s
-// (x - z rounded on its own), clamped to [0, LB]. The quotient is formed as
-// (x - z) * rs, whose distance to the correctly rounded quotient is at most
-// about 2^-22 of its magnitude (two roundings of 2^-24 each, plus the
-// quotient's own): below 6.2e-5 while |q| <= 257. Away from a half-integer by
-// more than 1e-4 the two round to the same integer, and beyond 257 the clamp
-// decides; within 1e-4 of a half-integer the correctly rounded division is
-// taken, so the code equals rint(fl((x - z) / s)) in every case.
-// The correctly rounded quotient's integer, out of line: it runs only for
-// quotients within 1e-4 of a half-integer, and inlined it would multiply the
-// size of every quantisation loop.
-__device__ __noinline__ float rint_of_quotient(float d, float s) { return rintf(__fdiv_rn(d, s)); }
-
-template <int LB>
-__device__ __forceinline__ uint32_t quantize_code(float x, float s, float z, float rs) {
-  const float d = __fsub_rn(x, z);
-  const float q = __fmul_rn(d, rs);
-  float qr = rintf(q);
-  if (fabsf(__fsub_rn(q, qr)) > 0.4999f) qr = rint_of_quotient(d, s);  // within 1e-4 of a half-integer
-  qr = fminf(fmaxf(qr, 0.0f), static_cast<float>(LB));
-  return static_cast<uint32_t>(qr);
-}
-
-// Bit position of the element i (0 .. 32/BITS - 1) of a packed word (the
-// frag_bits layout: pair j = i / 2, element e = i % 2).
-template <int BITS>
-__device__ __forceinline__ int word_bit(int i) {
-  const int j = i >> 1, e = i & 1;
-  if (BITS == 2) return 8 * (j & 3) + 2 * (j >> 2) + 4 * e;
-  if (BITS == 4) return 16 * (j & 1) + 4 * (j >> 1) + 8 * e;
-  return 8 * j + 16 * e;
-}
-
-// Byte offset, from the lane's base (K: cs[g][t D / 4], V: cs[2t][g]), of
-// the code of fragment element f of lane (g, t) (kvq_layout.h k_frag_pos,
-// v_frag_pos): a constant, so that packing loads each code with one
-// shared-memory byte load (rows are D + 4 bytes: the lanes' loads fall in
-// distinct banks or share a word).
-template <int D, bool IS_K, bool PR>
-__device__ __forceinline__ constexpr int frag_code_offset(int f) {
-  const int e = f & 1, r = (f >> 1) & 3, hi = f >> 3;
-  if (IS_K) {
-    const int mt = hi / (D / 16), s = hi % (D / 16);
-    if (PR) return (16 * mt + 8 * (r & 1)) * (D + 4) + 2 * s + (r >> 1) + e * (D / 2);
-    return (16 * mt + 8 * (r & 1)) * (D + 4) + 4 * s + 2 * (r >> 1) + e;
-  }
-  const int m = hi >> 1, kb = hi & 1;
-  return (16 * kb + e + 8 * (r >> 1)) * (D + 4) + 16 * m + 8 * (r & 1);
-}
-
-// Words [W0, W0 + NW) of every lane's K (IS_K) or V fragment block, packed
-// by this warp's thread `lane` for fragment lane `lane`; 3-bit codes in
-// blocks of three words (W0, NW multiples of 3). PR: the K channel order of
-// keys stored before RoPE (kvq_layout.h k_frag_pos).
-template <int D, int BITS, bool IS_K, bool PR, int W0, int NW>
-__device__ __forceinline__ void pack_words(const uint8_t (*cs)[D + 4], uint8_t* region, int lane) {
-  constexpr int WPL = D * BITS / 32, PW = piece_words(WPL);
-  const int g = lane >> 2, t = lane & 3;
-  const uint8_t* base = IS_K ? &cs[g][t * (PR ? D / 8 : D / 4)] : &cs[2 * t][g];
-  if constexpr (BITS == 3) {
-#pragma unroll
-    for (int blk = W0 / 3; blk < (W0 + NW) / 3; ++blk) {
-      uint32_t w[3] = {0u, 0u, 0u};
-#pragma unroll
-      for (int i = 0; i < 32; ++i) frag3_put(w, i, base[frag_code_offset<D, IS_K, PR>(32 * blk + i)]);
-#pragma unroll
-      for (int q = 0; q < 3; ++q)
-        *reinterpret_cast<uint32_t*>(region + code_word_offset(lane, 3 * blk + q, PW)) = w[q];
-    }
-  } else {
-    constexpr int PER = 32 / BITS;
-#pragma unroll
-    for (int w = W0; w < W0 + NW; ++w) {
-      uint32_t word = 0;
-#pragma unroll
-      for (int i = 0; i < PER; ++i)
-        word |= static_cast<uint32_t>(base[frag_code_offset<D, IS_K, PR>(w * PER + i)]) << word_bit<BITS>(i);
-      *reinterpret_cast<uint32_t*>(region + code_word_offset(lane, w, PW)) = word;
-    }
-  }
-}
-
-// The codes of one group (cs[token][channel]) in the decode kernel's
-// fragment order: the D / 32 warps of the CTA take equal shares of the
-// words of every lane's block.
-template <int D, int BITS, bool IS_K, bool PR = false>
-__device__ __forceinline__ void pack_fragments(const uint8_t (*cs)[D + 4], uint8_t* region, int tid) {
-  constexpr int NWARP = D / 32, NW = D * BITS / 32 / NWARP;
-  static_assert(NW * NWARP == D * BITS / 32 && (BITS != 3 || NW % 3 == 0), "equal shares");
-  const int warp = tid >> 5, lane = tid & 31;
-  if (warp == 0) pack_words<D, BITS, IS_K, PR, 0, NW>(cs, region, lane);
-  else if (warp == 1) pack_words<D, BITS, IS_K, PR, NW, NW>(cs, region, lane);
-  if constexpr (NWARP > 2) {
-    if (warp == 2) pack_words<D, BITS, IS_K, PR, 2 * NW, NW>(cs, region, lane);
-    else if (warp == 3) pack_words<D, BITS, IS_K, PR, 3 * NW, NW>(cs, region, lane);
-  }
-}
-
-// KB, VB: code widths (levels 2^bits - 1), packed tight (3-bit codes in
-// blocks of three words, kvq_layout.h frag3_put).
-template <int D, int KB, int VB>
-__global__ void __launch_bounds__(D) kivi_flush_kernel(AppendArgs a) {
-  constexpr int HALF = D / 2, NV = D / 32, CPR = HALF / 8;
-  constexpr int LK = (1 << KB) - 1, LV = (1 << VB) - 1;
-  constexpr int SK = KB, SV = VB;
-  // the group's rows as activation-dtype bits (rows padded by 16 bytes so
-  // that 16-byte row stores stay aligned and column reads spread over banks)
-  __shared__ __align__(16) uint16_t xk[32][D + 8];
-  __shared__ __align__(16) uint16_t xv[32][D + 8];
-  __shared__ __align__(16) uint8_t ck[32][D + 4];  // rows padded by a word: the packing gathers down columns
-  __shared__ __align__(16) uint8_t cv[32][D + 4];
-  __shared__ int sub[32];
-  __shared__ uint32_t smask;
-  const Geometry& G = a.geo;
-  const int tid = threadIdx.x;
-  const int bh = blockIdx.y, b = bh / G.H, h = bh % G.H;
-  const int64_t g = a.g_first + blockIdx.x;
-  const int64_t p0 = g * kGroup;
-  const int slot = static_cast<int>(g % G.n_slots);
-  const int bf16 = G.act_bf16;
-
-  if (tid < 32) {  // KVSink: the nearest non-sink row of each row (ties to the earlier)
-    uint32_t m = 0;
-    if (a.dyn_active) {
-      for (int j = 0; j < a.n_dyn_sel; ++j) {
-        const int64_t p = a.lay.sink_pos[b * kMaxSinks + j];
-        if (p >= p0 && p < p0 + kGroup) m |= 1u << (p - p0);
-      }
-    }
-    const int r = tid;
-    int sr = r;
-    if (((m >> r) & 1u) && m != 0xFFFFFFFFu) {
-      for (int d = 1; d < 32; ++d) {
-        if (r - d >= 0 && !((m >> (r - d)) & 1u)) { sr = r - d; break; }
-        if (r + d < 32 && !((m >> (r + d)) & 1u)) { sr = r + d; break; }
-      }
-    }
-    sub[r] = sr;
-    if (r == 0) smask = m;
-  }
-  __syncthreads();
-
-#pragma unroll
-  for (int idx = tid; idx < 32 * CPR; idx += D) {
-    const int r = idx / CPR, c0 = (idx % CPR) * 8;
-    const int64_t pos = p0 + sub[r];
-    uint4 klo, khi, vlo, vhi;
-    if (pos < a.L0) {
-      const size_t t = (static_cast<size_t>(bh) * G.tail_cap + (pos & (G.tail_cap - 1))) * D;
-      klo = *reinterpret_cast<const uint4*>(a.lay.tail_k + t + c0);
-      khi = *reinterpret_cast<const uint4*>(a.lay.tail_k + t + HALF + c0);
-      vlo = *reinterpret_cast<const uint4*>(a.lay.tail_v + t + c0);
-      vhi = *reinterpret_cast<const uint4*>(a.lay.tail_v + t + HALF + c0);
-    } else {
-      const size_t t = (static_cast<size_t>(bh) * a.n + (pos - a.L0)) * D;
-      klo = *reinterpret_cast<const uint4*>(a.k + t + c0);
-      khi = *reinterpret_cast<const uint4*>(a.k + t + HALF + c0);
-      vlo = *reinterpret_cast<const uint4*>(a.v + t + c0);
-      vhi = *reinterpret_cast<const uint4*>(a.v + t + HALF + c0);
-      if (a.tab.rope) rotate8(klo, khi, a.tab.rope + static_cast<size_t>(pos) * D, c0, bf16);
-    }
-    *reinterpret_cast<uint4*>(&xk[r][c0]) = klo;
-    *reinterpret_cast<uint4*>(&xk[r][HALF + c0]) = khi;
-    *reinterpret_cast<uint4*>(&xv[r][c0]) = vlo;
-    *reinterpret_cast<uint4*>(&xv[r][HALF + c0]) = vhi;
-  }
-  __syncthreads();
-
-  uint8_t* chunk = a.lay.chunks + (static_cast<size_t>(bh) * G.n_slots + slot) * G.chunk.bytes;
-  // the first half of the threads quantise K (two channels each, over the
-  // 32 tokens), the second half V (two (token, 32-channel group) slices
-  // each); every value is read from shared memory once (32-bit and 16-byte
-  // loads) and kept in registers between min/max and the codes
-  if (tid < D / 2) {  // K: channels 2 tid, 2 tid + 1
-    const int c = 2 * tid;
-    auto kpair = [&](int r) {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(&xk[r][c]);
-      return make_float2(act_to_float(static_cast<uint16_t>(w & 0xffffu), bf16),
-                         act_to_float(static_cast<uint16_t>(w >> 16), bf16));
-    };
-    float2 x = kpair(0);
-    float mn0 = x.x, mx0 = x.x, mn1 = x.y, mx1 = x.y;
-#pragma unroll 4
-    for (int r = 1; r < 32; ++r) {
-      x = kpair(r);
-      mn0 = fminf(mn0, x.x), mx0 = fmaxf(mx0, x.x);
-      mn1 = fminf(mn1, x.y), mx1 = fmaxf(mx1, x.y);
-    }
-    __half sh0, zh0, sh1, zh1;
-    float s0, z0, s1, z1;
-    quantize_slice_params(mn0, mx0, KB, &sh0, &zh0, &s0, &z0);
-    quantize_slice_params(mn1, mx1, KB, &sh1, &zh1, &s1, &z1);
-    const float rs0 = __frcp_rn(s0), rs1 = __frcp_rn(s1);
-#pragma unroll 4
-    for (int r = 0; r < 32; ++r) {
-      x = kpair(r);
-      const uint32_t q0 = quantize_code<LK>(x.x, s0, z0, rs0), q1 = quantize_code<LK>(x.y, s1, z1, rs1);
-      *reinterpret_cast<uint16_t*>(&ck[r][c]) = static_cast<uint16_t>(q0 | (q1 << 8));
-    }
-    // K scales and zeros in the decode's B-operand orders (keys stored
-    // before RoPE: the natural channel order)
-    __half* km = reinterpret_cast<__half*>(chunk + G.chunk.kmeta_off);
-    const bool pr = G.k_pre_rope;
-    km[pr ? c : kmeta_pos(D, c)] = sh0;
-    km[D + (pr ? c : kzero_pos(D, c))] = zh0;
-    km[pr ? c + 1 : kmeta_pos(D, c + 1)] = sh1;
-    km[D + (pr ? c + 1 : kzero_pos(D, c + 1))] = zh1;
-  } else {  // V: two (token r, channel group vg) slices
-#pragma unroll 1
-    for (int k = 0; k < 2; ++k) {
-      const int si = tid - D / 2 + k * (D / 2);
-      const int r = si % 32, vg = si / 32, base = 32 * vg;  // a warp's lanes take 32 rows: no bank conflicts
-      const uint4* row = reinterpret_cast<const uint4*>(&xv[r][base]);  // 4 x 8 values
-      auto unpack8 = [&](const uint4& u, float (&o)[8]) {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          o[2 * i] = act_to_float(static_cast<uint16_t>(w[i] & 0xffffu), bf16);
-          o[2 * i + 1] = act_to_float(static_cast<uint16_t>(w[i] >> 16), bf16);
-        }
-      };
-      __half sh, zh;
-      float o[8];
-      if (VB == 4 && G.v_q4_0) {
-        // the symmetric q4_0 form ([P3] "Summary"): d = m / -8 with m the value
-        // of largest magnitude (the first in channel order on ties), code
-        // min(15, floor(x / d + 8.5)) from the stored d, zero -8 d
-        float m = 0.0f, am = -1.0f;
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-          unpack8(row[q], o);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (fabsf(o[i]) > am) am = fabsf(o[i]), m = o[i];
-        }
-        sh = __float2half_rn(__fdiv_rn(m, -8.0f));
-        const float d = __half2float(sh);
-        zh = __float2half_rn(__fmul_rn(d, -8.0f));  // exact: a power-of-two multiple
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-          unpack8(row[q], o);
-          uint32_t cw[2] = {0u, 0u};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float qv = 8.0f;
-            if (d != 0.0f) qv = fminf(fmaxf(floorf(__fadd_rn(__fdiv_rn(o[i], d), 8.5f)), 0.0f), 15.0f);
-            cw[i >> 2] |= static_cast<uint32_t>(qv) << (8 * (i & 3));
-          }
-          reinterpret_cast<uint32_t*>(&cv[r][base + 8 * q])[0] = cw[0];  // rows of D + 4 bytes: 4-byte aligned
-          reinterpret_cast<uint32_t*>(&cv[r][base + 8 * q])[1] = cw[1];
-        }
-      } else {
-        float mn = INFINITY, mx = -INFINITY;
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-          unpack8(row[q], o);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mn = fminf(mn, o[i]), mx = fmaxf(mx, o[i]);
-        }
-        float sv, zv;
-        quantize_slice_params(mn, mx, VB, &sh, &zh, &sv, &zv);
-        const float rs = __frcp_rn(sv);
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-          unpack8(row[q], o);
-          uint32_t cw[2] = {0u, 0u};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) cw[i >> 2] |= quantize_code<LV>(o[i], sv, zv, rs) << (8 * (i & 3));
-          reinterpret_cast<uint32_t*>(&cv[r][base + 8 * q])[0] = cw[0];  // rows of D + 4 bytes: 4-byte aligned
-          reinterpret_cast<uint32_t*>(&cv[r][base + 8 * q])[1] = cw[1];
-        }
-      }
-      __half* vm = reinterpret_cast<__half*>(chunk + G.chunk.vmeta_off);
-      vm[vscale_pos(NV, r, vg)] = sh;
-      vm[vzero_pos(NV, r, vg)] = zh;
-    }
-  }
-  __syncthreads();
-
-  // pack in the decode kernel's fragment order (kvq_layout.h)
-  if (G.k_pre_rope) pack_fragments<D, SK, true, true>(ck, chunk + G.chunk.kc_off, tid);
-  else pack_fragments<D, SK, true>(ck, chunk + G.chunk.kc_off, tid);
-  pack_fragments<D, SV, false>(cv, chunk + G.chunk.vc_off, tid);
-  if (G.n_dyn && h == 0 && tid == 0) a.lay.sink_mask[b * G.n_slots + slot] = smask;
-}
-
-template <int D>
-void launch_flush(const AppendArgs& a, dim3 grid, cudaStream_t s) {
-  const int kb = a.geo.kb, vb = a.geo.vb;
-#define KVQ_FLUSH(K, V) \
-  if (kb == K && vb == V) { kivi_flush_kernel<D, K, V><<<grid, D, 0, s>>>(a); return; }
-  KVQ_FLUSH(2, 2) KVQ_FLUSH(2, 3) KVQ_FLUSH(2, 4) KVQ_FLUSH(2, 8)
-  KVQ_FLUSH(3, 2) KVQ_FLUSH(3, 3) KVQ_FLUSH(3, 4) KVQ_FLUSH(3, 8)
-  KVQ_FLUSH(4, 2) KVQ_FLUSH(4, 3) KVQ_FLUSH(4, 4) KVQ_FLUSH(4, 8)
-  KVQ_FLUSH(8, 2) KVQ_FLUSH(8, 3) KVQ_FLUSH(8, 4) KVQ_FLUSH(8, 8)
-#undef KVQ_FLUSH
 }
 
 // ---------------------------------------------------------------- TurboQuant
@@ -565,8 +244,8 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int64_t* launches
   const int BH = G.B * G.H;
   if (!G.mode_tq && a.n_groups > 0) {
     dim3 grid(a.n_groups, BH);
-    if (G.D == 128) launch_flush<128>(a, grid, s);
-    else launch_flush<64>(a, grid, s);
+    if (G.D == 128) (G.kb <= 3 ? launch_flush_d128_k23 : launch_flush_d128_k48)(a, grid, s);
+    else (G.kb <= 3 ? launch_flush_d64_k23 : launch_flush_d64_k48)(a, grid, s);
     ++*launches;
   }
   if (G.mode_tq && a.n > 0) {  // token pairs (2 pi, 2 pi + 1) that meet [L0, L0 + n)

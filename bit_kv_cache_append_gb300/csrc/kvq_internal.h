@@ -98,6 +98,12 @@ struct SinkSelectArgs {
 };
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int64_t* launches);
+// KIVI group quantisation of a.n_groups completed groups (flush_d*_k*.cu:
+// head_dim 128 or 64, K codes of 2 or 3 bits, or of 4 or 8 bits).
+void launch_flush_d128_k23(const AppendArgs& a, dim3 grid, cudaStream_t s);
+void launch_flush_d128_k48(const AppendArgs& a, dim3 grid, cudaStream_t s);
+void launch_flush_d64_k23(const AppendArgs& a, dim3 grid, cudaStream_t s);
+void launch_flush_d64_k48(const AppendArgs& a, dim3 grid, cudaStream_t s);
 cudaError_t launch_sink_select(const SinkSelectArgs& a, cudaStream_t s, int64_t* launches);
 // KVSink calls of at most this many tokens take the single-launch path
 // (norms, set update and new sink rows in one kernel per sequence).

@@ -208,3 +208,37 @@ def test_v_q4_0_prefill_then_appends(kb, act, D, H, Hq):
         pos += n
     compare_exports(gc, oc, 0)
     _decode_both(gc, oc, 0, W.queries(w, 8, 1), act)
+
+
+@pytest.mark.parametrize("kb,vb", [(2, 2), (3, 3), (4, 4), (8, 8)])
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+def test_quotients_on_half_integers(kb, vb, act):
+    """Values on the half-integer grid of their slice (j / 2 for j = 0 ..
+    2 LB, scale 1 where the slice spans 0 .. LB), so that many quotients are
+    exact half-integers and round half to even, plus values one step of the
+    activation dtype on either side of a half-integer: codes bit-exact (no
+    RoPE, sinks or window, so every value is quantised as given)."""
+    w = W.scaled(W.WORKLOADS["tiny"], batch=2, n_kv_heads=2, n_q_heads=4, head_dim=128, n_sink=0, window=0,
+                 k_bits=kb, v_bits=vb, act_dtype=act)
+    kw = cache_kwargs(w, 256, rope_base=0.0)
+    gc, oc = _pair(kw)
+    lb = (1 << kb) - 1
+    B, H, T, D = 2, 2, 96, 128
+    t = np.arange(T)[:, None]
+    c = np.arange(D)[None, :]
+    k = ((t * 7 + c * 3) % (2 * lb + 1)).astype(np.float32) * 0.5
+    k[0, :], k[1, :] = 0.0, float(lb)                     # every channel of group 0 spans 0 .. LB
+    k[32, :], k[33, :] = 0.0, float(lb)
+    k[64, :], k[65, :] = 0.0, float(lb)
+    lv = (1 << vb) - 1
+    v = ((t * 5 + c) % (2 * lv + 1)).astype(np.float32) * 0.5
+    v[:, 0::32], v[:, 1::32] = 0.0, float(lv)             # every 32-channel slice spans 0 .. LB
+    # one activation step either side of a half-integer on some rows
+    step = np.float32(2.0 ** -7 if act == "bf16" else 2.0 ** -10)
+    k[10::7, 5::11] += step * np.maximum(k[10::7, 5::11], 1.0)
+    v[12::9, 7::13] -= step * np.maximum(v[12::9, 7::13], 1.0)
+    k = W.round_to_act(np.broadcast_to(k, (B, H, T, D)).copy(), act)
+    v = W.round_to_act(np.broadcast_to(v, (B, H, T, D)).copy(), act)
+    gc.prefill_quantize(0, torch_act(k, act), torch_act(v, act))
+    oc.prefill_quantize(0, k, v)
+    compare_exports(gc, oc, 0)
