@@ -105,9 +105,26 @@ __device__ __forceinline__ uint32_t act_max2(uint32_t a, uint32_t b) {
   }
   return r;
 }
+// Two floats rounded to the activation dtype (nearest even), packed low |
+// high << 16 (one conversion instruction for both).
 template <bool BF16>
 __device__ __forceinline__ uint32_t act_pack(float lo, float hi) {
-  return static_cast<uint32_t>(float_to_act(lo, BF16)) | (static_cast<uint32_t>(float_to_act(hi, BF16)) << 16);
+  uint32_t r;
+  if constexpr (BF16) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    r = *reinterpret_cast<const uint32_t*>(&v);
+  } else {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    r = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return r;
+}
+
+// RN(n / s) from r = RN(1 / s) (Markstein's correction step).
+__device__ __forceinline__ float quotient(float n, float s, float r) {
+  const float q0 = __fmul_rn(n, r);
+  const float e = __fmaf_rn(-q0, s, n);
+  return __fmaf_rn(e, r, q0);
 }
 
 // Stored scale and zero of one slice from its min and max: sh, zh the fp16
@@ -117,7 +134,8 @@ __device__ __forceinline__ uint32_t act_pack(float lo, float hi) {
 template <int LB>
 __device__ __forceinline__ void slice_params(float mn, float mx, __half* sh, __half* zh, uint32_t* zs,
                                              float* r, bool* ok) {
-  const float s32 = fmaxf(__fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(LB)), 1e-5f);
+  constexpr float lb = static_cast<float>(LB), inv_lb = 1.0f / lb;  // RN(1 / LB), folded by the compiler
+  const float s32 = fmaxf(quotient(__fsub_rn(mx, mn), lb, inv_lb), 1e-5f);
   *sh = __float2half_rn(s32);
   *zh = __float2half_rn(mn);
   const float s = __half2float(*sh), z = __half2float(*zh);
@@ -147,19 +165,35 @@ __device__ __forceinline__ Slice make_slice(uint32_t zs, float r) {
   return q;
 }
 
-// RN(n / s) from r = RN(1 / s) (Markstein's correction step).
-__device__ __forceinline__ float quotient(float n, float s, float r) {
-  const float q0 = __fmul_rn(n, r);
-  const float e = __fmaf_rn(-q0, s, n);
-  return __fmaf_rn(e, r, q0);
+// Two slices' constants side by side for the packed FP32x2 instructions:
+// -zero, -scale and RN(1 / scale).
+struct Slice2 {
+  float2 nz, ns, r;
+};
+__device__ __forceinline__ Slice2 pair_slices(const Slice& a, const Slice& b) {
+  Slice2 q;
+  q.nz = make_float2(-a.z, -b.z);
+  q.ns = make_float2(-a.s, -b.s);
+  q.r = make_float2(a.r, b.r);
+  return q;
 }
 
-// Accumulates (kMagicBits + code) << bit of x into acc and the kMagicBits
-// part into corr (a constant after unrolling).
-__device__ __forceinline__ void add_code(float x, const Slice& q, int bit, uint32_t& acc, uint32_t& corr) {
-  const float t = __fadd_rn(quotient(__fsub_rn(x, q.z), q.s, q.r), kMagic);
-  acc += __float_as_uint(t) << bit;
-  corr += kMagicBits << bit;
+// The codes of two values of two slices, each accumulated as (kMagicBits +
+// code) << bit into its word (corr collects the kMagicBits parts, constants
+// after unrolling): d = RN(x - z), q0 = RN(d r), e = RN(d - q0 s), RN(q0 + e r)
+// = RN(d / s), then + 1.5 * 2^23 rounds half to even; two values per
+// instruction with Blackwell's FP32x2 add, multiply and FMA (each lane
+// rounded as the scalar instruction would).
+__device__ __forceinline__ void add_code2(float2 x, const Slice2& q, int bit0, int bit1, uint32_t& acc0,
+                                          uint32_t& corr0, uint32_t& acc1, uint32_t& corr1) {
+  const float2 d = __fadd2_rn(x, q.nz);
+  const float2 q0 = __fmul2_rn(d, q.r);
+  const float2 e = __ffma2_rn(q0, q.ns, d);
+  const float2 t = __fadd2_rn(__ffma2_rn(e, q.r, q0), make_float2(kMagic, kMagic));
+  acc0 += __float_as_uint(t.x) << bit0;
+  corr0 += kMagicBits << bit0;
+  acc1 += __float_as_uint(t.y) << bit1;
+  corr1 += kMagicBits << bit1;
 }
 
 // q4_0: min(15, floor(RN(RN(x / d) + 8.5))) clamped at 0, d the stored scale
@@ -256,9 +290,11 @@ __device__ __noinline__ uint4 k_exact_g(const uint16_t* row0, const uint16_t* ro
   return make_uint4(acc[0], acc[1], acc[2], acc[3]);
 }
 
+// lin: the group's first K row when its 32 rows are consecutive rows of the
+// appended input (no sink substitution, nothing from the tail), else null.
 template <int D, int KB, bool BF16, bool PR>
 __device__ __forceinline__ void flush_k(const AppendArgs& a, const int* sub, int64_t p0, int bh, uint8_t* chunk,
-                                        uint32_t* zsk, uint4 (*scratch)[D]) {
+                                        uint32_t* zsk, uint4 (*scratch)[D], const uint16_t* lin) {
   using M = KMap<KB, PR>;
   constexpr int LB = (1 << KB) - 1, HALF = D / 2, S = D / 16;
   constexpr int PW = piece_words(D * KB / 32);
@@ -269,17 +305,22 @@ __device__ __forceinline__ void flush_k(const AppendArgs& a, const int* sub, int
   // every load is issued before the first use: the rows, then (RoPE at
   // append) the table rows of the appended tokens
   uint32_t x[8][4];
+  auto row_idx = [&](int i) { return 16 * mt + gb + (i >> 1) + 8 * (i & 1); };
   auto pos_of = [&](int i) {
-    const int r = 16 * mt + gb + (i >> 1) + 8 * (i & 1);
+    const int r = row_idx(i);
     return p0 + (sub ? sub[r] : r);
   };
+  auto load_rows = [&](auto row_of) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint16_t* row = group_row(a, a.lay.tail_k, a.k, bh, pos_of(i));
-    const uint2 lo = __ldg(reinterpret_cast<const uint2*>(row + 4 * cq));
-    const uint2 hi = __ldg(reinterpret_cast<const uint2*>(row + HALF + 4 * cq));
-    x[i][0] = lo.x, x[i][1] = lo.y, x[i][2] = hi.x, x[i][3] = hi.y;
-  }
+    for (int i = 0; i < 8; ++i) {
+      const uint16_t* row = row_of(i);
+      const uint2 lo = __ldg(reinterpret_cast<const uint2*>(row + 4 * cq));
+      const uint2 hi = __ldg(reinterpret_cast<const uint2*>(row + HALF + 4 * cq));
+      x[i][0] = lo.x, x[i][1] = lo.y, x[i][2] = hi.x, x[i][3] = hi.y;
+    }
+  };
+  if (lin) load_rows([&](int i) { return lin + row_idx(i) * D; });  // the group's rows, in order, all appended
+  else load_rows([&](int i) { return group_row(a, a.lay.tail_k, a.k, bh, pos_of(i)); });
   if (rope) {  // RoPE at the absolute position, rounded back to the activation dtype
 #pragma unroll
     for (int i0 = 0; i0 < 8; i0 += 4) {  // four tokens' table rows in flight at a time
@@ -340,11 +381,12 @@ __device__ __forceinline__ void flush_k(const AppendArgs& a, const int* sub, int
     zsk[c] = zs[h];
   }
   __syncwarp();
-  Slice q[8];
+  Slice2 q[4];  // channels (2p, 2p + 1), from lane p of the quad
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int src = (lane & ~3) | (k >> 1);
-    q[k] = make_slice(__shfl_sync(0xffffffffu, zs[k & 1], src), __shfl_sync(0xffffffffu, rr[k & 1], src));
+  for (int p = 0; p < 4; ++p) {
+    const int src = (lane & ~3) | p;
+    q[p] = pair_slices(make_slice(__shfl_sync(0xffffffffu, zs[0], src), __shfl_sync(0xffffffffu, rr[0], src)),
+                       make_slice(__shfl_sync(0xffffffffu, zs[1], src), __shfl_sync(0xffffffffu, rr[1], src)));
   }
   // a slice whose codes could leave [0, LB] sends the quad's words down the exact path
   const bool clamp = ((__ballot_sync(0xffffffffu, !ok) >> (lane & ~3)) & 0xfu) != 0;
@@ -363,9 +405,10 @@ __device__ __forceinline__ void flush_k(const AppendArgs& a, const int* sub, int
 #pragma unroll
     for (int ts = 0; ts < 2; ++ts) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int j = M::acc(ts, k);
-        add_code(act_half<BF16>(xg[ts][k >> 1], k & 1), q[k], M::bit(ts, k), acc[j], corr[j]);
+      for (int p = 0; p < 4; ++p) {  // channels 2p, 2p + 1: the two halves of one word
+        const int j0 = M::acc(ts, 2 * p), j1 = M::acc(ts, 2 * p + 1);
+        add_code2(make_float2(act_lo<BF16>(xg[ts][p]), act_hi<BF16>(xg[ts][p])), q[p], M::bit(ts, 2 * p),
+                  M::bit(ts, 2 * p + 1), acc[j0], corr[j0], acc[j1], corr[j1]);
       }
     }
 #pragma unroll
@@ -470,9 +513,10 @@ __device__ __noinline__ uint2 v_exact_g(const uint16_t* row0, const uint16_t* ro
   return make_uint2(acc[0], acc[1]);
 }
 
+// lin: as for flush_k, the group's first V row or null.
 template <int D, int VB, bool BF16>
 __device__ __forceinline__ void flush_v(const AppendArgs& a, const int* sub, int64_t p0, int bh, uint8_t* chunk,
-                                        uint4 (*scratch)[D]) {
+                                        uint4 (*scratch)[D], const uint16_t* lin) {
   using M = VMap<VB>;
   constexpr int LB = (1 << VB) - 1, NV = D / 32;
   constexpr int PW = piece_words(D * VB / 32);
@@ -482,15 +526,19 @@ __device__ __forceinline__ void flush_v(const AppendArgs& a, const int* sub, int
   const bool odd = m & 1;
   const uint16_t* rows[4];
   uint32_t x[4][8];
+  auto load_rows = [&](auto row_of) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = 16 * kb + 2 * t + (i & 1) + 8 * (i >> 1);
-    rows[i] = group_row(a, a.lay.tail_v, a.v, bh, p0 + (sub ? sub[r] : r)) + 16 * m;
-    const uint4 u0 = __ldg(reinterpret_cast<const uint4*>(rows[i]));
-    const uint4 u1 = __ldg(reinterpret_cast<const uint4*>(rows[i] + 8));
-    x[i][0] = u0.x, x[i][1] = u0.y, x[i][2] = u0.z, x[i][3] = u0.w;
-    x[i][4] = u1.x, x[i][5] = u1.y, x[i][6] = u1.z, x[i][7] = u1.w;
-  }
+    for (int i = 0; i < 4; ++i) {
+      const int r = 16 * kb + 2 * t + (i & 1) + 8 * (i >> 1);
+      rows[i] = row_of(r) + 16 * m;
+      const uint4 u0 = __ldg(reinterpret_cast<const uint4*>(rows[i]));
+      const uint4 u1 = __ldg(reinterpret_cast<const uint4*>(rows[i] + 8));
+      x[i][0] = u0.x, x[i][1] = u0.y, x[i][2] = u0.z, x[i][3] = u0.w;
+      x[i][4] = u1.x, x[i][5] = u1.y, x[i][6] = u1.z, x[i][7] = u1.w;
+    }
+  };
+  if (lin) load_rows([&](int r) { return lin + r * D; });
+  else load_rows([&](int r) { return group_row(a, a.lay.tail_v, a.v, bh, p0 + (sub ? sub[r] : r)); });
   // slot 2 g2 + hh of this thread's scratch column: the channel pairs
   // (2 g2, +1) and (2 g2 + 8, +9) of tokens 2 hh, 2 hh + 1, what the g = 2 g2,
   // 2 g2 + 1 steps of the compact loop below read
@@ -504,6 +552,7 @@ __device__ __forceinline__ void flush_v(const AppendArgs& a, const int* sub, int
   const int vg = m >> 1, mk = 2 * m + kb;
   const bool q40 = VB == 4 && G.v_q4_0;
   Slice q[4];
+  Slice2 q2[2];  // tokens (0, 1) and (2, 3)
   uint32_t zsv[4] = {0u, 0u, 0u, 0u};
   float qd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   bool clamp = false;
@@ -520,7 +569,7 @@ __device__ __forceinline__ void flush_v(const AppendArgs& a, const int* sub, int
       }
       const float am2 = __shfl_xor_sync(0xffffffffu, am, 1), mv2 = __shfl_xor_sync(0xffffffffu, mv, 1);
       if (odd ? am2 >= am : am2 > am) mv = mv2;
-      const __half sh = __float2half_rn(__fdiv_rn(mv, -8.0f));
+      const __half sh = __float2half_rn(__fmul_rn(mv, -0.125f));  // = RN(mv / -8): a power of two
       qd[i] = __half2float(sh);
       q[i].r = __frcp_rn(qd[i]);
       if ((i >> 1) == static_cast<int>(odd)) {  // each of the pair writes two tokens' meta
@@ -562,6 +611,8 @@ __device__ __forceinline__ void flush_v(const AppendArgs& a, const int* sub, int
       q[e] = make_slice(zsv[e], odd ? ro : rr[e]);
       q[2 + e] = make_slice(zsv[2 + e], odd ? rr[e] : ro);
     }
+    q2[0] = pair_slices(q[0], q[1]);
+    q2[1] = pair_slices(q[2], q[3]);
     // a slice whose codes could leave [0, LB] sends the pair's words down the exact path
     clamp = __shfl_xor_sync(0xffffffffu, static_cast<int>(!ok), 1) != 0 || !ok;
   }
@@ -585,10 +636,13 @@ __device__ __forceinline__ void flush_v(const AppendArgs& a, const int* sub, int
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 4; i += 2) {  // tokens i, i + 1: two slices
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          add_code(act_half<BF16>(xg[i][h], gg), q[i], M::bit(i, h), acc[M::acc(i, h)], corr[M::acc(i, h)]);
+        for (int h = 0; h < 2; ++h) {
+          const int j0 = M::acc(i, h), j1 = M::acc(i + 1, h);
+          add_code2(make_float2(act_half<BF16>(xg[i][h], gg), act_half<BF16>(xg[i + 1][h], gg)), q2[i >> 1],
+                    M::bit(i, h), M::bit(i + 1, h), acc[j0], corr[j0], acc[j1], corr[j1]);
+        }
       }
     }
 #pragma unroll
@@ -621,11 +675,15 @@ __device__ __forceinline__ void flush_v(const AppendArgs& a, const int* sub, int
 template <int D, int KB, int VB, bool BF16>
 __device__ __forceinline__ void flush_group(const AppendArgs& a, const int* sub, int64_t p0, int bh, uint8_t* chunk,
                                             uint32_t* zsk, uint4 (*scratch)[D]) {
+  // the common prefill case: the group's 32 rows are consecutive appended rows
+  const size_t lin_off = (!sub && p0 >= a.L0) ? (static_cast<size_t>(bh) * a.n + (p0 - a.L0)) * D : ~size_t{0};
   if (threadIdx.x < D / 2) {
-    if (a.geo.k_pre_rope) flush_k<D, KB, BF16, true>(a, sub, p0, bh, chunk, zsk, scratch);
-    else flush_k<D, KB, BF16, false>(a, sub, p0, bh, chunk, zsk, scratch);
+    const uint16_t* lin = lin_off != ~size_t{0} ? a.k + lin_off : nullptr;
+    if (a.geo.k_pre_rope) flush_k<D, KB, BF16, true>(a, sub, p0, bh, chunk, zsk, scratch, lin);
+    else flush_k<D, KB, BF16, false>(a, sub, p0, bh, chunk, zsk, scratch, lin);
   } else {
-    flush_v<D, VB, BF16>(a, sub, p0, bh, chunk, scratch);
+    const uint16_t* lin = lin_off != ~size_t{0} ? a.v + lin_off : nullptr;
+    flush_v<D, VB, BF16>(a, sub, p0, bh, chunk, scratch, lin);
   }
 }
 
