@@ -673,11 +673,17 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
               }
             }
           }
+          const float2 ci = make_float2(CodeConsts<KB>::kCodeInv, CodeConsts<KB>::kCodeInv);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float z = zb[0][e] + zb[1][e];
-            sc[0][e] = fmaf(sa[0][0][e] + sa[0][1][e], CodeConsts<KB>::kCodeInv, z);
-            sc[1][e] = fmaf(sa[1][0][e] + sa[1][1][e], CodeConsts<KB>::kCodeInv, z);
+          for (int e = 0; e < 4; e += 2) {  // two accumulator elements per FP32x2 instruction
+            const float2 z = __fadd2_rn(make_float2(zb[0][e], zb[0][e + 1]), make_float2(zb[1][e], zb[1][e + 1]));
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              const float2 r = __ffma2_rn(__fadd2_rn(make_float2(sa[mt][0][e], sa[mt][0][e + 1]),
+                                                     make_float2(sa[mt][1][e], sa[mt][1][e + 1])),
+                                          ci, z);
+              sc[mt][e] = r.x, sc[mt][e + 1] = r.y;
+            }
           }
         }
       };
@@ -727,12 +733,17 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
             }
           }
         }
+        const float2 ci = make_float2(CodeConsts<KB>::kCodeInv, CodeConsts<KB>::kCodeInv);
 #pragma unroll
         for (int q = 0; q < 2; ++q)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            sc[q][0][e] = fmaf(sa[q][0][e], CodeConsts<KB>::kCodeInv, zb[q][e]);
-            sc[q][1][e] = fmaf(sa[q][1][e], CodeConsts<KB>::kCodeInv, zb[q][e]);
+          for (int e = 0; e < 4; e += 2) {  // two accumulator elements per FP32x2 FMA
+            const float2 z = make_float2(zb[q][e], zb[q][e + 1]);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              const float2 r = __ffma2_rn(make_float2(sa[q][mt][e], sa[q][mt][e + 1]), ci, z);
+              sc[q][mt][e] = r.x, sc[q][mt][e + 1] = r.y;
+            }
           }
       };
       for (int k = 0; k < n_my && !failed; ++k, ++n_t) {
@@ -799,23 +810,29 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           m_run = mn;
         }
         const float nref = (m_run == -INFINITY) ? 0.0f : -m_run * ks;  // exponent offset
-        uint32_t ph[GPB][4];  // weights as (f16 value, 0) per token: the odd B columns stay zero
+        // weights as (f16 value, 0) per token (the odd B columns stay zero),
+        // tokens g and g + 8 of an m-tile in one f16x2 word; two tokens per
+        // FP32x2 instruction
+        uint32_t ph[GPB][2];
+        const float2 ks2 = make_float2(ks, ks), nref2 = make_float2(nref, nref);
+        float2 l2 = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int q = 0; q < GPB; ++q)
 #pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const float p = fast_exp2(fmaf(pr[q][mt][r], ks, nref));
-              l_run += p;
-              float w = p;
-              if constexpr (TQ) {  // the V norm of the token folded in (rows past F hold no data: weight 0)
-                const float nv = reinterpret_cast<const float*>(stages + st * STAGE + q * CHUNK +
-                                                                T::VMETA)[16 * mt + g + 8 * r];
-                w = p > 0.0f ? p * nv : 0.0f;
-              }
-              ph[q][mt * 2 + r] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(w)));
+          for (int mt = 0; mt < 2; ++mt) {
+            const float2 x2 = __ffma2_rn(make_float2(pr[q][mt][0], pr[q][mt][1]), ks2, nref2);
+            const float2 p2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
+            l2 = __fadd2_rn(l2, p2);
+            float2 w = p2;
+            if constexpr (TQ) {  // the V norm of the token folded in (rows past F hold no data: weight 0)
+              const float* nv = reinterpret_cast<const float*>(stages + st * STAGE + q * CHUNK + T::VMETA);
+              w.x = p2.x > 0.0f ? p2.x * nv[16 * mt + g] : 0.0f;
+              w.y = p2.y > 0.0f ? p2.y * nv[16 * mt + g + 8] : 0.0f;
             }
+            const __half2 wh = __floats2half2_rn(w.x, w.y);
+            ph[q][mt] = *reinterpret_cast<const uint32_t*>(&wh);
+          }
+        l_run += l2.x + l2.y;
         // hand the weights to the PV warp
         if (!warp_wait(&pempty[pb], static_cast<uint32_t>(((n_t >> 1) & 1) ^ 1), abort_flag)) {
           failed = true;
@@ -824,8 +841,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
         uint8_t* pw = pbuf + pb * T::PBUF;
 #pragma unroll
         for (int q = 0; q < GPB; ++q)
-          *reinterpret_cast<uint2*>(pw + (q * 32 + lane) * 8) =
-              make_uint2(ph[q][0] | (ph[q][1] << 16), ph[q][2] | (ph[q][3] << 16));
+          *reinterpret_cast<uint2*>(pw + (q * 32 + lane) * 8) = make_uint2(ph[q][0], ph[q][1]);
         reinterpret_cast<float*>(pw + GPB * 32 * 8)[t] = al;  // the 8 lanes of query head t store the same value
         mbar_arrive(&pfull[pb]);
       }
