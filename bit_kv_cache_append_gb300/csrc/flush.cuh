@@ -1,6 +1,7 @@
 // KIVI group quantisation: the flush of completed 32-token groups into the
-// code chunks, straight from registers into the decode kernel's fragment
-// order (kvq_layout.h), with no shared-memory staging of values or codes.
+// code chunks, as whole words of the decode kernel's fragment order
+// (kvq_layout.h) built in registers; each thread's values wait in its own
+// column of a shared-memory scratch between min/max and the per-word loop.
 //
 // One CTA per (group, b, h), D threads: the first D/2 quantise K, the rest V.
 // Quantisation follows posttrainllm "StreamingLLM + KIVI", "Affine
@@ -61,7 +62,6 @@ namespace {
 // mantissa bits.
 constexpr float kMagic = 12582912.0f;
 constexpr uint32_t kMagicBits = 0x4B400000u;
-constexpr float kRcpLo = 1.0f - 0x1p-20f, kRcpHi = 1.0f + 0x1p-20f;
 
 template <bool BF16>
 __device__ __forceinline__ float act_lo(uint32_t w) {
