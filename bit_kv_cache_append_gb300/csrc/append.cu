@@ -96,13 +96,23 @@ __device__ __forceinline__ float tq_code_row(float (&x)[D / 32], const float* si
     if (lane < st) acc = __fadd_rn(acc, o);
   }
   const float n = __shfl_sync(0xffffffffu, __fsqrt_rn(acc), 0);
-  const int nb = (1 << bits) - 1;
+  // u = RN(y / n) by Markstein's correction step from RN(1 / n) (P.
+  // Markstein, IBM J. Res. Dev. 34(1), 1990), exact like the division
+  const float rn = n > 0.0f ? __frcp_rn(n) : 0.0f;
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
-    const float u = (n > 0.0f) ? __fdiv_rn(y[i], n) : 0.0f;
+    float u = 0.0f;
+    if (n > 0.0f) {
+      const float q0 = __fmul_rn(y[i], rn);
+      u = __fmaf_rn(__fmaf_rn(-q0, n, y[i]), rn, q0);
+    }
     const float w = __fmul_rn(__fadd_rn(u, 1.0f), 0.5f);
+    // the number of boundaries <= w: a branchless binary search over the
+    // ascending boundaries (padded to 16 with 2.0, above every w)
     int code = 0;
-    for (int k = 0; k < nb; ++k) code += (w >= bnd[k]) ? 1 : 0;
+#pragma unroll
+    for (int step = 8; step >= 1; step >>= 1)
+      if (step < (1 << bits)) code += (w >= bnd[code + step - 1]) ? step : 0;
     codes_smem[i * 32 + lane] = static_cast<uint8_t>(code);
   }
   return n;
@@ -139,37 +149,47 @@ __global__ void __launch_bounds__(128) tq_quantize_kernel(AppendArgs a, int64_t 
   const int slot = static_cast<int>((p0 / kGroup) % G.n_slots);
   uint8_t* chunk = a.lay.chunks + (static_cast<size_t>(bh) * G.n_slots + slot) * G.chunk.bytes;
   const int kb = G.kb, vb = G.vb;
+  // both tokens' rows first (a token not in this call reads the other's
+  // row and stores nothing), so that their butterflies and searches overlap
   bool have[2];
+  float xk[2][NS], xv[2][NS];
+#pragma unroll
   for (int e = 0; e < 2; ++e) {
     const int64_t pos = p0 + e;
     have[e] = pos >= a.L0 && pos < a.L0 + a.n;
-    if (!have[e]) continue;
-    const size_t in_row = (static_cast<size_t>(bh) * a.n + (pos - a.L0)) * D;
-    float xk[NS], xv[NS];
+    const int64_t lp = have[e] ? pos : (have[e ^ 1] ? p0 + (e ^ 1) : a.L0);
+    const size_t in_row = (static_cast<size_t>(bh) * a.n + (lp - a.L0)) * D;
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
-      xk[i] = act_to_float(a.k[in_row + i * 32 + lane], bf16);
-      xv[i] = act_to_float(a.v[in_row + i * 32 + lane], bf16);
+      xk[e][i] = act_to_float(a.k[in_row + i * 32 + lane], bf16);
+      xv[e][i] = act_to_float(a.v[in_row + i * 32 + lane], bf16);
     }
     if (a.tab.rope) {
-      const float* tr = a.tab.rope + static_cast<size_t>(pos) * D;
+      const float* tr = a.tab.rope + static_cast<size_t>(lp) * D;
 #pragma unroll
       for (int i = 0; i < NS / 2; ++i) {
         const int c = i * 32 + lane;
         float rx, ry;
-        rope_pair(xk[i], xk[i + NS / 2], tr[2 * c], tr[2 * c + 1], &rx, &ry);
-        xk[i] = act_to_float(float_to_act(rx, bf16), bf16);
-        xk[i + NS / 2] = act_to_float(float_to_act(ry, bf16), bf16);
+        rope_pair(xk[e][i], xk[e][i + NS / 2], tr[2 * c], tr[2 * c + 1], &rx, &ry);
+        xk[e][i] = act_to_float(float_to_act(rx, bf16), bf16);
+        xk[e][i + NS / 2] = act_to_float(float_to_act(ry, bf16), bf16);
       }
     }
-    const int r = static_cast<int>(pos % kGroup);
-    const float nk = tq_code_row<D>(xk, s_signs, s_bk, kb, rsq, codes[warp][0][e]);
-    const float nv = tq_code_row<D>(xv, s_signs, s_bv, vb, rsq, codes[warp][1][e]);
+  }
+  float nk[2], nv[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    nk[e] = tq_code_row<D>(xk[e], s_signs, s_bk, kb, rsq, codes[warp][0][e]);
+    nv[e] = tq_code_row<D>(xv[e], s_signs, s_bv, vb, rsq, codes[warp][1][e]);
+  }
+  __syncwarp();
+  for (int e = 0; e < 2; ++e) {
+    if (!have[e]) continue;
+    const int r = static_cast<int>((p0 + e) % kGroup);
     if (lane == 0) {
-      reinterpret_cast<float*>(chunk + G.chunk.kmeta_off)[r] = nk;
-      reinterpret_cast<float*>(chunk + G.chunk.vmeta_off)[r] = nv;
+      reinterpret_cast<float*>(chunk + G.chunk.kmeta_off)[r] = nk[e];
+      reinterpret_cast<float*>(chunk + G.chunk.vmeta_off)[r] = nv[e];
     }
-    __syncwarp();
     // K: block b = 2 (r / 16) + (r / 8) % 2 of lanes 4 (r % 8) + t; lane
     // 2 BBK / 2 ... writes 16-bit half h of the block of lane t
     const int bbk = D * kb / 32;  // bytes per token block
@@ -189,7 +209,6 @@ __global__ void __launch_bounds__(128) tq_quantize_kernel(AppendArgs a, int64_t 
       *reinterpret_cast<uint16_t*>(chunk + G.chunk.kc_off + lane_byte_offset(L, blk * bbk + 2 * hw, pw)) =
           static_cast<uint16_t>(half);
     }
-    __syncwarp();
   }
   // V: the pair row, 16-bit halves; a token not in this call keeps its bits
   const int rb = tq_vrow_bytes(D, vb);
