@@ -282,14 +282,22 @@ __device__ __forceinline__ void load_lane_range(const uint8_t* region, int lane,
   }
 }
 
-// The field of 2 BITS bits at bit `bit` of a lane's bit string (w[] has one
-// word of padding after the string).
-template <int BITS>
-__device__ __forceinline__ uint32_t lane_field(const uint32_t* w, int bit) {
-  constexpr uint32_t M = (1u << (2 * BITS)) - 1u;
+// The table entry of the field of 2 BITS bits at bit `bit` of a lane's bit
+// string: entry e of copy cp sits at byte (e NLUT + cp) 4 of the table, so
+// the field is taken out already scaled to e NLUT 4 (one shift, or a funnel
+// shift where it straddles two words) and joined with cp4 = 4 cp by the
+// mask's own instruction; the table's shared-memory base folds into the
+// load's immediate.
+template <int BITS, int NLUT>
+__device__ __forceinline__ uint32_t table_entry(const uint32_t* table, const uint32_t* w, int bit, uint32_t cp4) {
+  constexpr int SH = NLUT == 32 ? 7 : 6;
+  static_assert(NLUT == 32 || NLUT == 16, "copies");
+  constexpr uint32_t M = ((1u << (2 * BITS)) - 1u) << SH;
   const int wi = bit >> 5, sh = bit & 31;
-  if (sh + 2 * BITS <= 32) return (w[wi] >> sh) & M;
-  return __funnelshift_r(w[wi], w[wi + 1], sh) & M;
+  uint32_t x;
+  if (sh + 2 * BITS <= 32) x = sh >= SH ? (w[wi] >> (sh - SH)) : (w[wi] << (SH - sh));
+  else x = __funnelshift_r(w[wi], w[wi + 1], sh - SH);  // sh > 32 - 2 BITS >= SH here
+  return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(table) + ((x & M) | cp4));
 }
 
 // Walks the runs of pair p inside its CTA's range [i0, i1): per unit (run of
@@ -562,19 +570,20 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           uint32_t kw[KWT + 1];
           load_lane_words<KWT, PWT>(tile, lane, kw);
           kw[KWT] = 0u;
-          const uint32_t* lk = lut_k + (lane % T::NLUT);
+          const uint32_t cp4 = 4u * static_cast<uint32_t>(lane % T::NLUT);
           float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
+          for (int s = 0; s < S; ++s) {  // one read of the query operand per k-step serves both m-tiles
+            const uint4 q4 = qsm[s * 32 + lane];
 #pragma unroll
-            for (int s = 0; s < S; ++s) {
-              const uint4 q4 = qsm[s * 32 + lane];
-              const uint32_t a0 = lk[lane_field<KB>(kw, tq_kfield_bit(D, KB, 2 * mt, 2 * s)) * T::NLUT];
-              const uint32_t a1 = lk[lane_field<KB>(kw, tq_kfield_bit(D, KB, 2 * mt + 1, 2 * s)) * T::NLUT];
-              const uint32_t a2 = lk[lane_field<KB>(kw, tq_kfield_bit(D, KB, 2 * mt, 2 * s + 1)) * T::NLUT];
-              const uint32_t a3 = lk[lane_field<KB>(kw, tq_kfield_bit(D, KB, 2 * mt + 1, 2 * s + 1)) * T::NLUT];
+            for (int mt = 0; mt < 2; ++mt) {
+              const uint32_t a0 = table_entry<KB, T::NLUT>(lut_k, kw, tq_kfield_bit(D, KB, 2 * mt, 2 * s), cp4);
+              const uint32_t a1 = table_entry<KB, T::NLUT>(lut_k, kw, tq_kfield_bit(D, KB, 2 * mt + 1, 2 * s), cp4);
+              const uint32_t a2 = table_entry<KB, T::NLUT>(lut_k, kw, tq_kfield_bit(D, KB, 2 * mt, 2 * s + 1), cp4);
+              const uint32_t a3 = table_entry<KB, T::NLUT>(lut_k, kw, tq_kfield_bit(D, KB, 2 * mt + 1, 2 * s + 1), cp4);
               mma_f16(acc[mt], a0, a1, a2, a3, q4.y, q4.w);
             }
+          }
           const float* kn = reinterpret_cast<const float*>(tile + T::KMETA);
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt) {
@@ -874,7 +883,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           // its A pairs (channel, two tokens); the lane's copy of the table
           // turns them into f16x2
           constexpr int RB = tq_vrow_bytes(D, VB), BB = D * VB / 32, BW = (BB + 3) / 4;
-          const uint32_t* lv = lut_v + (lane % T::NLUT);
+          const uint32_t cp4 = 4u * static_cast<uint32_t>(lane % T::NLUT);
           const uint8_t* vrows = tile + T::VC;
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
@@ -902,7 +911,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
               bw[BW] = 0u;
 #pragma unroll
               for (int jj = 0; jj < 2 * MV; ++jj)
-                A[jj >> 1][2 * hh + (jj & 1)] = lv[lane_field<VB>(bw, 2 * VB * jj) * T::NLUT];
+                A[jj >> 1][2 * hh + (jj & 1)] = table_entry<VB, T::NLUT>(lut_v, bw, 2 * VB * jj, cp4);
             }
 #pragma unroll
             for (int m = 0; m < MV; ++m) mma_f16(oacc[m], A[m][0], A[m][1], A[m][2], A[m][3], b0, b1);
