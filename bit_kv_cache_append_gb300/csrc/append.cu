@@ -65,10 +65,13 @@ __device__ __forceinline__ float tq_code_row(float (&x)[D / 32], const float* si
   }
 #pragma unroll
   for (int len = 1; len < 32; len <<= 1) {
+    // the upper lane of a butterfly takes o - y, the lower y + o: one FMA
+    // with y times -1 or +1 (exact), rounded like the subtraction or sum
+    const float sgn = (lane & len) ? -1.0f : 1.0f;
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
       const float o = __shfl_xor_sync(0xffffffffu, y[i], len);
-      y[i] = (lane & len) ? __fsub_rn(o, y[i]) : __fadd_rn(y[i], o);
+      y[i] = __fmaf_rn(y[i], sgn, o);
     }
   }
 #pragma unroll
