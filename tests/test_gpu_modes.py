@@ -271,7 +271,7 @@ def test_kvsink_group_of_only_sinks():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("kb,vb,act", [(2, 4, "bf16"), (4, 4, "f16"), (3, 8, "bf16")])
+@pytest.mark.parametrize("kb,vb,act", [(2, 4, "bf16"), (4, 4, "f16"), (3, 8, "bf16"), (8, 2, "f16")])
 @pytest.mark.parametrize("D", [128, 64])
 def test_pre_rope_prefill_then_appends(kb, vb, act, D):
     """Keys stored before RoPE (posttrainllm "RoPE caveat"): prefill 1000
@@ -297,3 +297,33 @@ def test_pre_rope_prefill_then_appends(kb, vb, act, D):
             _decode_both(gc, oc, 0, W.queries(w, 12, pos), act)
     compare_exports(gc, oc, 0)
     _decode_both(gc, oc, 0, W.queries(w, 12, 99), act)
+
+
+@pytest.mark.parametrize("kb,vb,act", [(2, 4, "bf16"), (3, 3, "f16"), (8, 8, "bf16"), (4, 2, "bf16"), (2, 3, "f16")])
+@pytest.mark.parametrize("D", [128, 64])
+def test_rope_at_append_prefill_then_appends(kb, vb, act, D):
+    """Keys rotated when appended (posttrainllm "RoPE caveat": each key keeps
+    the rotation of its absolute position, rounded back to the activation
+    dtype): a prefill of 1000 tokens, whose groups are quantised from the
+    rotated rows in one pass, then appends of mixed sizes whose groups are
+    completed from the tail ring; codes, scales and zeros bit-exact,
+    attention within tolerance."""
+    w = W.scaled(W.WORKLOADS["llama8b"], batch=2, n_kv_heads=2, n_q_heads=8, head_dim=D, context=2048,
+                 k_bits=kb, v_bits=vb, act_dtype=act, n_sink=4, window=40, rope_base=10000.0)
+    kw = cache_kwargs(w, 2048, rope_max_pos=2048)
+    gc, oc = _pair(kw)
+    k, v = W.kv_tokens(w, 14, 1000)
+    gc.prefill_quantize(0, torch_act(k, act), torch_act(v, act))
+    oc.prefill_quantize(0, k, v)
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 14, 0), act)
+    pos = 1000
+    for i, n in enumerate([1, 3, 31, 1, 32, 7, 64, 1]):
+        k, v = W.kv_tokens(w, 14, n, first_pos=pos)
+        gc.append(0, torch_act(k, act), torch_act(v, act))
+        oc.append(0, k, v)
+        pos += n
+        if i % 3 == 2:
+            _decode_both(gc, oc, 0, W.queries(w, 14, pos), act)
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 14, 99), act)
