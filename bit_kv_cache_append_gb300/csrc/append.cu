@@ -46,6 +46,32 @@ __global__ void tail_write_kernel(AppendArgs a, int row_begin, int n_rows) {
 }
 
 // ---------------------------------------------------------------- TurboQuant
+// Token pairs each warp of the quantiser takes in turn (the CTA's setup,
+// the codebook boundaries and the warp's signs, is paid once for them).
+constexpr int kTqPairsPerWarp = 8;
+// The code search's guess table: w in [0, 1] falls in cell floor(kTqCells w)
+// (kTqCells + 1 cells with w = 1); the cell's entry is the number of
+// boundaries <= its start, valid while no cell holds two boundaries.
+constexpr int kTqCells = 256;
+constexpr float kMagicF = 12582912.0f;  // 1.5 * 2^23: x + kMagicF keeps floor / rint(x) in the low bits
+constexpr uint32_t kMagicBitsF = 0x4B400000u;
+
+// Builds the guess table of nb ascending boundaries (threads of the CTA in
+// turn); returns, through ok (shared, set to 1 before), whether every cell
+// holds at most one boundary.
+__device__ __forceinline__ void tq_guess_table(const float* bnd, int nb, uint8_t* guess, int* ok) {
+  for (int j = threadIdx.x; j <= kTqCells; j += blockDim.x) {
+    const float lo = static_cast<float>(j) / kTqCells, hi = static_cast<float>(j + 1) / kTqCells;
+    int below = 0, inside = 0;
+    for (int k = 0; k < nb; ++k) {
+      below += bnd[k] <= lo ? 1 : 0;
+      inside += (bnd[k] > lo && bnd[k] < hi) ? 1 : 0;
+    }
+    guess[j] = static_cast<uint8_t>(below);
+    if (inside > 1) *ok = 0;
+  }
+}
+
 // One warp per (token, b, h): Foundry "TurboQuant KV Cache Compression - Spec",
 // "Algorithm Detail" with the as-built order (signs, then the Walsh-Hadamard
 // butterflies with stage length 1, 2, 4, ..., then 1/sqrt(d)); the norm is the
@@ -53,14 +79,14 @@ __global__ void tail_write_kernel(AppendArgs a, int row_begin, int n_rows) {
 // coordinate becomes w = (y/n + 1) * 0.5 and its code counts the boundaries
 // <= w. Lane l holds channels i*32 + l.
 template <int D>
-__device__ __forceinline__ float tq_code_row(float (&x)[D / 32], const float* signs, const float* bnd,
-                                             int bits, float rsq, uint8_t* codes_smem) {
+__device__ __forceinline__ float tq_code_row(float (&x)[D / 32], const float (&sg)[D / 32], const float* bnd,
+                                             const uint8_t* guess, int bits, float rsq, uint8_t* codes_smem) {
   constexpr int NS = D / 32;
   const int lane = threadIdx.x & 31;
   float y[NS], sq[NS];
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
-    y[i] = __fmul_rn(x[i], signs[i * 32 + lane]);
+    y[i] = __fmul_rn(x[i], sg[i]);
     sq[i] = __fmul_rn(x[i], x[i]);
   }
 #pragma unroll
@@ -110,12 +136,20 @@ __device__ __forceinline__ float tq_code_row(float (&x)[D / 32], const float* si
       u = __fmaf_rn(__fmaf_rn(-q0, n, y[i]), rn, q0);
     }
     const float w = __fmul_rn(__fadd_rn(u, 1.0f), 0.5f);
-    // the number of boundaries <= w: a branchless binary search over the
-    // ascending boundaries (padded to 16 with 2.0, above every w)
+    // the number of boundaries <= w (ascending, padded to 16 with 2.0,
+    // above every w): from the guess of w's cell (w is in [0, 1]) and one
+    // comparison, or a branchless binary search where a cell holds two
+    // boundaries
     int code = 0;
+    if (guess) {
+      const float t = __fmaf_rd(w, static_cast<float>(kTqCells), kMagicF);  // kMagicF + floor(kTqCells w)
+      const int g = guess[__float_as_uint(t) - kMagicBitsF];
+      code = g + (w >= bnd[g] ? 1 : 0);
+    } else {
 #pragma unroll
-    for (int step = 8; step >= 1; step >>= 1)
-      if (step < (1 << bits)) code += (w >= bnd[code + step - 1]) ? step : 0;
+      for (int step = 8; step >= 1; step >>= 1)
+        if (step < (1 << bits)) code += (w >= bnd[code + step - 1]) ? step : 0;
+    }
     codes_smem[i * 32 + lane] = static_cast<uint8_t>(code);
   }
   return n;
@@ -132,18 +166,30 @@ template <int D>
 __global__ void __launch_bounds__(128) tq_quantize_kernel(AppendArgs a, int64_t pair_begin, int n_pairs) {
   constexpr int NS = D / 32;
   __shared__ uint8_t codes[4][2][2][D];  // [warp][K, V][token of the pair][channel]
-  __shared__ float s_signs[D];
   __shared__ float s_bk[16], s_bv[16];
+  __shared__ uint8_t s_gk[kTqCells + 1], s_gv[kTqCells + 1];
+  __shared__ int s_ok[2];
   const Geometry& G = a.geo;
-  for (int i = threadIdx.x; i < D; i += blockDim.x) s_signs[i] = a.tab.signs[i];
   if (threadIdx.x < 16) {
     s_bk[threadIdx.x] = (threadIdx.x < (1 << G.kb) - 1) ? a.tab.cb_k[threadIdx.x] : 2.0f;
     s_bv[threadIdx.x] = (threadIdx.x < (1 << G.vb) - 1) ? a.tab.cb_v[threadIdx.x] : 2.0f;
   }
+  if (threadIdx.x < 2) s_ok[threadIdx.x] = 1;
   __syncthreads();
+  tq_guess_table(s_bk, (1 << G.kb) - 1, s_gk, &s_ok[0]);
+  tq_guess_table(s_bv, (1 << G.vb) - 1, s_gv, &s_ok[1]);
+  __syncthreads();
+  const uint8_t* gk = s_ok[0] ? s_gk : nullptr;
+  const uint8_t* gv = s_ok[1] ? s_gv : nullptr;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pi_idx = blockIdx.x * 4 + warp;
-  if (pi_idx >= n_pairs) return;
+  float sg[NS];  // this lane's signs (channels i * 32 + lane)
+#pragma unroll
+  for (int i = 0; i < NS; ++i) sg[i] = a.tab.signs[i * 32 + lane];
+  // the CTA's pairs [first, first + 4 kTqPairsPerWarp), warp w taking w, w + 4, ...
+  const int first = blockIdx.x * 4 * kTqPairsPerWarp;
+  const int last = min(n_pairs, first + 4 * kTqPairsPerWarp);
+  for (int pi_idx = first + warp; pi_idx < last; pi_idx += 4) {
+  __syncwarp();  // the previous pair's codes have been read
   const int64_t pi = pair_begin + pi_idx;
   const int bh = blockIdx.y;
   const int bf16 = G.act_bf16;
@@ -182,8 +228,8 @@ __global__ void __launch_bounds__(128) tq_quantize_kernel(AppendArgs a, int64_t 
   float nk[2], nv[2];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    nk[e] = tq_code_row<D>(xk[e], s_signs, s_bk, kb, rsq, codes[warp][0][e]);
-    nv[e] = tq_code_row<D>(xv[e], s_signs, s_bv, vb, rsq, codes[warp][1][e]);
+    nk[e] = tq_code_row<D>(xk[e], sg, s_bk, gk, kb, rsq, codes[warp][0][e]);
+    nv[e] = tq_code_row<D>(xv[e], sg, s_bv, gv, vb, rsq, codes[warp][1][e]);
   }
   __syncwarp();
   for (int e = 0; e < 2; ++e) {
@@ -231,6 +277,7 @@ __global__ void __launch_bounds__(128) tq_quantize_kernel(AppendArgs a, int64_t 
     if (mask != 0xffffu) half = (row[hw] & ~mask) | (half & mask);
     row[hw] = static_cast<uint16_t>(half);
   }
+  }
 }
 
 // ---------------------------------------------------------------- KVSink rows
@@ -273,7 +320,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int64_t* launches
   if (G.mode_tq && a.n > 0) {  // token pairs (2 pi, 2 pi + 1) that meet [L0, L0 + n)
     const int64_t pair_begin = a.L0 / 2, pair_end = (a.L0 + a.n + 1) / 2;
     const int n_pairs = static_cast<int>(pair_end - pair_begin);
-    dim3 grid((n_pairs + 3) / 4, BH);
+    dim3 grid((n_pairs + 4 * kTqPairsPerWarp - 1) / (4 * kTqPairsPerWarp), BH);
     if (G.D == 128) tq_quantize_kernel<128><<<grid, 128, 0, s>>>(a, pair_begin, n_pairs);
     else tq_quantize_kernel<64><<<grid, 128, 0, s>>>(a, pair_begin, n_pairs);
     ++*launches;
