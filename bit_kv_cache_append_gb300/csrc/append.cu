@@ -2,6 +2,7 @@
 // per-token quantisation and the KVSink sink-row gather; the launch of the
 // KIVI group quantisation (flush.cuh).
 #include <algorithm>
+#include <type_traits>
 
 #include "kvq_device.cuh"
 
@@ -72,15 +73,22 @@ __device__ __forceinline__ void tq_guess_table(const float* bnd, int nb, uint8_t
   }
 }
 
-// One warp per (token, b, h): Foundry "TurboQuant KV Cache Compression - Spec",
-// "Algorithm Detail" with the as-built order (signs, then the Walsh-Hadamard
-// butterflies with stage length 1, 2, 4, ..., then 1/sqrt(d)); the norm is the
-// fixed pairwise tree over x^2 (stride D/2, D/4, ..., 1) and its sqrt; each
-// coordinate becomes w = (y/n + 1) * 0.5 and its code counts the boundaries
-// <= w. Lane l holds channels i*32 + l.
-template <int D>
-__device__ __forceinline__ float tq_code_row(float (&x)[D / 32], const float (&sg)[D / 32], const float* bnd,
-                                             const uint8_t* guess, int bits, float rsq, uint8_t* codes_smem) {
+// How a row's codes are searched: the three 2-bit boundaries in registers,
+// the guess table and one comparison, or a binary search over the padded
+// boundaries in shared memory (where a guess cell holds two boundaries).
+enum TqSearch { kTqRegs = 0, kTqGuess = 1, kTqBinary = 2 };
+
+// One row (token, b, h) of a warp: Foundry "TurboQuant KV Cache Compression
+// - Spec", "Algorithm Detail" with the as-built order (signs, then the
+// Walsh-Hadamard butterflies with stage length 1, 2, 4, ..., then 1/sqrt(d));
+// the norm is the fixed pairwise tree over x^2 (stride D/2, D/4, ..., 1) and
+// its sqrt; each coordinate becomes w = (y/n + 1) * 0.5 and its code counts
+// the boundaries <= w. Lane l holds channels i*32 + l; bs[k] is -1 on the
+// lanes that take the upper end of a butterfly of length 2^k, else +1.
+template <int D, int BITS, int SEARCH>
+__device__ __forceinline__ float tq_code_row(const float (&x)[D / 32], const float (&sg)[D / 32], const float (&bs)[5],
+                                             const float (&br)[3], const float* bnd, const uint8_t* guess, float rsq,
+                                             uint32_t (&code)[D / 32]) {
   constexpr int NS = D / 32;
   const int lane = threadIdx.x & 31;
   float y[NS], sq[NS];
@@ -90,14 +98,13 @@ __device__ __forceinline__ float tq_code_row(float (&x)[D / 32], const float (&s
     sq[i] = __fmul_rn(x[i], x[i]);
   }
 #pragma unroll
-  for (int len = 1; len < 32; len <<= 1) {
+  for (int k = 0; k < 5; ++k) {
     // the upper lane of a butterfly takes o - y, the lower y + o: one FMA
     // with y times -1 or +1 (exact), rounded like the subtraction or sum
-    const float sgn = (lane & len) ? -1.0f : 1.0f;
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
-      const float o = __shfl_xor_sync(0xffffffffu, y[i], len);
-      y[i] = __fmaf_rn(y[i], sgn, o);
+      const float o = __shfl_xor_sync(0xffffffffu, y[i], 1 << k);
+      y[i] = __fmaf_rn(y[i], bs[k], o);
     }
   }
 #pragma unroll
@@ -112,8 +119,6 @@ __device__ __forceinline__ float tq_code_row(float (&x)[D / 32], const float (&s
     }
   }
 #pragma unroll
-  for (int i = 0; i < NS; ++i) y[i] = __fmul_rn(y[i], rsq);
-#pragma unroll
   for (int sl = NS / 2; sl >= 1; sl >>= 1) {
 #pragma unroll
     for (int i = 0; i < sl; ++i) sq[i] = __fadd_rn(sq[i], sq[i + sl]);
@@ -126,157 +131,283 @@ __device__ __forceinline__ float tq_code_row(float (&x)[D / 32], const float (&s
   }
   const float n = __shfl_sync(0xffffffffu, __fsqrt_rn(acc), 0);
   // u = RN(y / n) by Markstein's correction step from RN(1 / n) (P.
-  // Markstein, IBM J. Res. Dev. 34(1), 1990), exact like the division
+  // Markstein, IBM J. Res. Dev. 34(1), 1990), exact like the division; a
+  // zero norm takes 1/n = 0, which gives u = 0
   const float rn = n > 0.0f ? __frcp_rn(n) : 0.0f;
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
-    float u = 0.0f;
-    if (n > 0.0f) {
-      const float q0 = __fmul_rn(y[i], rn);
-      u = __fmaf_rn(__fmaf_rn(-q0, n, y[i]), rn, q0);
-    }
-    const float w = __fmul_rn(__fadd_rn(u, 1.0f), 0.5f);
-    // the number of boundaries <= w (ascending, padded to 16 with 2.0,
-    // above every w): from the guess of w's cell (w is in [0, 1]) and one
-    // comparison, or a branchless binary search where a cell holds two
-    // boundaries
-    int code = 0;
-    if (guess) {
-      const float t = __fmaf_rd(w, static_cast<float>(kTqCells), kMagicF);  // kMagicF + floor(kTqCells w)
-      const int g = guess[__float_as_uint(t) - kMagicBitsF];
-      code = g + (w >= bnd[g] ? 1 : 0);
-    } else {
+    const float yr = __fmul_rn(y[i], rsq);
+    const float q0 = __fmul_rn(yr, rn);
+    const float u = __fmaf_rn(__fmaf_rn(-q0, n, yr), rn, q0);
+    // RN(u / 2 + 1 / 2) = RN(u + 1) / 2: halving is exact for u + 1 in [0, 2]
+    const float w = __fmaf_rn(u, 0.5f, 0.5f);
+    uint32_t c;
+    if constexpr (SEARCH == kTqRegs) {  // three ascending boundaries
+      c = w >= br[1] ? 2u : 0u;
+      c += w >= (c ? br[2] : br[0]) ? 1u : 0u;
+    } else if constexpr (SEARCH == kTqGuess) {
+      // kMagicF + floor(kTqCells w), w clamped to [0, 1] for the cell only: u
+      // may stray past -1 or 1 by rounding, and a w outside [0, 1] is coded
+      // right from cell 0 (guess 0) or cell kTqCells (every boundary but the
+      // padding below it)
+      const float t = __fmaf_rd(__saturatef(w), static_cast<float>(kTqCells), kMagicF);
+      const uint32_t g = guess[__float_as_uint(t) - kMagicBitsF];
+      c = g + (w >= bnd[g] ? 1u : 0u);
+    } else {  // boundaries padded to 16 with 2.0, above every w
+      c = 0;
 #pragma unroll
       for (int step = 8; step >= 1; step >>= 1)
-        if (step < (1 << bits)) code += (w >= bnd[code + step - 1]) ? step : 0;
+        if (step < (1 << BITS)) c += (w >= bnd[c + step - 1]) ? step : 0;
     }
-    codes_smem[i * 32 + lane] = static_cast<uint8_t>(code);
+    code[i] = c;
   }
   return n;
 }
 
+// ORs value v, placed at bit `bit` of a little-endian string of W words,
+// into the string (v < 2^(32 - bit % 32) unless the string has a next word).
+template <int W>
+__device__ __forceinline__ void tq_place(uint32_t (&s)[W], int word, int shift, uint32_t v, bool straddle) {
+  if (!straddle) {
+    s[word] |= v << shift;
+  } else {
+    const uint64_t x = static_cast<uint64_t>(v) << shift;
+    s[word] |= static_cast<uint32_t>(x);
+    if (word + 1 < W) s[word + 1] |= static_cast<uint32_t>(x >> 32);
+  }
+}
+
+// Word k of a string held in registers (k from the lane, a select chain).
+template <int W>
+__device__ __forceinline__ uint32_t tq_word(const uint32_t (&s)[W], int k) {
+  uint32_t r = s[0];
+#pragma unroll
+  for (int j = 1; j < W; ++j)
+    if (k == j) r = s[j];
+  return r;
+}
+
 // One warp per token pair (2 pi, 2 pi + 1) of a group, for the tokens of
-// the pair this call appends. Codes go to the decode's layouts
-// (kvq_layout.h): K in fragment order (each token's fields are whole bytes
-// of four lanes' strings, written as 16-bit halves), V in token-pair rows
-// (a field holds both tokens' codes, so the warp writes the whole row; where
-// only one token of the pair is in this call, the other's bits are kept).
+// the pair this call appends; KB and VB are the code widths. Codes go to the
+// decode's layouts (kvq_layout.h), packed in registers and merged across
+// lanes by shuffles:
+//  * K in fragment order: string t (0..3) of a token holds the channels c
+//    with (c mod 8) / 2 = t, channel c at bit KB (2 (c / 8) + c mod 2); the
+//    lanes l with (l mod 8) / 2 = t hold them (channel i 32 + l at bit
+//    KB (8 i + 2 (l / 8) + l mod 2)). The string is the token's block
+//    (2 (r / 16) + (r / 8) mod 2, r its row in the group) of decode lane
+//    4 (r mod 8) + t.
+//  * V in token-pair rows: field f = (c mod 8) D / 8 + c / 8 holds both
+//    tokens' codes of channel c; the lanes with l mod 8 = p hold the fields
+//    of block p (channel i 32 + l at field p D / 8 + 4 i + l / 8). A token
+//    not in this call keeps its bits of the row.
 // The norms go to the group's norm arrays.
-template <int D>
+template <int D, int KB, int VB>
 __global__ void __launch_bounds__(128) tq_quantize_kernel(AppendArgs a, int64_t pair_begin, int n_pairs) {
   constexpr int NS = D / 32;
-  __shared__ uint8_t codes[4][2][2][D];  // [warp][K, V][token of the pair][channel]
+  constexpr int KSB = D / 4 * KB;           // bits of a K string
+  constexpr int KW = (KSB + 31) / 32;       // its words
+  constexpr int BBK = D * KB / 32;          // bytes of a K string (a token block of a decode lane)
+  constexpr bool KWORDS = BBK % 4 == 0;     // written as words, else as 16-bit halves
+  constexpr int VSB = D / 8 * 2 * VB;       // bits of a V block (fields of one l mod 8)
+  constexpr int VW = (VSB + 31) / 32;
+  constexpr int VBB = VSB / 8;              // its bytes
+  constexpr bool VWORDS = VBB % 4 == 0;
   __shared__ float s_bk[16], s_bv[16];
   __shared__ uint8_t s_gk[kTqCells + 1], s_gv[kTqCells + 1];
   __shared__ int s_ok[2];
   const Geometry& G = a.geo;
   if (threadIdx.x < 16) {
-    s_bk[threadIdx.x] = (threadIdx.x < (1 << G.kb) - 1) ? a.tab.cb_k[threadIdx.x] : 2.0f;
-    s_bv[threadIdx.x] = (threadIdx.x < (1 << G.vb) - 1) ? a.tab.cb_v[threadIdx.x] : 2.0f;
+    s_bk[threadIdx.x] = (threadIdx.x < (1 << KB) - 1) ? a.tab.cb_k[threadIdx.x] : 2.0f;
+    s_bv[threadIdx.x] = (threadIdx.x < (1 << VB) - 1) ? a.tab.cb_v[threadIdx.x] : 2.0f;
   }
   if (threadIdx.x < 2) s_ok[threadIdx.x] = 1;
   __syncthreads();
-  tq_guess_table(s_bk, (1 << G.kb) - 1, s_gk, &s_ok[0]);
-  tq_guess_table(s_bv, (1 << G.vb) - 1, s_gv, &s_ok[1]);
+  if (KB > 2) tq_guess_table(s_bk, (1 << KB) - 1, s_gk, &s_ok[0]);
+  if (VB > 2) tq_guess_table(s_bv, (1 << VB) - 1, s_gv, &s_ok[1]);
   __syncthreads();
-  const uint8_t* gk = s_ok[0] ? s_gk : nullptr;
-  const uint8_t* gv = s_ok[1] ? s_gv : nullptr;
+  const bool gk_ok = s_ok[0] != 0, gv_ok = s_ok[1] != 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float sg[NS];  // this lane's signs (channels i * 32 + lane)
 #pragma unroll
   for (int i = 0; i < NS; ++i) sg[i] = a.tab.signs[i * 32 + lane];
+  float bs[5];
+#pragma unroll
+  for (int k = 0; k < 5; ++k) bs[k] = (lane >> k) & 1 ? -1.0f : 1.0f;
+  const float brk[3] = {s_bk[0], s_bk[1], s_bk[2]}, brv[3] = {s_bv[0], s_bv[1], s_bv[2]};
+  const int bh = blockIdx.y;
+  const int bf16 = G.act_bf16;
+  const float rsq = static_cast<float>(1.0 / sqrt(static_cast<double>(D)));
+  const int q8 = lane >> 3, lo = lane & 1;
   // the CTA's pairs [first, first + 4 kTqPairsPerWarp), warp w taking w, w + 4, ...
   const int first = blockIdx.x * 4 * kTqPairsPerWarp;
   const int last = min(n_pairs, first + 4 * kTqPairsPerWarp);
   for (int pi_idx = first + warp; pi_idx < last; pi_idx += 4) {
-  __syncwarp();  // the previous pair's codes have been read
-  const int64_t pi = pair_begin + pi_idx;
-  const int bh = blockIdx.y;
-  const int bf16 = G.act_bf16;
-  const float rsq = static_cast<float>(1.0 / sqrt(static_cast<double>(D)));
-  const int64_t p0 = 2 * pi;
-  const int slot = static_cast<int>((p0 / kGroup) % G.n_slots);
-  uint8_t* chunk = a.lay.chunks + (static_cast<size_t>(bh) * G.n_slots + slot) * G.chunk.bytes;
-  const int kb = G.kb, vb = G.vb;
-  // both tokens' rows first (a token not in this call reads the other's
-  // row and stores nothing), so that their butterflies and searches overlap
-  bool have[2];
-  float xk[2][NS], xv[2][NS];
+    const int64_t p0 = 2 * (pair_begin + pi_idx);
+    const int slot = static_cast<int>((p0 / kGroup) % G.n_slots);
+    uint8_t* chunk = a.lay.chunks + (static_cast<size_t>(bh) * G.n_slots + slot) * G.chunk.bytes;
+    // both tokens' rows first (a token not in this call reads the other's
+    // row and stores nothing), so that their butterflies and searches overlap
+    bool have[2];
+    float xk[2][NS], xv[2][NS];
+    int64_t lp[2];
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int64_t pos = p0 + e;
-    have[e] = pos >= a.L0 && pos < a.L0 + a.n;
-    const int64_t lp = have[e] ? pos : (have[e ^ 1] ? p0 + (e ^ 1) : a.L0);
-    const size_t in_row = (static_cast<size_t>(bh) * a.n + (lp - a.L0)) * D;
+    for (int e = 0; e < 2; ++e) {
+      const int64_t pos = p0 + e;
+      have[e] = pos >= a.L0 && pos < a.L0 + a.n;
+      lp[e] = have[e] ? pos : (have[e ^ 1] ? p0 + (e ^ 1) : a.L0);
+    }
+    auto load = [&](auto bf) {
+      constexpr bool BF = decltype(bf)::value;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const size_t in_row = (static_cast<size_t>(bh) * a.n + (lp[e] - a.L0)) * D;
+#pragma unroll
+        for (int i = 0; i < NS; ++i) {
+          const uint16_t kbits = a.k[in_row + i * 32 + lane], vbits = a.v[in_row + i * 32 + lane];
+          xk[e][i] = BF ? __uint_as_float(static_cast<uint32_t>(kbits) << 16) : __half2float(__ushort_as_half(kbits));
+          xv[e][i] = BF ? __uint_as_float(static_cast<uint32_t>(vbits) << 16) : __half2float(__ushort_as_half(vbits));
+        }
+      }
+    };
+    if (bf16) load(std::true_type{});
+    else load(std::false_type{});
+    if (a.tab.rope) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float* tr = a.tab.rope + static_cast<size_t>(lp[e]) * D;
+#pragma unroll
+        for (int i = 0; i < NS / 2; ++i) {
+          const int c = i * 32 + lane;
+          float rx, ry;
+          rope_pair(xk[e][i], xk[e][i + NS / 2], tr[2 * c], tr[2 * c + 1], &rx, &ry);
+          xk[e][i] = act_to_float(float_to_act(rx, bf16), bf16);
+          xk[e][i + NS / 2] = act_to_float(float_to_act(ry, bf16), bf16);
+        }
+      }
+    }
+    float nk[2], nv[2];
+    uint32_t ck[2][NS], cv[2][NS];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      if constexpr (KB == 2) nk[e] = tq_code_row<D, KB, kTqRegs>(xk[e], sg, bs, brk, s_bk, s_gk, rsq, ck[e]);
+      else if (gk_ok) nk[e] = tq_code_row<D, KB, kTqGuess>(xk[e], sg, bs, brk, s_bk, s_gk, rsq, ck[e]);
+      else nk[e] = tq_code_row<D, KB, kTqBinary>(xk[e], sg, bs, brk, s_bk, s_gk, rsq, ck[e]);
+      if constexpr (VB == 2) nv[e] = tq_code_row<D, VB, kTqRegs>(xv[e], sg, bs, brv, s_bv, s_gv, rsq, cv[e]);
+      else if (gv_ok) nv[e] = tq_code_row<D, VB, kTqGuess>(xv[e], sg, bs, brv, s_bv, s_gv, rsq, cv[e]);
+      else nv[e] = tq_code_row<D, VB, kTqBinary>(xv[e], sg, bs, brv, s_bv, s_gv, rsq, cv[e]);
+    }
+    const int r0 = static_cast<int>(p0 % kGroup);  // the pair's first row in the group
+    if (lane < 2 && (lane ? have[1] : have[0])) {  // lane e stores token e's norms
+      reinterpret_cast<float*>(chunk + G.chunk.kmeta_off)[r0 + lane] = lane ? nk[1] : nk[0];
+      reinterpret_cast<float*>(chunk + G.chunk.vmeta_off)[r0 + lane] = lane ? nv[1] : nv[0];
+    }
+
+    // K: this lane's codes in both tokens' strings t = (lane mod 8) / 2, then
+    // the strings merged over the eight lanes of each t: lane bit 4 picks the
+    // token (the other token's words go to the partner), bits 3 and 0 merge
+    uint32_t ks[2][KW];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+#pragma unroll
+      for (int w = 0; w < KW; ++w) ks[e][w] = 0u;
+#pragma unroll
+      for (int i = 0; i < NS; ++i) {
+        const int bit0 = KB * 8 * i;  // the lane's bit is bit0 + KB (2 q8 + lo)
+        tq_place<KW>(ks[e], bit0 / 32, bit0 % 32 + KB * (2 * q8 + lo), ck[e][i], KB == 3);
+      }
+    }
+    const int ktok = (lane >> 4) & 1;
+    uint32_t kstr[KW];
+#pragma unroll
+    for (int w = 0; w < KW; ++w) {
+      const uint32_t send = ktok ? ks[0][w] : ks[1][w];
+      kstr[w] = (ktok ? ks[1][w] : ks[0][w]) | __shfl_xor_sync(0xffffffffu, send, 16);
+      kstr[w] |= __shfl_xor_sync(0xffffffffu, kstr[w], 8);
+      kstr[w] |= __shfl_xor_sync(0xffffffffu, kstr[w], 1);
+    }
+    if (ktok ? have[1] : have[0]) {
+      const int r = r0 + ktok;
+      const int t = (lane & 7) >> 1, idx = 2 * (q8 & 1) + lo;  // idx: the writer among the four lanes
+      const int L = 4 * (r & 7) + t, blk = 2 * (r >> 4) + ((r >> 3) & 1);
+      constexpr int pw = piece_words(D * KB / 32);
+      if constexpr (KWORDS) {
+        if (idx < KW)
+          *reinterpret_cast<uint32_t*>(chunk + G.chunk.kc_off + lane_byte_offset(L, blk * BBK + 4 * idx, pw)) =
+              tq_word<KW>(kstr, idx);
+      } else {
+        if (idx < BBK / 2)
+          *reinterpret_cast<uint16_t*>(chunk + G.chunk.kc_off + lane_byte_offset(L, blk * BBK + 2 * idx, pw)) =
+              static_cast<uint16_t>(tq_word<KW>(kstr, idx >> 1) >> (16 * (idx & 1)));
+      }
+    }
+
+    // V: the fields of block p = lane mod 8 (both tokens' codes), merged
+    // over the four lanes of each p (lane bits 3 and 4)
+    const uint32_t keep_lo = (have[0] ? (1u << VB) - 1u : 0u) | (have[1] ? ((1u << VB) - 1u) << VB : 0u);
+    const bool whole = have[0] && have[1];
+    uint32_t vs[VW], vm[VW];
+#pragma unroll
+    for (int w = 0; w < VW; ++w) vs[w] = vm[w] = 0u;
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
-      xk[e][i] = act_to_float(a.k[in_row + i * 32 + lane], bf16);
-      xv[e][i] = act_to_float(a.v[in_row + i * 32 + lane], bf16);
+      const int bit0 = 2 * VB * 4 * i;  // the lane's field is at bit0 + 2 VB q8
+      const uint32_t f = (cv[0][i] | (cv[1][i] << VB)) & keep_lo;
+      tq_place<VW>(vs, bit0 / 32, bit0 % 32 + 2 * VB * q8, f, VB == 3);
+      if (!whole) tq_place<VW>(vm, bit0 / 32, bit0 % 32 + 2 * VB * q8, keep_lo, VB == 3);
     }
-    if (a.tab.rope) {
-      const float* tr = a.tab.rope + static_cast<size_t>(lp) * D;
 #pragma unroll
-      for (int i = 0; i < NS / 2; ++i) {
-        const int c = i * 32 + lane;
-        float rx, ry;
-        rope_pair(xk[e][i], xk[e][i + NS / 2], tr[2 * c], tr[2 * c + 1], &rx, &ry);
-        xk[e][i] = act_to_float(float_to_act(rx, bf16), bf16);
-        xk[e][i + NS / 2] = act_to_float(float_to_act(ry, bf16), bf16);
+    for (int w = 0; w < VW; ++w) {
+      vs[w] |= __shfl_xor_sync(0xffffffffu, vs[w], 8);
+      vs[w] |= __shfl_xor_sync(0xffffffffu, vs[w], 16);
+      if (!whole) {
+        vm[w] |= __shfl_xor_sync(0xffffffffu, vm[w], 8);
+        vm[w] |= __shfl_xor_sync(0xffffffffu, vm[w], 16);
+      }
+    }
+    {
+      const int p = lane & 7, idx = q8;  // idx: the writer among the four lanes
+      uint8_t* row = chunk + G.chunk.vc_off + static_cast<size_t>(r0 / 2) * tq_vrow_bytes(D, VB) + p * VBB;
+      if constexpr (VWORDS) {
+        if (idx < VW) {
+          uint32_t* dst = reinterpret_cast<uint32_t*>(row + 4 * idx);
+          uint32_t val = tq_word<VW>(vs, idx);
+          if (!whole) {
+            const uint32_t m = tq_word<VW>(vm, idx);
+            val = (*dst & ~m) | (val & m);
+          }
+          *dst = val;
+        }
+      } else {
+        if (idx < VBB / 2) {
+          uint16_t* dst = reinterpret_cast<uint16_t*>(row + 2 * idx);
+          uint32_t val = tq_word<VW>(vs, idx >> 1) >> (16 * (idx & 1));
+          if (!whole) {
+            const uint32_t m = tq_word<VW>(vm, idx >> 1) >> (16 * (idx & 1));
+            val = (*dst & ~m) | (val & m);
+          }
+          *dst = static_cast<uint16_t>(val);
+        }
       }
     }
   }
-  float nk[2], nv[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    nk[e] = tq_code_row<D>(xk[e], sg, s_bk, gk, kb, rsq, codes[warp][0][e]);
-    nv[e] = tq_code_row<D>(xv[e], sg, s_bv, gv, vb, rsq, codes[warp][1][e]);
+}
+
+template <int D, int KB>
+void launch_tq_kb(const AppendArgs& a, dim3 grid, cudaStream_t s, int64_t pair_begin, int n_pairs) {
+  switch (a.geo.vb) {
+    case 2: tq_quantize_kernel<D, KB, 2><<<grid, 128, 0, s>>>(a, pair_begin, n_pairs); break;
+    case 3: tq_quantize_kernel<D, KB, 3><<<grid, 128, 0, s>>>(a, pair_begin, n_pairs); break;
+    default: tq_quantize_kernel<D, KB, 4><<<grid, 128, 0, s>>>(a, pair_begin, n_pairs); break;
   }
-  __syncwarp();
-  for (int e = 0; e < 2; ++e) {
-    if (!have[e]) continue;
-    const int r = static_cast<int>((p0 + e) % kGroup);
-    if (lane == 0) {
-      reinterpret_cast<float*>(chunk + G.chunk.kmeta_off)[r] = nk[e];
-      reinterpret_cast<float*>(chunk + G.chunk.vmeta_off)[r] = nv[e];
-    }
-    // K: block b = 2 (r / 16) + (r / 8) % 2 of lanes 4 (r % 8) + t; lane
-    // 2 BBK / 2 ... writes 16-bit half h of the block of lane t
-    const int bbk = D * kb / 32;  // bytes per token block
-    const int pw = piece_words(D * kb / 32);
-    const int blk = 2 * (r >> 4) + ((r >> 3) & 1);
-    if (lane < 2 * bbk) {
-      const int t = lane / (bbk / 2), hw = lane % (bbk / 2);
-      uint32_t half = 0;
-      for (int j = (16 * hw) / (2 * kb); j * 2 * kb < 16 * hw + 16; ++j) {  // the fields that meet this half
-        const int c0 = 16 * (j >> 1) + 2 * t + 8 * (j & 1);
-        const uint32_t f = codes[warp][0][e][c0] | (static_cast<uint32_t>(codes[warp][0][e][c0 + 1]) << kb);
-        const int sh = 2 * kb * j - 16 * hw;
-        half |= sh >= 0 ? (f << sh) : (f >> -sh);
-      }
-      half &= 0xffffu;
-      const int L = 4 * (r & 7) + t;
-      *reinterpret_cast<uint16_t*>(chunk + G.chunk.kc_off + lane_byte_offset(L, blk * bbk + 2 * hw, pw)) =
-          static_cast<uint16_t>(half);
-    }
-  }
-  // V: the pair row, 16-bit halves; a token not in this call keeps its bits
-  const int rb = tq_vrow_bytes(D, vb);
-  uint16_t* row = reinterpret_cast<uint16_t*>(chunk + G.chunk.vc_off + static_cast<size_t>((p0 % kGroup) / 2) * rb);
-  const uint32_t lo_mask = (1u << vb) - 1u;
-  const uint32_t keep = (have[0] ? lo_mask : 0u) | (have[1] ? lo_mask << vb : 0u);  // bits of a field written here
-  for (int hw = lane; hw < rb / 2; hw += 32) {
-    uint32_t half = 0, mask = 0;
-    for (int f = (16 * hw) / (2 * vb); f * 2 * vb < 16 * hw + 16; ++f) {  // the fields that meet this half
-      const int c = 8 * (f % (D / 8)) + f / (D / 8);  // the channel of field position f
-      const uint32_t v = (have[0] ? codes[warp][1][0][c] : 0u) | (have[1] ? static_cast<uint32_t>(codes[warp][1][1][c]) << vb : 0u);
-      const int sh = 2 * vb * f - 16 * hw;
-      half |= sh >= 0 ? (v << sh) : (v >> -sh);
-      mask |= sh >= 0 ? (keep << sh) : (keep >> -sh);
-    }
-    mask &= 0xffffu;
-    if (mask != 0xffffu) half = (row[hw] & ~mask) | (half & mask);
-    row[hw] = static_cast<uint16_t>(half);
-  }
+}
+
+template <int D>
+void launch_tq(const AppendArgs& a, dim3 grid, cudaStream_t s, int64_t pair_begin, int n_pairs) {
+  switch (a.geo.kb) {
+    case 2: launch_tq_kb<D, 2>(a, grid, s, pair_begin, n_pairs); break;
+    case 3: launch_tq_kb<D, 3>(a, grid, s, pair_begin, n_pairs); break;
+    default: launch_tq_kb<D, 4>(a, grid, s, pair_begin, n_pairs); break;
   }
 }
 
@@ -321,8 +452,8 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s, int64_t* launches
     const int64_t pair_begin = a.L0 / 2, pair_end = (a.L0 + a.n + 1) / 2;
     const int n_pairs = static_cast<int>(pair_end - pair_begin);
     dim3 grid((n_pairs + 4 * kTqPairsPerWarp - 1) / (4 * kTqPairsPerWarp), BH);
-    if (G.D == 128) tq_quantize_kernel<128><<<grid, 128, 0, s>>>(a, pair_begin, n_pairs);
-    else tq_quantize_kernel<64><<<grid, 128, 0, s>>>(a, pair_begin, n_pairs);
+    if (G.D == 128) launch_tq<128>(a, grid, s, pair_begin, n_pairs);
+    else launch_tq<64>(a, grid, s, pair_begin, n_pairs);
     ++*launches;
   }
   // rows [r0, r1) of the append that go to the sink buffer or the tail: the

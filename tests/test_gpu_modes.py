@@ -135,6 +135,35 @@ def test_turboquant_zero_rows():
     _decode_both(gc, oc, 0, W.queries(w, 2), "f16")
 
 
+@pytest.mark.parametrize("D", [128, 64])
+@pytest.mark.parametrize("kb,vb", [(4, 2), (3, 3), (2, 4)])
+def test_turboquant_one_hot_rotations(kb, vb, D):
+    """Rows that the rotation sends to one coordinate: x = a signs * H_r (a
+    row of the Sylvester-Hadamard matrix), so y = a d e_r and u = y / n is
+    +-1 up to rounding; w = (u + 1) / 2 sits at or just past 0 and 1, where
+    the code is 0 or the top level. Mixed with ordinary rows; codes, norms
+    and attention match the oracle."""
+    w = W.scaled(W.WORKLOADS["turboquant_k4v2"], batch=2, n_kv_heads=2, n_q_heads=8, head_dim=D,
+                 k_bits=kb, v_bits=vb)
+    gc, oc = _pair(cache_kwargs(w, 512, seed=31))
+    sgn = gc.export(0, "tq_signs").astype(np.float32)
+    rng = np.random.default_rng(5)
+    j = np.arange(D)
+    k, v = W.kv_tokens(w, 12, 96)
+    amps = np.array([1.0, 0.375, 0.8125, 0.0625], np.float32)  # the unit scale the tolerances assume
+    for x in (k, v):
+        for b in range(2):
+            for h in range(2):
+                for t in rng.choice(96, size=40, replace=False):
+                    r = int(rng.integers(D))
+                    hrow = np.array([1.0 if bin(r & c).count("1") % 2 == 0 else -1.0 for c in j], np.float32)
+                    x[b, h, t] = rng.choice(amps) * rng.choice([-1.0, 1.0]) * sgn * hrow
+    gc.prefill_quantize(0, torch_act(k, "f16"), torch_act(v, "f16"))
+    oc.prefill_quantize(0, k, v)
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 12), "f16")
+
+
 # ------------------------------------------------------------------ KVSink
 
 @pytest.mark.parametrize("T", [4096, 1000, 37])
