@@ -46,6 +46,8 @@
 // that every other wait of the CTA gives up at once.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_common.cuh"
 
 namespace kvq {
@@ -179,6 +181,11 @@ constexpr float kLazyRescale = KVQ_LAZY_RESCALE;
 #ifndef KVQ_DECODE_MIN_CTAS
 #define KVQ_DECODE_MIN_CTAS (8 / KVQ_DECODE_PAIRS)
 #endif
+// TurboQuant: one CTA per SM of KVQ_TQ_PAIRS warp pairs, so that one copy of
+// the 64 KB byte tables serves sixteen warps.
+#ifndef KVQ_TQ_PAIRS
+#define KVQ_TQ_PAIRS 8
+#endif
 
 template <int D, int KB, int VB, bool TQ = false, bool PR = false>
 struct KiviTile {
@@ -189,7 +196,8 @@ struct KiviTile {
   static constexpr int VC = KMETA + (TQ ? 4 * 32 : 4 * D);
   static constexpr int VMETA = VC + 32 * D * VB / 8;
   static constexpr int CHUNK = VMETA + (TQ ? 4 * 32 : 4 * D);
-  static constexpr int NP = KVQ_DECODE_PAIRS;           // warp pairs per CTA
+  static constexpr int NP = TQ ? KVQ_TQ_PAIRS : KVQ_DECODE_PAIRS;  // warp pairs per CTA
+  static constexpr int MIN_CTAS = TQ ? 8 / KVQ_TQ_PAIRS : KVQ_DECODE_MIN_CTAS;
   // groups per stage: a pair takes runs of GPB consecutive groups, so the
   // waits, hand-off and rescale decision are paid once per run (KIVI chunks
   // up to 6 KB); one for TurboQuant, whose tables leave less shared memory,
@@ -199,42 +207,48 @@ struct KiviTile {
   static constexpr int PBUF = GPB * 32 * 8 + 16;         // weights (4 f16, 8 B per lane per group) + 4 rescale factors
   static constexpr int RED_FLOATS = NP * kMaxGqa * (D + 2);  // one merged state per pair
   // TurboQuant codebook tables: a field (two codes, low | high << bits) ->
-  // f16x2 of their values 2 c[code] - 1, in NLUT interleaved copies (entry e
-  // of copy cp at e NLUT + cp, lane % NLUT picks the copy): with 32 copies
-  // every lane reads its own bank
-  static constexpr int lut_bytes(int bits, int nlut) { return TQ ? (1 << (2 * bits)) * nlut * 4 : 0; }
-  static constexpr int smem_for(int nst, int nlut) {
-    return NP * nst * STAGE + NP * 2 * PBUF + (D / 16) * 32 * 16 + (TQ ? kMaxGqa * D * 4 : 0) +
-           lut_bytes(KB, nlut) + lut_bytes(VB, nlut) + RED_FLOATS * 4 + NP * (nst + 4) * 8 + 16;
+  // f16x2 of their values 2 c[code] - 1, in NLUT = 32 interleaved copies,
+  // lane l reading copy l (its own bank). 4-bit K codes are read by the
+  // byte that holds their field: 256 blocks of 256 B, entry e of copy cp
+  // at 256 e + 4 cp, so the address is the byte in bits 8..15 and the copy
+  // offset in bits 0..7, one byte permute. Every other field (V, and K of 2
+  // and 3 bits) is shifted to its scaled offset in a table of 2^(2 bits)
+  // entries, entry e of copy cp at 4 (e NLUT + cp). (Byte lookups of the V
+  // fields, 64 bits wide for 2-bit pairs, were measured slower.)
+  static constexpr bool KBYTE = TQ && KB == 4;
+  static constexpr int NLUT = 32;
+  static constexpr int shift_lut_bytes(int bits) { return TQ ? (1 << (2 * bits)) * NLUT * 4 : 0; }
+  static constexpr int LUTK = KBYTE ? 256 * 256 : shift_lut_bytes(KB), LUTV = shift_lut_bytes(VB);
+  static constexpr int smem_for(int nst) {
+    return NP * nst * STAGE + NP * 2 * PBUF + (D / 16) * 32 * 16 + (TQ ? kMaxGqa * D * 4 : 0) + LUTK + LUTV +
+           RED_FLOATS * 4 + NP * (nst + 4) * 8 + 16;
   }
-  // what one of two CTAs may take of an SM's 228 KB (1 KB of each CTA's
-  // share is reserved by the hardware)
-  static constexpr int kTwoCtaSmem = 228 * 1024 / 2 - 1024;
-  // bulk-copy stages per pair: three where they leave room for two CTAs per
-  // SM (runs of two groups up to 4 KB each; single groups), else two; the
-  // tables keep 32 copies unless even two stages leave no room for them
-  static constexpr int NLUT = (!TQ || smem_for(2, 32) <= kTwoCtaSmem) ? 32 : 16;
+  // what one of MIN_CTAS CTAs may take of an SM's 228 KB (1 KB of each
+  // CTA's share is reserved by the hardware)
+  static constexpr int kCtaSmem = 228 * 1024 / MIN_CTAS - 1024;
+  // bulk-copy stages per pair: three where they leave room for MIN_CTAS CTAs
+  // per SM (runs of two groups up to 4 KB each; single groups), else two
 #ifndef KVQ_DECODE_STAGES
-  static constexpr int NST = smem_for(3, NLUT) <= kTwoCtaSmem ? 3 : 2;
+  static constexpr int NST = smem_for(3) <= kCtaSmem ? 3 : 2;
 #else
   static constexpr int NST = KVQ_DECODE_STAGES;
 #endif
-  static constexpr int LUTK = lut_bytes(KB, NLUT);
-  static constexpr int LUTV = lut_bytes(VB, NLUT);
   // shared memory: stages | weight buffers | query operand | query scratch |
   // tables | red | barriers | abort flag
   static constexpr int OFF_PBUF = NP * NST * STAGE;
   static constexpr int OFF_Q = OFF_PBUF + NP * 2 * PBUF;  // [D/16 k-steps][32 lanes] x 16 B
   static constexpr int OFF_QF = OFF_Q + (D / 16) * 32 * 16;  // TurboQuant: rotated queries [kMaxGqa][D] f32
-  static constexpr int OFF_LUT = OFF_QF + (TQ ? kMaxGqa * D * 4 : 0);
-  static constexpr int OFF_RED = OFF_LUT + LUTK + LUTV;
+  static constexpr int OFF_LUTK = OFF_QF + (TQ ? kMaxGqa * D * 4 : 0);
+  static constexpr int OFF_LUTV = OFF_LUTK + LUTK;
+  static constexpr int OFF_RED = OFF_LUTV + LUTV;
   static constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
   static constexpr int NBAR = NP * (NST + 4);             // full[NST], pfull[2], pempty[2]
   static constexpr int OFF_ABORT = OFF_BAR + NBAR * 8;
   static constexpr size_t smem_bytes() { return OFF_ABORT + 16; }
-  static_assert(smem_bytes() == static_cast<size_t>(smem_for(NST, NLUT)), "layout and its size agree");
+  static_assert(smem_bytes() == static_cast<size_t>(smem_for(NST)), "layout and its size agree");
+  static_assert(OFF_LUTK % 16 == 0, "tables 16-byte aligned");
   static_assert(OFF_BAR % 8 == 0, "mbarriers are 8-byte aligned");
-  static_assert(!TQ || smem_bytes() <= static_cast<size_t>(kTwoCtaSmem), "two CTAs per SM");
+  static_assert(!TQ || smem_bytes() <= static_cast<size_t>(kCtaSmem), "MIN_CTAS CTAs per SM");
 };
 
 // CTA that owns flattened item i under the equal split of `work` items into
@@ -298,6 +312,17 @@ __device__ __forceinline__ uint32_t table_entry(const uint32_t* table, const uin
   if (sh + 2 * BITS <= 32) x = sh >= SH ? (w[wi] >> (sh - SH)) : (w[wi] << (SH - sh));
   else x = __funnelshift_r(w[wi], w[wi + 1], sh - SH);  // sh > 32 - 2 BITS >= SH here
   return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(table) + ((x & M) | cp4));
+}
+
+// Offset of byte k of a lane's code words w inside a byte table: the byte
+// in bits 8..15, the lane's copy offset cpo (< 256) in bits 0..7, by one
+// byte permute.
+__device__ __forceinline__ uint32_t byte_offset(const uint32_t* w, int k, uint32_t cpo) {
+  return __byte_perm(w[k >> 2], cpo, 0x6504u | (static_cast<uint32_t>(k & 3) << 4));
+}
+// The f16x2 of the field (4-bit codes: a whole byte) in byte k.
+__device__ __forceinline__ uint32_t byte_entry(const uint8_t* table, const uint32_t* w, int k, uint32_t cpo) {
+  return *reinterpret_cast<const uint32_t*>(table + byte_offset(w, k, cpo));
 }
 
 // Walks the runs of pair p inside its CTA's range [i0, i1): per unit (run of
@@ -364,7 +389,8 @@ struct RunCursor {
 // dequantises each key, rotates it at its position and scores it in two
 // MMAs (f16 value and residual of the rotated key).
 template <int D, int KB, int VB, bool TQ, bool QX, bool PR = false>
-__global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) decode_kivi_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(64 * KiviTile<D, KB, VB, TQ, PR>::NP, KiviTile<D, KB, VB, TQ, PR>::MIN_CTAS)
+    decode_kivi_kernel(DecodeArgs a) {
   using T = KiviTile<D, KB, VB, TQ, PR>;
   constexpr int NP = T::NP, NST = T::NST, CHUNK = T::CHUNK;
   constexpr int S = D / 16, MV = D / 16, NVG = D / 32;
@@ -399,20 +425,26 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
     for (int i = 0; i < 4; ++i) mbar_init(&pfull[i], 32);
     mbar_fence_init();
   }
-  uint32_t* lut_k = reinterpret_cast<uint32_t*>(smem + T::OFF_LUT);
-  uint32_t* lut_v = reinterpret_cast<uint32_t*>(smem + T::OFF_LUT + T::LUTK);
+  uint8_t* lut_k = smem + T::OFF_LUTK;
+  uint8_t* lut_v = smem + T::OFF_LUTV;
   if constexpr (TQ) {  // value of code c: 2 c[c] - 1 (Foundry TurboQuant spec, "Algorithm Detail")
     // a field is (low code | high code << bits); the codebooks have 2^bits levels
-    const int nk = 1 << KB, nv = 1 << VB, lk = nk, lv = nv;
-    auto level = [](const float* cb, int l, int c) { return 2.0f * cb[l - 1 + c] - 1.0f; };
-    for (int i = threadIdx.x; i < (1 << (2 * KB)) * T::NLUT; i += blockDim.x) {
-      const int e = i / T::NLUT;
-      lut_k[i] = f2_to_h2(level(a.tab.cb_k, lk, e & (nk - 1)), level(a.tab.cb_k, lk, e >> KB));
-    }
-    for (int i = threadIdx.x; i < (1 << (2 * VB)) * T::NLUT; i += blockDim.x) {
-      const int e = i / T::NLUT;
-      lut_v[i] = f2_to_h2(level(a.tab.cb_v, lv, e & (nv - 1)), level(a.tab.cb_v, lv, e >> VB));
-    }
+    auto field = [](const float* cb, int bits, int f) {
+      const int n = 1 << bits;
+      return f2_to_h2(2.0f * cb[n - 1 + (f & (n - 1))] - 1.0f, 2.0f * cb[n - 1 + (f >> bits)] - 1.0f);
+    };
+    auto build = [&](uint8_t* lut, const float* cb, auto bits_c, auto byte_c) {
+      constexpr int BITS = decltype(bits_c)::value;
+      if constexpr (decltype(byte_c)::value) {  // byte e = one field: 32 copies of 4 B in a 256-B block
+        for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x)
+          *reinterpret_cast<uint32_t*>(lut + (i >> 5) * 256 + (i & 31) * 4) = field(cb, BITS, i >> 5);
+      } else {  // fields of 2 BITS bits: 2^(2 BITS) entries in NLUT copies
+        for (int i = threadIdx.x; i < (1 << (2 * BITS)) * T::NLUT; i += blockDim.x)
+          reinterpret_cast<uint32_t*>(lut)[i] = field(cb, BITS, i / T::NLUT);
+      }
+    };
+    build(lut_k, a.tab.cb_k, std::integral_constant<int, KB>{}, std::bool_constant<T::KBYTE>{});
+    build(lut_v, a.tab.cb_v, std::integral_constant<int, VB>{}, std::false_type{});
   }
   __syncthreads();
 
@@ -570,17 +602,27 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           uint32_t kw[KWT + 1];
           load_lane_words<KWT, PWT>(tile, lane, kw);
           kw[KWT] = 0u;
-          const uint32_t cp4 = 4u * static_cast<uint32_t>(lane % T::NLUT);
+          const uint32_t cpk = 4u * (lane % T::NLUT);
           float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
           for (int s = 0; s < S; ++s) {  // one read of the query operand per k-step serves both m-tiles
             const uint4 q4 = qsm[s * 32 + lane];
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
-              const uint32_t a0 = table_entry<KB, T::NLUT>(lut_k, kw, tq_kfield_bit(D, KB, 2 * mt, 2 * s), cp4);
-              const uint32_t a1 = table_entry<KB, T::NLUT>(lut_k, kw, tq_kfield_bit(D, KB, 2 * mt + 1, 2 * s), cp4);
-              const uint32_t a2 = table_entry<KB, T::NLUT>(lut_k, kw, tq_kfield_bit(D, KB, 2 * mt, 2 * s + 1), cp4);
-              const uint32_t a3 = table_entry<KB, T::NLUT>(lut_k, kw, tq_kfield_bit(D, KB, 2 * mt + 1, 2 * s + 1), cp4);
+              // field (b, j) of the lane's string is at bit (b D / 8 + j) 2 KB
+              uint32_t a0, a1, a2, a3;
+              if constexpr (T::KBYTE) {  // one byte per field
+                a0 = byte_entry(lut_k, kw, 2 * mt * (D / 8) + 2 * s, cpk);
+                a1 = byte_entry(lut_k, kw, (2 * mt + 1) * (D / 8) + 2 * s, cpk);
+                a2 = byte_entry(lut_k, kw, 2 * mt * (D / 8) + 2 * s + 1, cpk);
+                a3 = byte_entry(lut_k, kw, (2 * mt + 1) * (D / 8) + 2 * s + 1, cpk);
+              } else {
+                const uint32_t* lk = reinterpret_cast<const uint32_t*>(lut_k);
+                a0 = table_entry<KB, T::NLUT>(lk, kw, tq_kfield_bit(D, KB, 2 * mt, 2 * s), cpk);
+                a1 = table_entry<KB, T::NLUT>(lk, kw, tq_kfield_bit(D, KB, 2 * mt + 1, 2 * s), cpk);
+                a2 = table_entry<KB, T::NLUT>(lk, kw, tq_kfield_bit(D, KB, 2 * mt, 2 * s + 1), cpk);
+                a3 = table_entry<KB, T::NLUT>(lk, kw, tq_kfield_bit(D, KB, 2 * mt + 1, 2 * s + 1), cpk);
+              }
               mma_f16(acc[mt], a0, a1, a2, a3, q4.y, q4.w);
             }
           }
@@ -883,7 +925,7 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
           // its A pairs (channel, two tokens); the lane's copy of the table
           // turns them into f16x2
           constexpr int RB = tq_vrow_bytes(D, VB), BB = D * VB / 32, BW = (BB + 3) / 4;
-          const uint32_t cp4 = 4u * static_cast<uint32_t>(lane % T::NLUT);
+          const uint32_t cpv = 4u * (lane % T::NLUT);
           const uint8_t* vrows = tile + T::VC;
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
@@ -909,9 +951,11 @@ __global__ void __launch_bounds__(64 * KVQ_DECODE_PAIRS, KVQ_DECODE_MIN_CTAS) de
                 bw[1] = h16[2];
               }
               bw[BW] = 0u;
+              // field jj of the block is at bit 2 VB jj
 #pragma unroll
               for (int jj = 0; jj < 2 * MV; ++jj)
-                A[jj >> 1][2 * hh + (jj & 1)] = table_entry<VB, T::NLUT>(lut_v, bw, 2 * VB * jj, cp4);
+                A[jj >> 1][2 * hh + (jj & 1)] =
+                    table_entry<VB, T::NLUT>(reinterpret_cast<const uint32_t*>(lut_v), bw, 2 * VB * jj, cpv);
             }
 #pragma unroll
             for (int m = 0; m < MV; ++m) mma_f16(oacc[m], A[m][0], A[m][1], A[m][2], A[m][3], b0, b1);
