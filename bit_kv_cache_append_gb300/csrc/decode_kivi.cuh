@@ -931,11 +931,9 @@ __global__ void __launch_bounds__(64 * KiviTile<D, KB, VB, TQ, PR>::NP, KiviTile
           for (int kb = 0; kb < 2; ++kb) {
             const uint32_t b0 = movmatrix_t(ph[2 * kb]);
             const uint32_t b1 = movmatrix_t(ph[2 * kb + 1]);
-            uint32_t A[MV][4];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+            // the words of block hh (pair row 8 kb + t + 4 hh, block g)
+            auto load_block = [&](int hh, uint32_t (&bw)[BW + 1]) {
               const uint8_t* blk = vrows + (8 * kb + t + 4 * hh) * RB + g * BB;
-              uint32_t bw[BW + 1];
               if constexpr (BB % 16 == 0) {
                 const uint4 v = *reinterpret_cast<const uint4*>(blk);
                 bw[0] = v.x, bw[1] = v.y, bw[2] = v.z, bw[3] = v.w;
@@ -951,14 +949,31 @@ __global__ void __launch_bounds__(64 * KiviTile<D, KB, VB, TQ, PR>::NP, KiviTile
                 bw[1] = h16[2];
               }
               bw[BW] = 0u;
-              // field jj of the block is at bit 2 VB jj
+            };
+            const uint32_t* lv = reinterpret_cast<const uint32_t*>(lut_v);
+            if constexpr (VB == 4) {
+              uint32_t bw[2][BW + 1];
+              load_block(0, bw[0]);
+              load_block(1, bw[1]);
 #pragma unroll
-              for (int jj = 0; jj < 2 * MV; ++jj)
-                A[jj >> 1][2 * hh + (jj & 1)] =
-                    table_entry<VB, T::NLUT>(reinterpret_cast<const uint32_t*>(lut_v), bw, 2 * VB * jj, cpv);
+              for (int m = 0; m < MV; ++m)
+                mma_f16(oacc[m], table_entry<VB, T::NLUT>(lv, bw[0], 4 * VB * m, cpv),
+                        table_entry<VB, T::NLUT>(lv, bw[0], 4 * VB * m + 2 * VB, cpv),
+                        table_entry<VB, T::NLUT>(lv, bw[1], 4 * VB * m, cpv),
+                        table_entry<VB, T::NLUT>(lv, bw[1], 4 * VB * m + 2 * VB, cpv), b0, b1);
+            } else {
+              uint32_t A[MV][4];
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                uint32_t bw[BW + 1];
+                load_block(hh, bw);
+#pragma unroll
+                for (int jj = 0; jj < 2 * MV; ++jj)
+                  A[jj >> 1][2 * hh + (jj & 1)] = table_entry<VB, T::NLUT>(lv, bw, 2 * VB * jj, cpv);
+              }
+#pragma unroll
+              for (int m = 0; m < MV; ++m) mma_f16(oacc[m], A[m][0], A[m][1], A[m][2], A[m][3], b0, b1);
             }
-#pragma unroll
-            for (int m = 0; m < MV; ++m) mma_f16(oacc[m], A[m][0], A[m][1], A[m][2], A[m][3], b0, b1);
           }
         } else {
         // the weights as the B operand (column g, token pairs 2t + 8 kk,
