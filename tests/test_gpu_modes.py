@@ -135,6 +135,33 @@ def test_turboquant_zero_rows():
     _decode_both(gc, oc, 0, W.queries(w, 2), "f16")
 
 
+@pytest.mark.parametrize("kb,vb,act", [(4, 2, "f16"), (3, 3, "bf16"), (2, 4, "bf16")])
+@pytest.mark.parametrize("D", [128, 64])
+def test_turboquant_rope_at_append(kb, vb, act, D):
+    """TurboQuant with the cache applying RoPE: each key is rotated at its
+    absolute position and rounded back to the activation dtype before the
+    Walsh-Hadamard rotation and coding (posttrainllm "RoPE caveat"), the
+    query at L - 1 before its own rotation; a prefill of 600 tokens, then
+    appends of mixed sizes that start and end inside token pairs. Codes and
+    norms bit-exact, attention within tolerance."""
+    w = W.scaled(W.WORKLOADS["turboquant_k4v2"], batch=2, n_kv_heads=2, n_q_heads=8, head_dim=D,
+                 k_bits=kb, v_bits=vb, act_dtype=act, rope_base=10000.0)
+    gc, oc = _pair(cache_kwargs(w, 1024, seed=91, rope_max_pos=1024))
+    k, v = W.kv_tokens(w, 15, 600)
+    gc.prefill_quantize(0, torch_act(k, act), torch_act(v, act))
+    oc.prefill_quantize(0, k, v)
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 15, 0), act)
+    pos = 600
+    for i, n in enumerate([1, 3, 31, 1, 32, 7]):
+        k, v = W.kv_tokens(w, 15, n, first_pos=pos)
+        gc.append(0, torch_act(k, act), torch_act(v, act))
+        oc.append(0, k, v)
+        pos += n
+    compare_exports(gc, oc, 0)
+    _decode_both(gc, oc, 0, W.queries(w, 15, 7), act)
+
+
 @pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("kb,vb", [(4, 2), (3, 3), (2, 4)])
 def test_turboquant_one_hot_rotations(kb, vb, D):

@@ -187,3 +187,14 @@ def test_rotated_domain_dot_equals_original():
     a = np.sum(q.astype(np.float64) * tq.unrotate(yh, sgn), 1)
     b = np.sum(tq.rotate(q, sgn).astype(np.float64) * yh, 1)
     assert np.allclose(a, b, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_codebook_boundaries_farther_apart_than_guess_cells(d, bits):
+    """The quantiser's code search guesses from cells of width 1/256 in w and
+    falls back to a binary search only where a cell holds two boundaries;
+    the Beta codebooks of every supported width and head_dim keep their
+    boundaries more than a cell apart, so the guess path is the one taken."""
+    bnd, _ = T.codebook(d, bits)
+    assert np.all(np.diff(bnd.astype(np.float64)) > 1.0 / 256)
