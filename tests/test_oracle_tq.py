@@ -196,5 +196,5 @@ def test_codebook_boundaries_farther_apart_than_guess_cells(d, bits):
     falls back to a binary search only where a cell holds two boundaries;
     the Beta codebooks of every supported width and head_dim keep their
     boundaries more than a cell apart, so the guess path is the one taken."""
-    bnd, _ = T.codebook(d, bits)
+    bnd, _ = tq.codebook(d, bits)
     assert np.all(np.diff(bnd.astype(np.float64)) > 1.0 / 256)
