@@ -1,13 +1,14 @@
-// Split-KV decode attention over the KIVI cache (internal template; the
-// instantiations live in decode_d64.cu and decode_d128.cu).
+// Split-KV decode attention over the KIVI and TurboQuant caches (internal
+// template; the instantiations live in decode_d{64,128}_{k2,k3,k4,k8,tq}.cu).
 //
 // Work decomposition (stream-K): the quantised segment of every (sequence,
 // KV head) unit is a run of 32-token groups; all units' groups form one flat
 // list cut into n_ctas equal contiguous ranges, one per persistent CTA
 // (n_ctas = SM count x resident CTAs). A CTA walks its range unit by unit;
-// for each unit it touches, its 4 warp pairs take the unit's groups in runs
-// of two consecutive groups (runs p, p+4, ...; one group per run where a
-// chunk exceeds 6 KB) and the CTA merges the pairs into one partial (max,
+// for each unit it touches, its NP warp pairs (4, two CTAs per SM; in
+// TurboQuant mode 8, one CTA per SM) take the unit's groups in runs of two
+// consecutive groups (runs p, p+NP, ...; one group per run for TurboQuant
+// and where a chunk exceeds 6 KB) and the CTA merges the pairs into one partial (max,
 // sum, unnormalised output) per query head. The exact pools (sinks and tail)
 // are left to the merge kernel, which combines them with every partial of a
 // (sequence, query head).
@@ -19,7 +20,7 @@
 // turns the V codes into the weighted sum and, being the last reader of each
 // staged run, refills the stage with the next run (one 1-D bulk copy when
 // its chunks are adjacent in the ring); three stages per pair where they
-// leave room for two CTAs per SM, else two. Each role keeps only its own
+// leave room for the CTAs per SM, else two. Each role keeps only its own
 // operands in registers, so more warps fit per SM and the two halves of a
 // group's dependency chain overlap across groups.
 //
