@@ -51,16 +51,17 @@ __global__ void tail_write_kernel(AppendArgs a, int row_begin, int n_rows) {
 // the codebook boundaries and the warp's signs, is paid once for them).
 constexpr int kTqPairsPerWarp = 8;
 // The code search's guess table: w in [0, 1] falls in cell floor(kTqCells w)
-// (kTqCells + 1 cells with w = 1); the cell's entry is the number of
-// boundaries <= its start, valid while no cell holds two boundaries.
+// (kTqCells + 1 cells with w = 1); the cell's entry is the number g of
+// boundaries <= its start and the boundary g (the next one up, or the
+// padding above every w), valid while no cell holds two boundaries.
 constexpr int kTqCells = 256;
 constexpr float kMagicF = 12582912.0f;  // 1.5 * 2^23: x + kMagicF keeps floor / rint(x) in the low bits
 constexpr uint32_t kMagicBitsF = 0x4B400000u;
 
-// Builds the guess table of nb ascending boundaries (threads of the CTA in
-// turn); returns, through ok (shared, set to 1 before), whether every cell
-// holds at most one boundary.
-__device__ __forceinline__ void tq_guess_table(const float* bnd, int nb, uint8_t* guess, int* ok) {
+// Builds the guess table of nb ascending boundaries, padded with 2.0 (threads
+// of the CTA in turn): entry (bits of boundary g, g); returns, through ok
+// (shared, set to 1 before), whether every cell holds at most one boundary.
+__device__ __forceinline__ void tq_guess_table(const float* bnd, int nb, uint2* guess, int* ok) {
   for (int j = threadIdx.x; j <= kTqCells; j += blockDim.x) {
     const float lo = static_cast<float>(j) / kTqCells, hi = static_cast<float>(j + 1) / kTqCells;
     int below = 0, inside = 0;
@@ -68,7 +69,7 @@ __device__ __forceinline__ void tq_guess_table(const float* bnd, int nb, uint8_t
       below += bnd[k] <= lo ? 1 : 0;
       inside += (bnd[k] > lo && bnd[k] < hi) ? 1 : 0;
     }
-    guess[j] = static_cast<uint8_t>(below);
+    guess[j] = make_uint2(__float_as_uint(bnd[below]), static_cast<uint32_t>(below));
     if (inside > 1) *ok = 0;
   }
 }
@@ -87,10 +88,9 @@ enum TqSearch { kTqRegs = 0, kTqGuess = 1, kTqBinary = 2 };
 // lanes that take the upper end of a butterfly of length 2^k, else +1.
 template <int D, int BITS, int SEARCH>
 __device__ __forceinline__ float tq_code_row(const float (&x)[D / 32], const float (&sg)[D / 32], const float (&bs)[5],
-                                             const float (&br)[3], const float* bnd, const uint8_t* guess, float rsq,
+                                             const float (&br)[3], const float* bnd, const uint2* guess, float rsq,
                                              uint32_t (&code)[D / 32]) {
   constexpr int NS = D / 32;
-  const int lane = threadIdx.x & 31;
   float y[NS], sq[NS];
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
@@ -123,13 +123,13 @@ __device__ __forceinline__ float tq_code_row(const float (&x)[D / 32], const flo
 #pragma unroll
     for (int i = 0; i < sl; ++i) sq[i] = __fadd_rn(sq[i], sq[i + sl]);
   }
+  // the tree's cross-lane levels as xor butterflies: lanes l and l ^ st add
+  // the same two partial sums (in either order: addition commutes), so
+  // every lane ends with the tree's root
   float acc = sq[0];
 #pragma unroll
-  for (int st = 16; st >= 1; st >>= 1) {
-    const float o = __shfl_down_sync(0xffffffffu, acc, st);
-    if (lane < st) acc = __fadd_rn(acc, o);
-  }
-  const float n = __shfl_sync(0xffffffffu, __fsqrt_rn(acc), 0);
+  for (int st = 16; st >= 1; st >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, st));
+  const float n = __fsqrt_rn(acc);
   // u = RN(y / n) by Markstein's correction step from RN(1 / n) (P.
   // Markstein, IBM J. Res. Dev. 34(1), 1990), exact like the division; a
   // zero norm takes 1/n = 0, which gives u = 0
@@ -151,8 +151,8 @@ __device__ __forceinline__ float tq_code_row(const float (&x)[D / 32], const flo
       // right from cell 0 (guess 0) or cell kTqCells (every boundary but the
       // padding below it)
       const float t = __fmaf_rd(__saturatef(w), static_cast<float>(kTqCells), kMagicF);
-      const uint32_t g = guess[__float_as_uint(t) - kMagicBitsF];
-      c = g + (w >= bnd[g] ? 1u : 0u);
+      const uint2 cell = guess[__float_as_uint(t) - kMagicBitsF];
+      c = cell.y + (w >= __uint_as_float(cell.x) ? 1u : 0u);
     } else {  // boundaries padded to 16 with 2.0, above every w
       c = 0;
 #pragma unroll
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(128) tq_quantize_kernel(AppendArgs a, int64_t 
   constexpr int VBB = VSB / 8;              // its bytes
   constexpr bool VWORDS = VBB % 4 == 0;
   __shared__ float s_bk[16], s_bv[16];
-  __shared__ uint8_t s_gk[kTqCells + 1], s_gv[kTqCells + 1];
+  __shared__ uint2 s_gk[kTqCells + 1], s_gv[kTqCells + 1];
   __shared__ int s_ok[2];
   const Geometry& G = a.geo;
   if (threadIdx.x < 16) {
