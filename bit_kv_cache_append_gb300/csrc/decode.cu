@@ -74,18 +74,20 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(DecodeArgs a, i
   if (!ok && threadIdx.x == 0) set_error(a.tab.err_flag, kErrTimeout);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= G.gqa) return;
-  pdl_wait_primary();  // the split partials are complete and visible from here on
+  // what does not read the partials comes before the wait: the unit's slot
+  // count (two 64-bit divisions) and the exact states' max (shared memory)
   const int j = warp;
   const int row = b * G.Hq + h * G.gqa + j;
   const int ns = slots_of_unit(a, u);
   const float* ml = a.part_ml + static_cast<size_t>(row) * a.ns * 2;
   const float* rj = red + j * (D + 2);  // warp w's state at rj + w * kMaxGqa * (D + 2)
-  // the exact states' max first (shared memory), then the split partials in
-  // chunks of four slots whose loads are all issued before any is used: the
-  // running max only grows, the sums so far are rescaled when it does
   float M = lane < NW ? rj[lane * kMaxGqa * (D + 2) + D] : -INFINITY;
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  pdl_wait_primary();  // the split partials are complete and visible from here on
+  // the split partials in chunks of four slots whose loads are all issued
+  // before any is used: the running max only grows, the sums so far are
+  // rescaled when it does
   float L = 0.0f, oq[NS], oe[NS];
 #pragma unroll
   for (int i = 0; i < NS; ++i) oq[i] = oe[i] = 0.0f;
